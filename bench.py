@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark of the fused submanifold sparse 3-D convolution hot path.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+the neighbour-map build from voxel coordinates (hash clear / insert / query)
+followed by the fused gather-GEMM-accumulate convolution, on the decoder-scale
+workload (3-thick shells of 12 random spheres in a 1024^3 grid, ~11.8 M
+voxels, K = 27, Ci = Co = 128, bf16 in/out, fp32 accumulation).
+
+Metric: TFLOP/s = 2 * valid_pairs * Ci * Co / time (whole job, all ranks).
+Inputs are resident in HBM when the timed region starts; they are larger
+than L2 (129 MB), so no flush is needed between steps.  ``e2e`` repeats the
+measurement through the public API with pinned host buffers, host<->device
+copies inside the timed region.  ``roofline`` reports the convolution
+kernel's achieved FLOP/s against the measured dense bf16 tensor peak.
+``cpu_baseline`` times the CPU oracle on a bounded sample of the workload.
+
+``--impl reference`` times the CPU oracle alone (the reference arm: there is
+no runnable reference implementation of this path on these machines).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "submconv3d TFLOP/s (2·valid_pairs·Ci·Co) & voxels/s; % of bf16 tensor roofline"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+DOMINANT_KERNEL = "submconv_tc_kernel<Bf16Traits>"
+KERNEL_SOURCES = ("submanifold_voxel_gather_gb300/csrc/conv_tc.cu",
+                  "submanifold_voxel_gather_gb300/csrc/ptx.cuh")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decoder")
+    ap.add_argument("--layer", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="approximate CPU work of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh).get(DOMINANT_KERNEL, {})
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != kernel_source_hash() or rec.get("workload") != workload:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_id):
+        self.device_id = device_id
+        self.proc = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.device_id is not None:
+            cmd += ["-i", str(self.device_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, power = [], [], set(), []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def smi_device_id(torch, dev):
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        return None
+
+
+def build_workload(name, layer_index):
+    import workloads as W
+    t0 = time.time()
+    wl = W.make(name)
+    return wl, wl.layers[layer_index], time.time() - t0
+
+
+def to_device(torch, arr, dtype, dev):
+    a = np.ascontiguousarray(arr)
+    if dtype == "bf16":
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(a).to(dev)
+
+
+def host_pinned(torch, arr, dtype):
+    a = np.ascontiguousarray(arr)
+    t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if dtype == "bf16" else torch.from_numpy(a)
+    return t.pin_memory()
+
+
+# --------------------------------------------------------------------- oracle
+_PER_ROW_S = None
+
+
+def oracle_step(wl, layer, seconds, threads, seed):
+    """One bounded oracle pass over a seeded sample of output rows: the
+    neighbour-map rows (sort of all N voxels + binary searches) and the fp64
+    conv loop nest of those rows, sized for about ``seconds`` of work on
+    ``threads`` threads.  Returns (flops, timed seconds, rows)."""
+    global _PER_ROW_S
+    import oracle
+    import workloads as W
+    n = wl.N
+
+    def conv_rows(sub, rows, nthreads):
+        full = np.full((wl.K, n), n, dtype=np.int32)   # untimed: sampled columns only
+        full[:, rows] = sub
+        t0 = time.perf_counter()
+        oracle.conv(layer.feats, full, layer.w, layer.bias, layer.dtype, rows=rows, threads=nthreads)
+        return time.perf_counter() - t0
+
+    if _PER_ROW_S is None:   # untimed calibration
+        cal = np.unique((W.draws_u64(7, 1, 0, 64) % np.uint64(n)).astype(np.int64))
+        _PER_ROW_S = max(conv_rows(oracle.nmap_rows(wl.coords, wl.offsets, cal), cal, 1) / len(cal),
+                         1e-6)
+    count = int(max(256, min(n, seconds * threads / _PER_ROW_S)))
+    rows = np.unique((W.draws_u64(seed, 2, 0, count) % np.uint64(n)).astype(np.int64))
+    t0 = time.perf_counter()
+    sub = oracle.nmap_rows(wl.coords, wl.offsets, rows)
+    t_map = time.perf_counter() - t0
+    t_conv = conv_rows(sub, rows, threads)
+    pairs = int(((sub >= 0) & (sub < n)).sum())
+    return 2.0 * pairs * layer.Ci * layer.Co, t_map + t_conv, len(rows)
+
+
+# --------------------------------------------------------------------- arms
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    wl, layer, _ = build_workload(args.workload, args.layer)
+    threads = oracle.host_threads()
+    step_seconds = max(2.0, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        oracle_step(wl, layer, step_seconds, threads, seed=500 + i)
+    flops = secs = 0.0
+    rows_total = 0
+    for i in range(args.steps):
+        f, s, r = oracle_step(wl, layer, step_seconds, threads, seed=1000 + i)
+        flops += f
+        secs += s
+        rows_total += r
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": layer.dtype,
+        "data": "synthetic (seeded generator)",
+        "config": workload_config(wl, layer),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_total // args.steps} seeded output rows per step "
+                                   f"(neighbour map by sort + binary search, fp64 conv loop nest)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl, layer, pairs=None):
+    cfg = {"workload": f"decoder-scale: {wl.note}" if wl.name == "decoder" else f"{wl.name}: {wl.note}",
+           "N": wl.N, "K": wl.K, "Ci": layer.Ci, "Co": layer.Co, "seed": wl.seed,
+           "step": "build_nmap + submconv3d",
+           "l2": "inputs larger than L2 (no flush between steps)"}
+    if pairs is not None:
+        cfg["valid_pairs"] = pairs
+    return cfg
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    import submanifold_voxel_gather_gb300 as sv
+    sv.load_library()
+    wl, layer, gen_s = build_workload(args.workload, args.layer)
+    n, k, ci, co = wl.N, wl.K, layer.Ci, layer.Co
+    dtype = layer.dtype
+
+    coords = torch.from_numpy(wl.coords).to(dev)
+    feats = to_device(torch, layer.feats, dtype, dev)
+    w = to_device(torch, layer.w, dtype, dev)
+    bias = to_device(torch, layer.bias, dtype, dev)
+    nmap = torch.empty((k, n), dtype=torch.int32, device=dev)
+    out = torch.empty((n, co), dtype=feats.dtype, device=dev)
+    ws = torch.empty(sv.workspace_size(n), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    tf = "tf32" if dtype == "tf32" else None
+
+    def step():
+        sv.build_nmap(coords, workspace=ws, out=nmap)
+        sv.submconv3d(feats, nmap, w, bias, out=out, dtype=tf)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    sv.device_status()
+    pairs = sv.count_valid_pairs(nmap)
+    flops = 2.0 * pairs * ci * co
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(smi_device_id(torch, dev))
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    t_start.record(stream)
+    for i in range(args.steps):
+        sv.build_nmap(coords, workspace=ws, out=nmap)
+        ev[i][0].record(stream)
+        sv.submconv3d(feats, nmap, w, bias, out=out, dtype=tf)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    conv_ms = [a.elapsed_time(b) for a, b in ev]
+    conv_avg_ms = sum(conv_ms) / len(conv_ms)
+    if pg is not None:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+        pg.barrier()
+    sv.device_status()
+    ms_per_step = total_ms / args.steps
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_coords = torch.from_numpy(wl.coords).pin_memory()
+        h_feats = host_pinned(torch, layer.feats, dtype)
+        h_w = host_pinned(torch, layer.w, dtype)
+        h_bias = host_pinned(torch, layer.bias, dtype)
+        h_out = torch.empty((n, co), dtype=feats.dtype).pin_memory()
+        d_coords = torch.empty_like(coords)
+        d_feats = torch.empty_like(feats)
+        d_w = torch.empty_like(w)
+        d_bias = torch.empty_like(bias)
+
+        def e2e_step():
+            d_coords.copy_(h_coords, non_blocking=True)
+            d_feats.copy_(h_feats, non_blocking=True)
+            d_w.copy_(h_w, non_blocking=True)
+            d_bias.copy_(h_bias, non_blocking=True)
+            sv.build_nmap(d_coords, workspace=ws, out=nmap)
+            sv.submconv3d(d_feats, nmap, d_w, d_bias, out=out, dtype=tf)
+            h_out.copy_(out, non_blocking=True)
+
+        for _ in range(max(1, min(args.warmup, 2))):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if pg is not None:
+            pg.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1)
+        if pg is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = sum(t.numel() * t.element_size() for t in (h_coords, h_feats, h_w, h_bias))
+        d2h = h_out.numel() * h_out.element_size()
+        e2e = {"value": world * flops / (e2e_ms / args.steps * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms / args.steps}
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return 0
+
+    bf16_peak, hbm_peak, peak_kind = peaks()
+    achieved = flops / (conv_avg_ms * 1e-3) / 1e12
+    elem = 2 if dtype == "bf16" else 4
+    comp_bytes = n * ci * elem + n * co * elem + 4 * k * n + k * ci * co * elem + co * elem
+    t_roof_ms = max(flops / (bf16_peak * 1e12), comp_bytes / (hbm_peak * 1e9)) * 1e3
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": achieved / bf16_peak, "traffic": recorded_traffic(args.workload),
+                "kernel": DOMINANT_KERNEL, "peak_source": f"{peak_kind} bf16 dense (burst)",
+                "algorithmic_flops_per_launch": flops, "conv_ms": conv_avg_ms,
+                "compulsory_bytes": comp_bytes, "t_roof_ms": t_roof_ms,
+                "frac_of_roofline": t_roof_ms / conv_avg_ms}
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        import oracle
+        threads = oracle.host_threads()
+        f, s, r = oracle_step(wl, layer, args.cpu_seconds, threads, seed=99)
+        cpu = {"value": f / s / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{r} seeded output rows of the same workload: neighbour map by sort + "
+                         f"binary search over all N voxels, fp64 conv loop nest over the sample; "
+                         f"{s:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": world * flops / (ms_per_step * 1e-3) / 1e12, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+        "data": "synthetic (seeded generator; decoder-scale voxel shells, random-init weights)",
+        "config": workload_config(wl, layer, pairs),
+        "voxels_per_s": world * n / (ms_per_step * 1e-3),
+        "conv_tflops": achieved,
+        "build_ms": ms_per_step - conv_avg_ms,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "generation_s": gen_s,
+    }
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -78,6 +78,8 @@ def _load():
             i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
             lib.oracle_build_nmap.argtypes = [vp, i64, vp, i32, vp]
             lib.oracle_build_nmap.restype = ctypes.c_int
+            lib.oracle_nmap_rows.argtypes = [vp, i64, vp, i32, vp, i64, vp]
+            lib.oracle_nmap_rows.restype = ctypes.c_int
             lib.oracle_conv.argtypes = [vp, i32, vp, vp, vp, i64, i32, i32, i32, vp, i64, vp, vp]
             lib.oracle_conv.restype = ctypes.c_int
             lib.oracle_count_valid_pairs.argtypes = [vp, i64, i32]
@@ -101,6 +103,21 @@ def build_nmap(coords: np.ndarray, offsets: np.ndarray) -> np.ndarray:
     if rc != OK:
         raise OracleError(rc, "build_nmap")
     return nmap
+
+
+def nmap_rows(coords: np.ndarray, offsets: np.ndarray, rows) -> np.ndarray:
+    """Columns ``rows`` of the neighbour map: (K, len(rows)) int32, entry
+    [k, r] = nmap[k, rows[r]] (the full table is still sorted)."""
+    lib = _load()
+    coords = np.ascontiguousarray(coords, dtype=np.int32).reshape(-1, 3)
+    offsets = np.ascontiguousarray(offsets, dtype=np.int32).reshape(-1, 3)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    N, K = coords.shape[0], offsets.shape[0]
+    out = np.empty((K, rows.shape[0]), dtype=np.int32)
+    rc = lib.oracle_nmap_rows(_ptr(coords), N, _ptr(offsets), K, _ptr(rows), rows.shape[0], _ptr(out))
+    if rc != OK:
+        raise OracleError(rc, "nmap_rows")
+    return out
 
 
 def conv(feats: np.ndarray, nmap: np.ndarray, w: np.ndarray, bias, dtype: str,

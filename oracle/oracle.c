@@ -68,21 +68,16 @@ static int oracle_cmp_entry(const void* a, const void* b)
     return (ka > kb) - (ka < kb);
 }
 
-/* Neighbour map by sort + binary search.  Returns ORACLE_OK or an error. */
-int oracle_build_nmap(const int32_t* coords, int64_t N, const int32_t* offsets, int32_t K,
-                      int32_t* nmap)
+/* Sorted (key, index) table of all voxels; NULL on allocation failure.
+ * *status is set to ORACLE_ERR_DUPLICATE_COORD when two voxels share a key. */
+static oracle_entry* oracle_sorted_table(const int32_t* coords, int64_t N, int* status)
 {
-    if (N < 0 || K < 1 || (N > 0 && (coords == NULL || nmap == NULL)) || offsets == NULL)
-        return ORACLE_ERR_INVALID_ARG;
-    if (N >= INT32_MAX) return ORACLE_ERR_INVALID_ARG;
-    if (N == 0) return ORACLE_OK;
-
-    for (int64_t n = 0; n < N; ++n)
-        for (int c = 0; c < 3; ++c)
-            if (!oracle_in_range(coords[3 * n + c])) return ORACLE_ERR_INVALID_ARG;
-
     oracle_entry* table = (oracle_entry*)malloc((size_t)N * sizeof(oracle_entry));
-    if (table == NULL) return ORACLE_ERR_NOMEM;
+    *status = ORACLE_OK;
+    if (table == NULL) {
+        *status = ORACLE_ERR_NOMEM;
+        return NULL;
+    }
     for (int64_t n = 0; n < N; ++n) {
         table[n].key = oracle_pack(coords[3 * n], coords[3 * n + 1], coords[3 * n + 2]);
         table[n].index = n;
@@ -91,27 +86,75 @@ int oracle_build_nmap(const int32_t* coords, int64_t N, const int32_t* offsets, 
     for (int64_t i = 1; i < N; ++i) {
         if (table[i].key == table[i - 1].key) {
             free(table);
-            return ORACLE_ERR_DUPLICATE_COORD;
+            *status = ORACLE_ERR_DUPLICATE_COORD;
+            return NULL;
         }
     }
+    return table;
+}
 
-    for (int64_t n = 0; n < N; ++n) {
-        for (int32_t k = 0; k < K; ++k) {
-            int64_t z = (int64_t)coords[3 * n] + offsets[3 * k];
-            int64_t y = (int64_t)coords[3 * n + 1] + offsets[3 * k + 1];
-            int64_t x = (int64_t)coords[3 * n + 2] + offsets[3 * k + 2];
-            int32_t found = (int32_t)N;
-            if (oracle_in_range(z) && oracle_in_range(y) && oracle_in_range(x)) {
-                oracle_entry probe;
-                probe.key = oracle_pack(z, y, x);
-                probe.index = 0;
-                const oracle_entry* hit = (const oracle_entry*)bsearch(
-                    &probe, table, (size_t)N, sizeof(oracle_entry), oracle_cmp_entry);
-                if (hit != NULL) found = (int32_t)hit->index;
-            }
-            nmap[(size_t)k * (size_t)N + (size_t)n] = found;
-        }
-    }
+/* Index of the voxel at coords[n] + offsets[k], or N. */
+static int32_t oracle_neighbour(const oracle_entry* table, const int32_t* coords, int64_t N,
+                                const int32_t* offsets, int64_t n, int32_t k)
+{
+    int64_t z = (int64_t)coords[3 * n] + offsets[3 * k];
+    int64_t y = (int64_t)coords[3 * n + 1] + offsets[3 * k + 1];
+    int64_t x = (int64_t)coords[3 * n + 2] + offsets[3 * k + 2];
+    if (!(oracle_in_range(z) && oracle_in_range(y) && oracle_in_range(x))) return (int32_t)N;
+    oracle_entry probe;
+    probe.key = oracle_pack(z, y, x);
+    probe.index = 0;
+    const oracle_entry* hit = (const oracle_entry*)bsearch(&probe, table, (size_t)N,
+                                                           sizeof(oracle_entry), oracle_cmp_entry);
+    return hit != NULL ? (int32_t)hit->index : (int32_t)N;
+}
+
+static int oracle_check_coords(const int32_t* coords, int64_t N)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int c = 0; c < 3; ++c)
+            if (!oracle_in_range(coords[3 * n + c])) return ORACLE_ERR_INVALID_ARG;
+    return ORACLE_OK;
+}
+
+/* Neighbour map by sort + binary search: nmap is (K, N).  Returns ORACLE_OK
+ * or an error. */
+int oracle_build_nmap(const int32_t* coords, int64_t N, const int32_t* offsets, int32_t K,
+                      int32_t* nmap)
+{
+    if (N < 0 || K < 1 || (N > 0 && (coords == NULL || nmap == NULL)) || offsets == NULL)
+        return ORACLE_ERR_INVALID_ARG;
+    if (N >= INT32_MAX) return ORACLE_ERR_INVALID_ARG;
+    if (N == 0) return ORACLE_OK;
+    int status = oracle_check_coords(coords, N);
+    if (status != ORACLE_OK) return status;
+    oracle_entry* table = oracle_sorted_table(coords, N, &status);
+    if (table == NULL) return status;
+    for (int64_t n = 0; n < N; ++n)
+        for (int32_t k = 0; k < K; ++k)
+            nmap[(size_t)k * (size_t)N + (size_t)n] = oracle_neighbour(table, coords, N, offsets, n, k);
+    free(table);
+    return ORACLE_OK;
+}
+
+/* The same map restricted to the voxels rows[0 .. n_rows): out is (K, n_rows),
+ * out[k, r] = nmap[k, rows[r]]. */
+int oracle_nmap_rows(const int32_t* coords, int64_t N, const int32_t* offsets, int32_t K,
+                     const int64_t* rows, int64_t n_rows, int32_t* out)
+{
+    if (N < 1 || K < 1 || coords == NULL || offsets == NULL || rows == NULL || out == NULL ||
+        n_rows < 0 || N >= INT32_MAX)
+        return ORACLE_ERR_INVALID_ARG;
+    for (int64_t r = 0; r < n_rows; ++r)
+        if (rows[r] < 0 || rows[r] >= N) return ORACLE_ERR_INVALID_ARG;
+    int status = oracle_check_coords(coords, N);
+    if (status != ORACLE_OK) return status;
+    oracle_entry* table = oracle_sorted_table(coords, N, &status);
+    if (table == NULL) return status;
+    for (int64_t r = 0; r < n_rows; ++r)
+        for (int32_t k = 0; k < K; ++k)
+            out[(size_t)k * (size_t)n_rows + (size_t)r] =
+                oracle_neighbour(table, coords, N, offsets, rows[r], k);
     free(table);
     return ORACLE_OK;
 }

@@ -1,0 +1,47 @@
+// Internal launchers shared between the C ABI and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "spconv.h"
+
+namespace spconv {
+
+// Records `msg` as the calling thread's last error and returns `code`.
+spconv_status fail(spconv_status code, const std::string& msg);
+
+// Checks a CUDA runtime result; on failure records it and returns false.
+bool cuda_ok(cudaError_t err, const char* what, spconv_status* out);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// ---- neighbour map (nmap_hash.cu)
+struct BuildOffsets {
+  int32_t d[3 * SPCONV_MAX_BUILD_OFFSETS];
+};
+
+size_t hash_capacity(int64_t n);
+spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOffsets& offs,
+                                int32_t k, int32_t* nmap, void* workspace, cudaStream_t stream);
+spconv_status launch_count_valid_pairs(const int32_t* nmap, int64_t n, int32_t k, int64_t* count,
+                                       cudaStream_t stream);
+
+// ---- exact fp32 convolution on CUDA cores (conv_simt.cu)
+spconv_status launch_conv_simt_f32(const float* feats, const int32_t* nmap, const float* w,
+                                   const float* bias, float* out, int64_t n, int32_t k,
+                                   int32_t ci, int32_t co, cudaStream_t stream);
+
+// ---- tensor-core convolution (conv_tc.cu); dtype is SPCONV_BF16 or SPCONV_TF32
+spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_t* nmap,
+                             const void* w, const void* bias, void* out, int64_t n, int32_t k,
+                             int32_t ci, int32_t co, cudaStream_t stream);
+
+// ---- device error word (ptx.cuh declares the symbol)
+spconv_status read_and_clear_device_error(cudaStream_t stream, unsigned int* bits);
+
+}  // namespace spconv

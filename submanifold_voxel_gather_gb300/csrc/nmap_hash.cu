@@ -1,0 +1,199 @@
+// GPU neighbour-map builder: open-addressing hash of voxel coordinates.
+//
+// The page "sparse_conv_metal.py" (trellis-2-mrp-mlx) consumes a (K, N) int32
+// map whose entry [k, n] is the row of the voxel at coords[n] + offsets[k]
+// and N where there is none (wrapper docstring, kernel body); it takes the
+// map as given.  This file builds it:
+//
+//   clear   every slot's key := EMPTY, error flags := 0
+//   insert  one thread per voxel: linear probing with a 64-bit atomicCAS on
+//           the packed key (21 bits per axis); an equal key already present
+//           flags a duplicate coordinate
+//   query   one thread per voxel, loop over the K offsets: probe for the
+//           shifted key (one 16-byte load per probe), write nmap[k, n] with
+//           coalesced stores across the warp
+//
+// Capacity is the next power of two >= 2N (load factor <= 1/2), so probe
+// sequences are short; every probe loop is still bounded by the capacity.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace spconv {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr unsigned long long kEmptyKey = ~0ull;
+constexpr size_t kFlagBytes = 256;
+
+enum : int { kFlagDuplicate = 1, kFlagRange = 2, kFlagFull = 4 };
+
+struct alignas(16) Slot {
+  unsigned long long key;
+  int32_t val;
+  int32_t pad;
+};
+
+__device__ __forceinline__ unsigned long long pack_coord(int z, int y, int x) {
+  return (static_cast<unsigned long long>(z) << 42) | (static_cast<unsigned long long>(y) << 21) |
+         static_cast<unsigned long long>(x);
+}
+
+// 64-bit finaliser of MurmurHash3 (Austin Appleby, public domain).
+__device__ __forceinline__ unsigned long long mix_hash(unsigned long long k) {
+  k ^= k >> 33;
+  k *= 0xff51afd7ed558ccdull;
+  k ^= k >> 33;
+  k *= 0xc4ceb9fe1a85ec53ull;
+  k ^= k >> 33;
+  return k;
+}
+
+__device__ __forceinline__ bool in_grid(int v) {
+  return v >= 0 && v < SPCONV_COORD_LIMIT;
+}
+
+__global__ void hash_clear_kernel(Slot* table, unsigned long long cap, int* flags) {
+  const unsigned long long stride = static_cast<unsigned long long>(gridDim.x) * blockDim.x;
+  for (unsigned long long i = static_cast<unsigned long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+       i < cap; i += stride) {
+    table[i].key = kEmptyKey;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *flags = 0;
+}
+
+__global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n, Slot* table,
+                                   unsigned long long mask, int* flags) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int z = coords[3 * i], y = coords[3 * i + 1], x = coords[3 * i + 2];
+  if (!in_grid(z) || !in_grid(y) || !in_grid(x)) {
+    atomicOr(flags, kFlagRange);
+    return;
+  }
+  const unsigned long long key = pack_coord(z, y, x);
+  unsigned long long h = mix_hash(key) & mask;
+  for (unsigned long long probe = 0; probe <= mask; ++probe) {
+    const unsigned long long prev = atomicCAS(&table[h].key, kEmptyKey, key);
+    if (prev == kEmptyKey) {
+      table[h].val = static_cast<int32_t>(i);
+      return;
+    }
+    if (prev == key) {
+      atomicOr(flags, kFlagDuplicate);
+      return;
+    }
+    h = (h + 1) & mask;
+  }
+  atomicOr(flags, kFlagFull);
+}
+
+__global__ void __launch_bounds__(kThreads)
+    nmap_query_kernel(const int32_t* __restrict__ coords, int64_t n, const Slot* __restrict__ table,
+                      unsigned long long mask, const BuildOffsets offs, int32_t k_count,
+                      int32_t* __restrict__ nmap) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int z = coords[3 * i], y = coords[3 * i + 1], x = coords[3 * i + 2];
+  const int32_t missing = static_cast<int32_t>(n);
+  for (int32_t k = 0; k < k_count; ++k) {
+    const int qz = z + offs.d[3 * k], qy = y + offs.d[3 * k + 1], qx = x + offs.d[3 * k + 2];
+    int32_t found = missing;
+    if (in_grid(qz) && in_grid(qy) && in_grid(qx)) {
+      const unsigned long long key = pack_coord(qz, qy, qx);
+      unsigned long long h = mix_hash(key) & mask;
+      for (unsigned long long probe = 0; probe <= mask; ++probe) {
+        const int4 s = __ldg(reinterpret_cast<const int4*>(table + h));
+        const unsigned long long sk =
+            (static_cast<unsigned long long>(static_cast<uint32_t>(s.y)) << 32) |
+            static_cast<uint32_t>(s.x);
+        if (sk == key) {
+          found = s.z;
+          break;
+        }
+        if (sk == kEmptyKey) break;
+        h = (h + 1) & mask;
+      }
+    }
+    nmap[static_cast<int64_t>(k) * n + i] = found;
+  }
+}
+
+__global__ void count_valid_kernel(const int32_t* __restrict__ nmap, int64_t total, int64_t n,
+                                   unsigned long long* count) {
+  unsigned long long local = 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int32_t v = nmap[i];
+    local += (v >= 0 && v < n) ? 1u : 0u;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) local += __shfl_down_sync(0xffffffffu, local, off);
+  if ((threadIdx.x & 31) == 0 && local != 0) atomicAdd(count, local);
+}
+
+__global__ void zero_u64_kernel(unsigned long long* p) { *p = 0; }
+
+}  // namespace
+
+size_t hash_capacity(int64_t n) {
+  size_t cap = 64;
+  while (cap < static_cast<size_t>(2 * n)) cap <<= 1;
+  return cap;
+}
+
+spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOffsets& offs,
+                                int32_t k, int32_t* nmap, void* workspace, cudaStream_t stream) {
+  const size_t cap = hash_capacity(n);
+  int* flags = static_cast<int*>(workspace);
+  Slot* table = reinterpret_cast<Slot*>(static_cast<char*>(workspace) + kFlagBytes);
+  const int sms = sm_count();
+  if (sms <= 0) return fail(SPCONV_ERR_CUDA, "could not query the SM count");
+  spconv_status st = SPCONV_OK;
+
+  const unsigned long long clear_blocks = (cap + kThreads - 1) / kThreads;
+  const unsigned clear_grid =
+      static_cast<unsigned>(clear_blocks < 16ull * sms ? clear_blocks : 16ull * sms);
+  hash_clear_kernel<<<clear_grid, kThreads, 0, stream>>>(table, cap, flags);
+  if (!cuda_ok(cudaGetLastError(), "hash_clear_kernel launch", &st)) return st;
+
+  const unsigned grid = static_cast<unsigned>((n + kThreads - 1) / kThreads);
+  hash_insert_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, flags);
+  if (!cuda_ok(cudaGetLastError(), "hash_insert_kernel launch", &st)) return st;
+
+  nmap_query_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, offs, k, nmap);
+  if (!cuda_ok(cudaGetLastError(), "nmap_query_kernel launch", &st)) return st;
+
+  int host_flags = 0;
+  if (!cuda_ok(cudaMemcpyAsync(&host_flags, flags, sizeof(int), cudaMemcpyDeviceToHost, stream),
+               "flag readback", &st))
+    return st;
+  if (!cuda_ok(cudaStreamSynchronize(stream), "cudaStreamSynchronize", &st)) return st;
+  if (host_flags & kFlagRange)
+    return fail(SPCONV_ERR_INVALID_ARG, "a coordinate lies outside [0, 2^20)");
+  if (host_flags & kFlagDuplicate)
+    return fail(SPCONV_ERR_DUPLICATE_COORD, "two voxels share a coordinate");
+  if (host_flags & kFlagFull) return fail(SPCONV_ERR_DEVICE, "hash table overflow");
+  return SPCONV_OK;
+}
+
+spconv_status launch_count_valid_pairs(const int32_t* nmap, int64_t n, int32_t k, int64_t* count,
+                                       cudaStream_t stream) {
+  spconv_status st = SPCONV_OK;
+  unsigned long long* c = reinterpret_cast<unsigned long long*>(count);
+  zero_u64_kernel<<<1, 1, 0, stream>>>(c);
+  if (!cuda_ok(cudaGetLastError(), "zero kernel launch", &st)) return st;
+  const int64_t total = static_cast<int64_t>(k) * n;
+  if (total == 0) return SPCONV_OK;
+  const int sms = sm_count();
+  if (sms <= 0) return fail(SPCONV_ERR_CUDA, "could not query the SM count");
+  const int64_t blocks = (total + kThreads - 1) / kThreads;
+  const unsigned grid = static_cast<unsigned>(blocks < 8ll * sms ? blocks : 8ll * sms);
+  count_valid_kernel<<<grid, kThreads, 0, stream>>>(nmap, total, n, c);
+  if (!cuda_ok(cudaGetLastError(), "count_valid_kernel launch", &st)) return st;
+  return SPCONV_OK;
+}
+
+}  // namespace spconv

@@ -1,0 +1,182 @@
+// C ABI of the library (declared in include/spconv.h): argument validation,
+// device checks and dispatch to the kernels.  Validation comes first and
+// nothing is enqueued when it fails.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+#include "spconv.h"
+
+namespace spconv {
+
+namespace {
+
+thread_local std::string t_last_error;
+
+constexpr int kMaxDevices = 64;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The kernels are built for sm_103a only; anything else fails loudly here
+// rather than with a missing-image launch error.
+spconv_status check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess)
+    return fail(SPCONV_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  static int checked[kMaxDevices] = {0};  // 0 unknown, 1 ok, -1 unsupported
+  if (dev >= 0 && dev < kMaxDevices && checked[dev] == 1) return SPCONV_OK;
+  int major = 0, minor = 0;
+  e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e != cudaSuccess)
+    return fail(SPCONV_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+  if (major != 10 || minor != 3) {
+    if (dev >= 0 && dev < kMaxDevices) checked[dev] = -1;
+    return fail(SPCONV_ERR_UNSUPPORTED, "device " + std::to_string(dev) + " has compute capability " +
+                                            std::to_string(major) + "." + std::to_string(minor) +
+                                            "; this library is built for 10.3 (sm_103a) only");
+  }
+  if (dev >= 0 && dev < kMaxDevices) checked[dev] = 1;
+  return SPCONV_OK;
+}
+
+spconv_status ok() {
+  t_last_error.clear();
+  return SPCONV_OK;
+}
+
+}  // namespace
+
+spconv_status fail(spconv_status code, const std::string& msg) {
+  t_last_error = msg;
+  return code;
+}
+
+bool cuda_ok(cudaError_t err, const char* what, spconv_status* out) {
+  if (err == cudaSuccess) return true;
+  *out = fail(SPCONV_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(err));
+  return false;
+}
+
+int sm_count() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev] = n;
+  return n;
+}
+
+}  // namespace spconv
+
+using spconv::fail;
+
+extern "C" {
+
+int spconv_version(void) { return SPCONV_VERSION; }
+
+const char* spconv_last_error(void) { return spconv::t_last_error.c_str(); }
+
+size_t spconv_build_nmap_workspace_size(int64_t N) {
+  if (N < 0) return 0;
+  return 256 + spconv::hash_capacity(N) * 16;
+}
+
+spconv_status spconv_build_nmap(const int32_t* coords_dev, int64_t N, const int32_t* offsets_host,
+                                int32_t K, int32_t* nmap_dev, void* workspace_dev,
+                                size_t workspace_bytes, void* stream) {
+  if (N < 0 || N >= INT32_MAX) return fail(SPCONV_ERR_INVALID_ARG, "N must satisfy 0 <= N < 2^31-1");
+  if (K < 1 || K > SPCONV_MAX_BUILD_OFFSETS)
+    return fail(SPCONV_ERR_INVALID_ARG, "K must satisfy 1 <= K <= SPCONV_MAX_BUILD_OFFSETS");
+  if (offsets_host == nullptr) return fail(SPCONV_ERR_INVALID_ARG, "offsets_host is NULL");
+  if (N == 0) return spconv::ok();
+  if (coords_dev == nullptr || nmap_dev == nullptr || workspace_dev == nullptr)
+    return fail(SPCONV_ERR_INVALID_ARG, "coords, nmap and workspace must be non-NULL");
+  if (!spconv::aligned(coords_dev, 4) || !spconv::aligned(nmap_dev, 4))
+    return fail(SPCONV_ERR_INVALID_ARG, "coords and nmap must be 4-byte aligned");
+  if (!spconv::aligned(workspace_dev, 256))
+    return fail(SPCONV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (workspace_bytes < spconv_build_nmap_workspace_size(N))
+    return fail(SPCONV_ERR_WORKSPACE, "workspace smaller than spconv_build_nmap_workspace_size(N)");
+  for (int32_t i = 0; i < 3 * K; ++i) {
+    const int32_t d = offsets_host[i];
+    if (d <= -SPCONV_COORD_LIMIT || d >= SPCONV_COORD_LIMIT)
+      return fail(SPCONV_ERR_INVALID_ARG, "offset component out of range");
+  }
+  spconv_status st = spconv::check_device();
+  if (st != SPCONV_OK) return st;
+  spconv::BuildOffsets offs;
+  std::memset(&offs, 0, sizeof offs);
+  std::memcpy(offs.d, offsets_host, sizeof(int32_t) * 3 * static_cast<size_t>(K));
+  st = spconv::launch_build_nmap(coords_dev, N, offs, K, nmap_dev, workspace_dev,
+                                 static_cast<cudaStream_t>(stream));
+  return st == SPCONV_OK ? spconv::ok() : st;
+}
+
+spconv_status spconv_submconv3d(const void* feats_dev, const int32_t* nmap_dev, const void* w_dev,
+                                const void* bias_dev, void* out_dev, int64_t N, int32_t K,
+                                int32_t Ci, int32_t Co, spconv_dtype dtype, void* stream) {
+  if (N < 0 || N >= INT32_MAX) return fail(SPCONV_ERR_INVALID_ARG, "N must satisfy 0 <= N < 2^31-1");
+  if (K < 1 || Ci < 1 || Co < 1) return fail(SPCONV_ERR_INVALID_ARG, "K, Ci and Co must be >= 1");
+  if (dtype != SPCONV_F32 && dtype != SPCONV_TF32 && dtype != SPCONV_BF16)
+    return fail(SPCONV_ERR_INVALID_ARG, "unknown dtype");
+  if (N == 0) return spconv::ok();
+  if (feats_dev == nullptr || nmap_dev == nullptr || w_dev == nullptr || out_dev == nullptr)
+    return fail(SPCONV_ERR_INVALID_ARG, "feats, nmap, w and out must be non-NULL");
+  if (!spconv::aligned(nmap_dev, 4)) return fail(SPCONV_ERR_INVALID_ARG, "nmap must be 4-byte aligned");
+  const size_t elem = dtype == SPCONV_BF16 ? 2 : 4;
+  if (static_cast<uint64_t>(N) * static_cast<uint64_t>(K) > (1ull << 40))
+    return fail(SPCONV_ERR_UNSUPPORTED, "K * N too large");
+  if (dtype == SPCONV_F32) {
+    if (!spconv::aligned(feats_dev, 4) || !spconv::aligned(w_dev, 4) || !spconv::aligned(out_dev, 4) ||
+        (bias_dev != nullptr && !spconv::aligned(bias_dev, 4)))
+      return fail(SPCONV_ERR_INVALID_ARG, "fp32 arrays must be 4-byte aligned");
+  } else {
+    if (Ci % 16 != 0 || Co % 16 != 0)
+      return fail(SPCONV_ERR_UNSUPPORTED, "bf16/tf32 need Ci and Co to be multiples of 16");
+    if (!spconv::aligned(feats_dev, 16) || !spconv::aligned(w_dev, 16) || !spconv::aligned(out_dev, 16))
+      return fail(SPCONV_ERR_INVALID_ARG, "feats, w and out must be 16-byte aligned");
+    if (bias_dev != nullptr && !spconv::aligned(bias_dev, elem))
+      return fail(SPCONV_ERR_INVALID_ARG, "bias is misaligned");
+  }
+  spconv_status st = spconv::check_device();
+  if (st != SPCONV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == SPCONV_F32)
+    st = spconv::launch_conv_simt_f32(static_cast<const float*>(feats_dev), nmap_dev,
+                                      static_cast<const float*>(w_dev),
+                                      static_cast<const float*>(bias_dev), static_cast<float*>(out_dev),
+                                      N, K, Ci, Co, s);
+  else
+    st = spconv::launch_conv_tc(dtype, feats_dev, nmap_dev, w_dev, bias_dev, out_dev, N, K, Ci, Co, s);
+  return st == SPCONV_OK ? spconv::ok() : st;
+}
+
+spconv_status spconv_count_valid_pairs(const int32_t* nmap_dev, int64_t N, int32_t K,
+                                       int64_t* count_dev, void* stream) {
+  if (N < 0 || N >= INT32_MAX || K < 1) return fail(SPCONV_ERR_INVALID_ARG, "bad N or K");
+  if (count_dev == nullptr || (N > 0 && nmap_dev == nullptr))
+    return fail(SPCONV_ERR_INVALID_ARG, "nmap and count must be non-NULL");
+  if (!spconv::aligned(count_dev, 8)) return fail(SPCONV_ERR_INVALID_ARG, "count must be 8-byte aligned");
+  spconv_status st = spconv::check_device();
+  if (st != SPCONV_OK) return st;
+  st = spconv::launch_count_valid_pairs(nmap_dev, N, K, count_dev, static_cast<cudaStream_t>(stream));
+  return st == SPCONV_OK ? spconv::ok() : st;
+}
+
+spconv_status spconv_device_status(void* stream) {
+  unsigned int bits = 0;
+  spconv_status st = spconv::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &bits);
+  if (st != SPCONV_OK) return st;
+  if (bits != 0) return fail(SPCONV_ERR_DEVICE, "device error bits 0x" + std::to_string(bits));
+  return spconv::ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,99 @@
+"""The C ABI library on a machine without a GPU: it builds, loads, exports
+every function include/spconv.h declares, and rejects bad arguments before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import submanifold_voxel_gather_gb300 as sv
+from submanifold_voxel_gather_gb300 import build as svbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spconv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    svbuild.build()
+    return sv.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spconv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("spconv_build_nmap", "spconv_submconv3d", "spconv_build_nmap_workspace_size",
+                     "spconv_last_error", "spconv_version", "spconv_count_valid_pairs",
+                     "spconv_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version_and_workspace_size(lib):
+    assert sv.version() == 1
+    assert sv.workspace_size(-1) == 0
+    assert sv.workspace_size(0) == 256 + 64 * 16
+    assert sv.workspace_size(32) == 256 + 64 * 16
+    assert sv.workspace_size(33) == 256 + 128 * 16
+    assert sv.workspace_size(11_773_199) == 256 + (1 << 25) * 16
+
+
+def _status(code):
+    return code, sv.load_library().spconv_last_error().decode()
+
+
+def test_argument_validation_without_gpu(lib):
+    offs = sv.default_offsets()
+    optr = offs.ctypes.data_as(ctypes.c_void_p)
+    fake = ctypes.c_void_p(0x100000)  # never dereferenced: validation fails first
+    # build_nmap
+    assert _status(lib.spconv_build_nmap(fake, -1, optr, 27, fake, fake, 1 << 30, None))[0] == -1
+    assert _status(lib.spconv_build_nmap(fake, 10, optr, 0, fake, fake, 1 << 30, None))[0] == -1
+    assert _status(lib.spconv_build_nmap(fake, 10, None, 27, fake, fake, 1 << 30, None))[0] == -1
+    assert _status(lib.spconv_build_nmap(None, 10, optr, 27, fake, fake, 1 << 30, None))[0] == -1
+    code, msg = _status(lib.spconv_build_nmap(fake, 10, optr, 27, fake, fake, 100, None))
+    assert code == -3 and "workspace" in msg
+    code, msg = _status(lib.spconv_build_nmap(fake, 10, optr, 27, fake, ctypes.c_void_p(0x100010),
+                                              1 << 30, None))
+    assert code == -1 and "256-byte" in msg
+    assert _status(lib.spconv_build_nmap(fake, 0, optr, 27, None, None, 0, None))[0] == 0
+    # submconv3d
+    assert _status(lib.spconv_submconv3d(fake, fake, fake, None, fake, -5, 27, 16, 16, 2, None))[0] == -1
+    assert _status(lib.spconv_submconv3d(fake, fake, fake, None, fake, 10, 0, 16, 16, 2, None))[0] == -1
+    assert _status(lib.spconv_submconv3d(fake, fake, fake, None, fake, 10, 27, 16, 16, 7, None))[0] == -1
+    code, msg = _status(lib.spconv_submconv3d(fake, fake, fake, None, fake, 10, 27, 24, 16, 2, None))
+    assert code == -2 and "multiples of 16" in msg
+    code, msg = _status(lib.spconv_submconv3d(ctypes.c_void_p(0x100008), fake, fake, None, fake, 10, 27,
+                                              16, 16, 2, None))
+    assert code == -1 and "aligned" in msg
+    assert _status(lib.spconv_submconv3d(None, fake, fake, None, fake, 10, 27, 16, 16, 0, None))[0] == -1
+    assert _status(lib.spconv_submconv3d(None, None, None, None, None, 0, 27, 16, 16, 2, None))[0] == 0
+    # count
+    assert _status(lib.spconv_count_valid_pairs(fake, 10, 27, None, None))[0] == -1
+
+
+def test_python_binding_rejects_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    with pytest.raises(TypeError):
+        sv.build_nmap(torch.zeros((4, 3), dtype=torch.int32))
+    with pytest.raises(TypeError):
+        sv.submconv3d(torch.zeros((4, 16)), torch.zeros((27, 4), dtype=torch.int32),
+                      torch.zeros((27, 16, 16)))
+
+
+def test_default_offsets_order():
+    offs = sv.default_offsets()
+    assert offs.shape == (27, 3)
+    for k, (dz, dy, dx) in enumerate(offs):
+        assert k == 9 * (dz + 1) + 3 * (dy + 1) + (dx + 1)

@@ -1,0 +1,106 @@
+"""GPU neighbour-map builder against the oracle: bit-exact."""
+import numpy as np
+import pytest
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import submanifold_voxel_gather_gb300 as mod
+    from submanifold_voxel_gather_gb300 import build
+    build.build()
+    return mod
+
+
+def gpu_nmap(sv, coords, offsets=None):
+    import torch
+    c = torch.from_numpy(np.ascontiguousarray(coords, dtype=np.int32)).cuda()
+    return sv.build_nmap(c, offsets).cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_shell1", "small"])
+def test_nmap_configs_exact(sv, oracle_mod, name):
+    coords = W.coords_only(name)
+    offs = W.offsets_3x3x3()
+    np.testing.assert_array_equal(gpu_nmap(sv, coords), oracle_mod.build_nmap(coords, offs))
+
+
+def test_nmap_shuffled_order_exact(sv, oracle_mod):
+    coords = W.coords_only("small")
+    coords = coords[W.permutation(len(coords), 1)]
+    np.testing.assert_array_equal(gpu_nmap(sv, coords), oracle_mod.build_nmap(coords, W.offsets_3x3x3()))
+
+
+@pytest.mark.parametrize("side,frac,seed", [(5, 1.0, 1), (12, 0.3, 2), (16, 0.05, 3)])
+def test_nmap_random_grids_exact(sv, oracle_mod, side, frac, seed):
+    coords = W.random_occupancy(side, frac, seed)
+    np.testing.assert_array_equal(gpu_nmap(sv, coords), oracle_mod.build_nmap(coords, W.offsets_3x3x3()))
+
+
+def test_nmap_edge_sizes_and_offsets(sv, oracle_mod):
+    base = W.random_occupancy(10, 0.4, 9)
+    for n in (1, 2, 127, 128, 129):
+        c = base[:n]
+        np.testing.assert_array_equal(gpu_nmap(sv, c), oracle_mod.build_nmap(c, W.offsets_3x3x3()))
+    centre = np.zeros((1, 3), np.int32)
+    np.testing.assert_array_equal(gpu_nmap(sv, base, centre), oracle_mod.build_nmap(base, centre))
+    wide = W.offsets_cube(2)
+    np.testing.assert_array_equal(gpu_nmap(sv, base, wide), oracle_mod.build_nmap(base, wide))
+    far = np.array([[5, -3, 2], [0, 0, 7], [-1, -1, -1]], np.int32)
+    np.testing.assert_array_equal(gpu_nmap(sv, base, far), oracle_mod.build_nmap(base, far))
+
+
+def test_nmap_grid_limits(sv, oracle_mod):
+    hi = (1 << 20) - 1
+    coords = np.array([[0, 0, 0], [hi, hi, hi], [0, hi, 0], [hi, 0, hi - 1], [hi, 0, hi]], np.int32)
+    np.testing.assert_array_equal(gpu_nmap(sv, coords), oracle_mod.build_nmap(coords, W.offsets_3x3x3()))
+
+
+def test_nmap_errors(sv):
+    import torch
+    dup = torch.tensor([[1, 2, 3], [4, 5, 6], [1, 2, 3]], dtype=torch.int32, device="cuda")
+    with pytest.raises(sv.SpconvError) as e:
+        sv.build_nmap(dup)
+    assert e.value.code == -4
+    bad = torch.tensor([[1, 2, 3], [1 << 20, 0, 0]], dtype=torch.int32, device="cuda")
+    with pytest.raises(sv.SpconvError) as e:
+        sv.build_nmap(bad)
+    assert e.value.code == -1
+    small_ws = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(sv.SpconvError) as e:
+        sv.build_nmap(torch.zeros((3, 3), dtype=torch.int32, device="cuda"), workspace=small_ws)
+    assert e.value.code == -3
+    # the library stays usable after errors
+    ok = torch.tensor([[1, 2, 3], [1, 2, 4]], dtype=torch.int32, device="cuda")
+    assert sv.build_nmap(ok)[14, 0].item() == 1
+
+
+@pytest.mark.parametrize("name", ["medium", "channel", "decoder"])
+def test_nmap_large_configs(sv, oracle_mod, name):
+    """Full-size maps: sampled columns equal the oracle's; the invariants
+    (centre = identity, symmetry, pair count) hold everywhere."""
+    import torch
+    from helpers import sample_rows
+    coords = W.coords_only(name)
+    n = len(coords)
+    offs = W.offsets_3x3x3()
+    c = torch.from_numpy(coords).cuda()
+    nm = sv.build_nmap(c)
+    rows = sample_rows(n, 4096, 5)
+    np.testing.assert_array_equal(nm[:, torch.from_numpy(rows).cuda()].cpu().numpy(),
+                                  oracle_mod.nmap_rows(coords, offs, rows))
+    ar = torch.arange(n, device="cuda", dtype=torch.int32)
+    assert torch.equal(nm[13], ar)
+    for k in range(27):
+        valid = nm[k] < n
+        m = nm[k][valid].long()
+        assert torch.equal(nm[26 - k][m], ar[valid])
+    vp = int(((nm >= 0) & (nm < n)).sum().item())
+    assert sv.count_valid_pairs(nm) == vp
+    assert vp >= n

@@ -341,3 +341,11 @@ def test_planted_mistakes_fail_a_pin(oracle_mod):
     gmap = oracle_mod.build_nmap(gc, offs)
     out, _ = oracle_mod.conv(gf, gmap, gw, None, "f32")
     assert not np.array_equal(out, np.asarray(ex["out"], np.float64))
+
+
+def test_nmap_rows_equals_full_map_columns(oracle_mod):
+    coords = W.random_occupancy(9, 0.5, 71)
+    offs = W.offsets_3x3x3()
+    full = brute_force_nmap(coords, offs)
+    rows = np.array([0, len(coords) - 1, 5, 5, len(coords) // 2], dtype=np.int64)
+    np.testing.assert_array_equal(oracle_mod.nmap_rows(coords, offs, rows), full[:, rows])
