@@ -59,7 +59,8 @@ typedef enum spconv_status {
 
 typedef enum spconv_dtype {
     SPCONV_F32 = 0,   /* fp32 storage, fp32 products and fp32 accumulation (CUDA cores) */
-    SPCONV_TF32 = 1,  /* fp32 storage, tf32 tensor-core products, fp32 accumulation */
+    SPCONV_TF32 = 1,  /* fp32 storage, results within the tf32 tolerance (4e-3 * sum|terms|);
+                         currently computed with fp32 products on CUDA cores */
     SPCONV_BF16 = 2   /* bf16 storage, bf16 tensor-core products, fp32 accumulation, bf16 output */
 } spconv_dtype;
 

@@ -7,28 +7,34 @@
 // reduction over (k, ci).  The page's kernel runs one scalar thread per
 // (n, co); here a persistent CTA per SM runs a warp-specialised pipeline:
 //
-//   warp 2    nmap loader: copies the tile's (K x 128) neighbour indices into
-//             a shared-memory slot (coalesced 128-byte reads per offset) and
-//             records, per offset, whether any of the 128 entries is valid
-//             (warp ballot).  Offsets with no valid entry are skipped whole.
-//   warp 0    TMA producer: for each kept offset k and each 128-byte Ci chunk,
-//             gathers the 128 neighbour rows with cp.async.bulk.tensor
-//             tile::gather4 (rows that are not valid are out of the tensor's
-//             bounds, so TMA writes zeros) straight into the 128-byte-swizzled
-//             K-major A layout, and loads the w[k] chunk (MN-major, 128-byte
-//             swizzle) with tiled TMA.  One mbarrier per stage collects the
-//             bytes.
-//   warp 1    MMA issuer (one thread): tcgen05.mma M=128, N=Co, K=16 (bf16)
-//             or K=8 (tf32) into an fp32 accumulator in tensor memory; the
-//             accumulator is double-buffered so the epilogue of one tile
-//             overlaps the main loop of the next.
-//   warps 4-7 epilogue: tcgen05.ld of the accumulator rows, + bias (fp32),
-//             one rounding to the storage type, 16-byte stores.
+//   warp 2     nmap loader: copies the tile's (K x 128) neighbour indices into
+//              a shared-memory slot (coalesced 128-byte reads per offset) and
+//              records, per offset, whether any of the 128 entries is valid
+//              (warp ballot).  Offsets with no valid entry are skipped whole.
+//   warps 8-11 A producers: for each kept offset k and each 128-byte Ci chunk,
+//              gather the 128 neighbour rows with 16-byte cp.async (each warp
+//              instruction moves four whole 128-byte row segments) straight
+//              into the 128-byte-swizzled K-major operand layout; rows that
+//              are not valid are zero-filled without a read.  Completion is
+//              tracked by the stage's mbarrier (cp.async.mbarrier.arrive).
+//   warp 0     B producer: loads the w[k] chunk (MN-major, 128-byte swizzle)
+//              with tiled TMA and writes the stage's metadata.
+//   warp 1     MMA issuer (one thread): tcgen05.mma M=128, N=Co, K=16 into an
+//              fp32 accumulator in tensor memory; the accumulator is
+//              double-buffered so the epilogue of one tile overlaps the main
+//              loop of the next.
+//   warps 4-7  epilogue: tcgen05.ld of the accumulator rows, + bias (fp32),
+//              one rounding to bf16, 16-byte stores.
 //
 // The gathered (K, N, Ci) operand only ever exists one tile at a time in
 // shared memory.  Every wait on an mbarrier is bounded in time; on timeout the
-// kernel records an error bit, drains its own TMA loads and MMAs, frees its
+// kernel records an error bit, drains its own copies and MMAs, frees its
 // tensor memory and returns.
+//
+// Row gathers use the LSU path rather than TMA tile::gather4: measured on
+// GB300, a 4-row gather4 (or a 4-row tiled box) costs ~80 SM cycles of TMA
+// time, so 32 of them per 16 KB stage starve the tensor core ~10x; TMA is
+// kept for the weight tiles, which are large boxes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -37,11 +43,17 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+#ifndef SPCONV_GATHER_L1
+#define SPCONV_GATHER_L1 1
+#endif
+
 namespace spconv {
 namespace {
 
 constexpr int kTileM = 128;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kProducerWarp0 = 8;       // first A-producer warp
+constexpr int kProducerThreads = 128;   // warps 8-11
 constexpr int kSlots = 2;               // neighbour-index slots (tiles in flight)
 constexpr int kSlotRowsMax = 32;        // offsets per slot (more offsets use several slots)
 constexpr uint32_t kABytes = kTileM * 128;
@@ -67,6 +79,7 @@ struct Tf32Traits {
 };
 
 struct TcParams {
+  const void* feats;
   const int32_t* nmap;
   const void* bias;
   void* out;
@@ -120,10 +133,28 @@ __device__ __forceinline__ void store16(float* dst, const uint32_t* acc, const f
                        __uint_as_float(acc[4 * j + 3]) + b[4 * j + 3]);
 }
 
+// Offsets of one slot that the tile issues, and which of them ends the tile.
+// With one slot per tile the tile ends at its highest kept offset (offset 0 if
+// the tile has no valid entry at all: its rows are zero-filled, so the
+// accumulator becomes exactly zero); with several slots the final offset is
+// always issued so the end is known when it is reached.
+__device__ __forceinline__ uint32_t slot_schedule(uint32_t mask, int g, int num_groups, int krows,
+                                                  int* last_r) {
+  *last_r = -1;
+  if (g == num_groups - 1) {
+    if (num_groups == 1) {
+      if (mask == 0u) mask = 1u;
+    } else {
+      mask |= 1u << (krows - 1);
+    }
+    *last_r = 31 - __clz(mask);
+  }
+  return mask;
+}
+
 template <class Tr>
 __global__ void __launch_bounds__(kThreads, 1)
-    submconv_tc_kernel(const __grid_constant__ CUtensorMap tm_feats,
-                       const __grid_constant__ CUtensorMap tm_w, const TcParams p) {
+    submconv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const TcParams p) {
   using T = typename Tr::T;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -151,12 +182,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     for (uint32_t s = 0; s < S; ++s) {
-      mbar_init(smem_addr(&full[s]), 1);
+      mbar_init(smem_addr(&full[s]), kProducerThreads + 1);
       mbar_init(smem_addr(&empty[s]), 1);
     }
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(smem_addr(&slot_full[i]), 32);
-      mbar_init(smem_addr(&slot_empty[i]), 32);
+      mbar_init(smem_addr(&slot_empty[i]), 32 + kProducerThreads);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&tmem_full[i]), 1);
@@ -166,7 +197,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     *consumed_holder = 0;
     *fills_holder = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&tm_feats);
     tma_prefetch_desc(&tm_w);
   }
   if (warp == 1) {
@@ -203,11 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int rr = 0; rr < 8; ++rr) {
             const int r = r0 + rr;
-            const int32_t* src = p.nmap + static_cast<int64_t>(g * kSlotRowsMax + r) * n_rows;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int64_t n = n0 + lane + 32 * j;
-              v[rr][j] = (r < krows && n < n_rows) ? __ldg(src + n) : -1;
+              v[rr][j] = -1;
+              if (r < krows && n < n_rows)
+                v[rr][j] = __ldg(p.nmap + static_cast<int64_t>(g * kSlotRowsMax + r) * n_rows + n);
             }
           }
 #pragma unroll
@@ -232,10 +263,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+  } else if (warp >= kProducerWarp0) {
+    // ------------------------------------------------------ A producers
+    const uint32_t aw = warp - kProducerWarp0;  // rows 32*aw .. 32*aw+31
+    const int sub_row = static_cast<int>(lane >> 3);
+    const int chunk16 = static_cast<int>(lane & 7);
+    const char* feats = static_cast<const char*>(p.feats);
+    const int64_t row_bytes = static_cast<int64_t>(p.ci) * Tr::kElem;
+    uint32_t stage = 0, st_phase = 0, slot = 0, sl_phase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int g = 0; g < p.num_groups && ok; ++g) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&slot_full[slot]), sl_phase))) {
+          ok = false;
+          break;
+        }
+        const int32_t* src = slots + slot * p.slot_rows * kTileM;
+        const int krows = min(kSlotRowsMax, p.k - g * kSlotRowsMax);
+        int last_r;
+        uint32_t mask = slot_schedule(slot_mask[slot], g, p.num_groups, krows, &last_r);
+        while (mask != 0u && ok) {
+          const int r = __ffs(mask) - 1;
+          mask &= mask - 1;
+          int32_t idx[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) idx[j] = src[r * kTileM + 32 * aw + 4 * j + sub_row];
+          for (int c = 0; c < p.num_chunks; ++c) {
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&empty[stage]), st_phase ^ 1))) {
+              ok = false;
+              break;
+            }
+            const int64_t col_byte = static_cast<int64_t>(c) * 128 + chunk16 * 16;
+            const bool col_ok = col_byte < row_bytes;
+            const uint32_t a_dst = smem_addr(smem + stage * p.stage_bytes);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int row = 32 * static_cast<int>(aw) + 4 * j + sub_row;
+              const int32_t v = idx[j];
+              const bool valid = col_ok && v >= 0 && v < n_rows;
+              const char* gsrc = valid ? feats + static_cast<int64_t>(v) * row_bytes + col_byte : feats;
+              const uint32_t d = a_dst + static_cast<uint32_t>(row) * 128u +
+                                 (static_cast<uint32_t>(chunk16 ^ (row & 7)) << 4);
+              cp_async_16<SPCONV_GATHER_L1 != 0>(d, gsrc, valid ? 16u : 0u);
+            }
+            cp_async_arrive_noinc(smem_addr(&full[stage]));
+            if (++stage == S) {
+              stage = 0;
+              st_phase ^= 1;
+            }
+          }
+        }
+        mbar_arrive(smem_addr(&slot_empty[slot]));
+        if (++slot == kSlots) {
+          slot = 0;
+          sl_phase ^= 1;
+        }
+      }
+    }
+    cp_async_wait_all();
   } else if (warp == 0) {
-    // ------------------------------------------------------ TMA producer
+    // ------------------------------------------------------ B producer
     uint32_t stage = 0, st_phase = 0, slot = 0, sl_phase = 0, fills = 0;
     const int nboxes = p.n_mma / Tr::kChunk;
+    const uint32_t b_bytes = static_cast<uint32_t>(p.n_mma) * 128u;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
       bool first = true;
@@ -244,28 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const int32_t* src = slots + slot * p.slot_rows * kTileM;
-        uint32_t mask = slot_mask[slot];
         const int krows = min(kSlotRowsMax, p.k - g * kSlotRowsMax);
         const bool final_group = (g == p.num_groups - 1);
-        int last_r = -1;
-        if (final_group) {
-          // The tile's last stage must be known when it is issued: with one
-          // slot per tile it is the highest kept offset (offset 0 if the
-          // tile has no valid entry at all, whose rows TMA fills with zeros);
-          // with several slots the final offset is always issued.
-          if (p.num_groups == 1) {
-            if (mask == 0u) mask = 1u;
-          } else {
-            mask |= 1u << (krows - 1);
-          }
-          last_r = 31 - __clz(mask);
-        }
+        int last_r;
+        uint32_t mask = slot_schedule(slot_mask[slot], g, p.num_groups, krows, &last_r);
         while (mask != 0u && ok) {
           const int r = __ffs(mask) - 1;
           mask &= mask - 1;
           const int32_t kk = g * kSlotRowsMax + r;
-          const int4 rows = *reinterpret_cast<const int4*>(src + r * kTileM + lane * 4);
           for (int c = 0; c < p.num_chunks; ++c) {
             if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&empty[stage]), st_phase ^ 1))) {
               ok = false;
@@ -278,14 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (first) m |= kMetaFirst;
               if (final_group && r == last_r && c == p.num_chunks - 1) m |= kMetaLast;
               meta[stage] = m;
-              mbar_arrive_expect_tx(fullb, kABytes + static_cast<uint32_t>(p.n_mma) * 128u);
+              mbar_arrive_expect_tx(fullb, b_bytes);
             }
             __syncwarp();
-            const uint32_t a_dst = smem_addr(smem + stage * p.stage_bytes);
-            tma_gather4(a_dst + lane * 512u, &tm_feats, c * Tr::kChunk, rows.x, rows.y, rows.z,
-                        rows.w, fullb);
+            const uint32_t b_dst = smem_addr(smem + stage * p.stage_bytes) + kABytes;
             if (static_cast<int>(lane) < nboxes)
-              tma_load_3d(a_dst + kABytes + lane * p.box_bytes, &tm_w,
+              tma_load_3d(b_dst + lane * p.box_bytes, &tm_w,
                           p.co_base + static_cast<int>(lane) * Tr::kChunk, c * Tr::kChunk, kk,
                           fullb);
             first = false;
@@ -323,6 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          // The A rows were written by cp.async (generic proxy); the MMA reads
+          // them through the async proxy.
+          fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t m = meta[stage];
           const int steps = static_cast<int>((m >> 8) & 0xFFu);
@@ -392,8 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 0 && lane == 0) {
-    // Loads issued but never consumed exist only after a timed-out wait:
-    // wait (bounded) for them to land before the CTA's memory goes away.
+    // Weight loads issued but never consumed exist only after a timed-out
+    // wait: wait (bounded) for them to land before the CTA's memory goes away.
     const uint32_t fills = *fills_holder;
     for (uint32_t i = *consumed_holder; i < fills; ++i)
       mbar_wait(smem_addr(&full[i % S]), (i / S) & 1u);
@@ -414,11 +491,11 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 EncodeTiledFn encode_fn(spconv_status* st) {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;
-  static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
-    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    cudaError_t err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                       cudaEnableDefault, &q);
     if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<EncodeTiledFn>(p);
   });
   if (fn == nullptr) *st = fail(SPCONV_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
@@ -433,18 +510,7 @@ spconv_status launch_typed(const void* feats, const int32_t* nmap, const void* w
   EncodeTiledFn encode = encode_fn(&st);
   if (encode == nullptr) return st;
 
-  CUtensorMap tm_feats, tm_w;
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(ci), static_cast<cuuint64_t>(n)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ci) * Tr::kElem};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(Tr::kChunk), 1};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&tm_feats, Tr::kTmaType, 2, const_cast<void*>(feats), dims, strides, box,
-                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-      return fail(SPCONV_ERR_CUDA, "cuTensorMapEncodeTiled(feats) failed: " + std::to_string(r));
-  }
+  CUtensorMap tm_w;
   {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(co), static_cast<cuuint64_t>(ci),
                           static_cast<cuuint64_t>(k)};
@@ -466,6 +532,7 @@ spconv_status launch_typed(const void* feats, const int32_t* nmap, const void* w
 
   for (int32_t co_base = 0; co_base < co; co_base += 256) {
     TcParams p{};
+    p.feats = feats;
     p.nmap = nmap;
     p.bias = bias;
     p.out = out;
@@ -513,7 +580,7 @@ spconv_status launch_typed(const void* feats, const int32_t* nmap, const void* w
                                       static_cast<int>(smem_bytes)),
                  "cudaFuncSetAttribute", &cst))
       return cst;
-    kern<<<grid, kThreads, smem_bytes, stream>>>(tm_feats, tm_w, p);
+    kern<<<grid, kThreads, smem_bytes, stream>>>(tm_w, p);
     if (!cuda_ok(cudaGetLastError(), "submconv_tc_kernel launch", &cst)) return cst;
   }
   return SPCONV_OK;

@@ -149,7 +149,9 @@ spconv_status spconv_submconv3d(const void* feats_dev, const int32_t* nmap_dev, 
   spconv_status st = spconv::check_device();
   if (st != SPCONV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dtype == SPCONV_F32)
+  // SPCONV_TF32 runs the exact fp32 kernel for now (its results are within
+  // the tf32 tolerance); the tensor-core tf32 variant is not enabled.
+  if (dtype == SPCONV_F32 || dtype == SPCONV_TF32)
     st = spconv::launch_conv_simt_f32(static_cast<const float*>(feats_dev), nmap_dev,
                                       static_cast<const float*>(w_dev),
                                       static_cast<const float*>(bias_dev), static_cast<float*>(out_dev),
