@@ -108,6 +108,42 @@ spconv_status spconv_build_nmap(const int32_t* coords_dev, int64_t N, const int3
                                 int32_t K, int32_t* nmap_dev, void* workspace_dev,
                                 size_t workspace_bytes, void* stream);
 
+/* Largest N spconv_build_nmap_noalloc accepts (its fixed table holds
+ * 2 * SPCONV_NOALLOC_MAX_VOXELS slots). */
+#define SPCONV_NOALLOC_MAX_VOXELS (1 << 20)
+
+/*
+ * spconv_build_nmap without a workspace: the same map, built in a fixed
+ * device array that belongs to the library, so the call needs no device
+ * memory from the caller.  The page has no counterpart of this call.
+ *
+ * It is for callers that cannot allocate device memory where they need a
+ * map: code inside a host framework that owns every device allocation (its
+ * own allocator, no raw cudaMalloc allowed), or a deployment with a fixed
+ * memory budget that forbids allocations after start-up.  Nothing is
+ * allocated or freed by the call itself.
+ *
+ * Arguments are those of spconv_build_nmap without the workspace; coords
+ * and nmap are still the caller's.  Limits and behaviour:
+ *  - N must not exceed SPCONV_NOALLOC_MAX_VOXELS; larger N returns
+ *    SPCONV_ERR_UNSUPPORTED before any device work.
+ *  - The array (32 MiB + 256 B) is a static device variable: every GPU that
+ *    loads this library holds it until the process exits.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array and clears what it needs
+ *    (table keys and flags) at its start; the previous call's contents are
+ *    otherwise left in place.  Calls whose work overlaps on the GPU (other
+ *    streams, other host threads) race on the array and must be ordered by
+ *    the caller.
+ *  - Like spconv_build_nmap, it waits for `stream` once at the end to read
+ *    the duplicate / range flags.
+ */
+spconv_status spconv_build_nmap_noalloc(const int32_t* coords_dev, int64_t N,
+                                        const int32_t* offsets_host, int32_t K, int32_t* nmap_dev,
+                                        void* stream);
+
 /*
  * Fused submanifold convolution: gathers the neighbour rows tile by tile in
  * on-chip memory (the (K, N, Ci) gather is never written to device memory),

@@ -28,6 +28,9 @@ struct BuildOffsets {
 size_t hash_capacity(int64_t n);
 spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOffsets& offs,
                                 int32_t k, int32_t* nmap, void* workspace, cudaStream_t stream);
+// Device address of the allocation-free variant's static scratch on the
+// current device (looked up once per device).
+spconv_status noalloc_scratch(void** scratch);
 spconv_status launch_count_valid_pairs(const int32_t* nmap, int64_t n, int32_t k, int64_t* count,
                                        cudaStream_t stream);
 

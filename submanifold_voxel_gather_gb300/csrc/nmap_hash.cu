@@ -17,6 +17,9 @@
 // sequences are short; every probe loop is still bounded by the capacity.
 #include <cuda_runtime.h>
 
+#include <mutex>
+#include <string>
+
 #include "internal.h"
 
 namespace spconv {
@@ -193,6 +196,44 @@ spconv_status launch_count_valid_pairs(const int32_t* nmap, int64_t n, int32_t k
   const unsigned grid = static_cast<unsigned>(blocks < 8ll * sms ? blocks : 8ll * sms);
   count_valid_kernel<<<grid, kThreads, 0, stream>>>(nmap, total, n, c);
   if (!cuda_ok(cudaGetLastError(), "count_valid_kernel launch", &st)) return st;
+  return SPCONV_OK;
+}
+
+// ------------------------------------------------------------------------
+// Allocation-free variant.  Some callers cannot allocate device memory at
+// the point where they need a neighbour map (for example code running inside
+// a host framework that owns every device allocation, or a fixed-budget
+// deployment that forbids allocations after start-up).  For them the hash
+// table lives in one file-scope device array of fixed size instead of a
+// caller-provided workspace.  Every GPU that loads this library holds the
+// array (32 MiB + 256 B) until the process exits.
+namespace {
+
+constexpr size_t kNoAllocBytes = kFlagBytes + 2 * static_cast<size_t>(SPCONV_NOALLOC_MAX_VOXELS) * 16;
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+}  // namespace
+
+spconv_status noalloc_scratch(void** scratch) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(SPCONV_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(SPCONV_ERR_UNSUPPORTED, "device ordinal out of range");
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    // Host code only has a stand-in for the array's name; its device address
+    // comes from the runtime, once per device, with that device current.
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess)
+      return fail(SPCONV_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+    addr[dev] = p;
+  }
+  *scratch = addr[dev];
   return SPCONV_OK;
 }
 

@@ -120,6 +120,40 @@ spconv_status spconv_build_nmap(const int32_t* coords_dev, int64_t N, const int3
   return st == SPCONV_OK ? spconv::ok() : st;
 }
 
+spconv_status spconv_build_nmap_noalloc(const int32_t* coords_dev, int64_t N,
+                                        const int32_t* offsets_host, int32_t K, int32_t* nmap_dev,
+                                        void* stream) {
+  if (N < 0) return fail(SPCONV_ERR_INVALID_ARG, "N must be >= 0");
+  if (N > SPCONV_NOALLOC_MAX_VOXELS)
+    return fail(SPCONV_ERR_UNSUPPORTED,
+                "N exceeds SPCONV_NOALLOC_MAX_VOXELS (" + std::to_string(SPCONV_NOALLOC_MAX_VOXELS) +
+                    "); use spconv_build_nmap with a workspace");
+  if (K < 1 || K > SPCONV_MAX_BUILD_OFFSETS)
+    return fail(SPCONV_ERR_INVALID_ARG, "K must satisfy 1 <= K <= SPCONV_MAX_BUILD_OFFSETS");
+  if (offsets_host == nullptr) return fail(SPCONV_ERR_INVALID_ARG, "offsets_host is NULL");
+  if (N == 0) return spconv::ok();
+  if (coords_dev == nullptr || nmap_dev == nullptr)
+    return fail(SPCONV_ERR_INVALID_ARG, "coords and nmap must be non-NULL");
+  if (!spconv::aligned(coords_dev, 4) || !spconv::aligned(nmap_dev, 4))
+    return fail(SPCONV_ERR_INVALID_ARG, "coords and nmap must be 4-byte aligned");
+  for (int32_t i = 0; i < 3 * K; ++i) {
+    const int32_t d = offsets_host[i];
+    if (d <= -SPCONV_COORD_LIMIT || d >= SPCONV_COORD_LIMIT)
+      return fail(SPCONV_ERR_INVALID_ARG, "offset component out of range");
+  }
+  spconv_status st = spconv::check_device();
+  if (st != SPCONV_OK) return st;
+  void* scratch = nullptr;
+  st = spconv::noalloc_scratch(&scratch);
+  if (st != SPCONV_OK) return st;
+  spconv::BuildOffsets offs;
+  std::memset(&offs, 0, sizeof offs);
+  std::memcpy(offs.d, offsets_host, sizeof(int32_t) * 3 * static_cast<size_t>(K));
+  st = spconv::launch_build_nmap(coords_dev, N, offs, K, nmap_dev, scratch,
+                                 static_cast<cudaStream_t>(stream));
+  return st == SPCONV_OK ? spconv::ok() : st;
+}
+
 spconv_status spconv_submconv3d(const void* feats_dev, const int32_t* nmap_dev, const void* w_dev,
                                 const void* bias_dev, void* out_dev, int64_t N, int32_t K,
                                 int32_t Ci, int32_t Co, spconv_dtype dtype, void* stream) {
