@@ -13,6 +13,13 @@
 //           shifted key (one 16-byte load per probe), write nmap[k, n] with
 //           coalesced stores across the warp
 //
+// The map is symmetric: if offsets k and k' are opposite, nmap[k, n] = m
+// exactly when nmap[k', m] = n.  So only one offset of each opposite pair is
+// probed; a hit writes both entries, and the rows of the unprobed offsets are
+// filled with N beforehand (by the clear kernel).  A zero offset gives
+// nmap[k, n] = n without a probe.  This halves the probes of a symmetric
+// offset set such as {-1,0,1}^3.
+//
 // Capacity is the next power of two >= 2N (load factor <= 1/2), so probe
 // sequences are short; every probe loop is still bounded by the capacity.
 #include <cuda_runtime.h>
@@ -31,6 +38,15 @@ constexpr unsigned long long kEmptyKey = ~0ull;
 constexpr size_t kFlagBytes = 256;
 
 enum : int { kFlagDuplicate = 1, kFlagRange = 2, kFlagFull = 4 };
+
+enum : int8_t { kRoleProbe = 0, kRoleMirror = 1, kRoleSelf = 2 };
+
+// Per-offset work of the query kernel (built on the host from the offsets).
+struct QueryPlan {
+  int32_t d[3 * SPCONV_MAX_BUILD_OFFSETS];   // offsets (dz, dy, dx)
+  int16_t mirror[SPCONV_MAX_BUILD_OFFSETS];  // probed offset: its opposite's row, or -1
+  int8_t role[SPCONV_MAX_BUILD_OFFSETS];     // kRoleProbe / kRoleMirror / kRoleSelf
+};
 
 struct alignas(16) Slot {
   unsigned long long key;
@@ -57,13 +73,23 @@ __device__ __forceinline__ bool in_grid(int v) {
   return v >= 0 && v < SPCONV_COORD_LIMIT;
 }
 
-__global__ void hash_clear_kernel(Slot* table, unsigned long long cap, int* flags) {
+// Clears the table and flags, and writes N into the map rows of the offsets
+// whose entries come from their opposite's hits (kRoleMirror).
+__global__ void hash_clear_kernel(Slot* table, unsigned long long cap, int* flags, int32_t* nmap,
+                                  int64_t n, int32_t fill_count, const __grid_constant__ QueryPlan plan) {
   const unsigned long long stride = static_cast<unsigned long long>(gridDim.x) * blockDim.x;
-  for (unsigned long long i = static_cast<unsigned long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-       i < cap; i += stride) {
-    table[i].key = kEmptyKey;
+  const unsigned long long tid = static_cast<unsigned long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (unsigned long long i = tid; i < cap; i += stride) table[i].key = kEmptyKey;
+  if (fill_count > 0) {
+    const int32_t missing = static_cast<int32_t>(n);
+    for (int32_t r = 0, seen = 0; seen < fill_count; ++r) {
+      if (plan.role[r] != kRoleMirror) continue;
+      ++seen;
+      int32_t* row = nmap + static_cast<int64_t>(r) * n;
+      for (unsigned long long i = tid; i < static_cast<unsigned long long>(n); i += stride) row[i] = missing;
+    }
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) *flags = 0;
+  if (tid == 0) *flags = 0;
 }
 
 __global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n, Slot* table,
@@ -94,30 +120,38 @@ __global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n
 
 __global__ void __launch_bounds__(kThreads)
     nmap_query_kernel(const int32_t* __restrict__ coords, int64_t n, const Slot* __restrict__ table,
-                      unsigned long long mask, const BuildOffsets offs, int32_t k_count,
-                      int32_t* __restrict__ nmap) {
+                      unsigned long long mask, const __grid_constant__ QueryPlan plan,
+                      int32_t k_count, int32_t* __restrict__ nmap) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const int z = coords[3 * i], y = coords[3 * i + 1], x = coords[3 * i + 2];
   const int32_t missing = static_cast<int32_t>(n);
   for (int32_t k = 0; k < k_count; ++k) {
-    const int qz = z + offs.d[3 * k], qy = y + offs.d[3 * k + 1], qx = x + offs.d[3 * k + 2];
+    const int8_t role = plan.role[k];
+    if (role == kRoleMirror) continue;
     int32_t found = missing;
-    if (in_grid(qz) && in_grid(qy) && in_grid(qx)) {
-      const unsigned long long key = pack_coord(qz, qy, qx);
-      unsigned long long h = mix_hash(key) & mask;
-      for (unsigned long long probe = 0; probe <= mask; ++probe) {
-        const int4 s = __ldg(reinterpret_cast<const int4*>(table + h));
-        const unsigned long long sk =
-            (static_cast<unsigned long long>(static_cast<uint32_t>(s.y)) << 32) |
-            static_cast<uint32_t>(s.x);
-        if (sk == key) {
-          found = s.z;
-          break;
+    if (role == kRoleSelf) {
+      found = static_cast<int32_t>(i);
+    } else {
+      const int qz = z + plan.d[3 * k], qy = y + plan.d[3 * k + 1], qx = x + plan.d[3 * k + 2];
+      if (in_grid(qz) && in_grid(qy) && in_grid(qx)) {
+        const unsigned long long key = pack_coord(qz, qy, qx);
+        unsigned long long h = mix_hash(key) & mask;
+        for (unsigned long long probe = 0; probe <= mask; ++probe) {
+          const int4 s = __ldg(reinterpret_cast<const int4*>(table + h));
+          const unsigned long long sk =
+              (static_cast<unsigned long long>(static_cast<uint32_t>(s.y)) << 32) |
+              static_cast<uint32_t>(s.x);
+          if (sk == key) {
+            found = s.z;
+            break;
+          }
+          if (sk == kEmptyKey) break;
+          h = (h + 1) & mask;
         }
-        if (sk == kEmptyKey) break;
-        h = (h + 1) & mask;
       }
+      const int16_t mk = plan.mirror[k];
+      if (mk >= 0 && found != missing) nmap[static_cast<int64_t>(mk) * n + found] = static_cast<int32_t>(i);
     }
     nmap[static_cast<int64_t>(k) * n + i] = found;
   }
@@ -159,14 +193,42 @@ spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOff
   const unsigned long long clear_blocks = (cap + kThreads - 1) / kThreads;
   const unsigned clear_grid =
       static_cast<unsigned>(clear_blocks < 16ull * sms ? clear_blocks : 16ull * sms);
-  hash_clear_kernel<<<clear_grid, kThreads, 0, stream>>>(table, cap, flags);
+  QueryPlan plan;
+  int32_t fill_count = 0;
+  for (int32_t a = 0; a < k; ++a) {
+    plan.d[3 * a] = offs.d[3 * a];
+    plan.d[3 * a + 1] = offs.d[3 * a + 1];
+    plan.d[3 * a + 2] = offs.d[3 * a + 2];
+    plan.mirror[a] = -1;
+    plan.role[a] = -1;
+  }
+  for (int32_t a = 0; a < k; ++a) {
+    if (plan.role[a] >= 0) continue;  // already the mirror of an earlier offset
+    const int32_t* da = plan.d + 3 * a;
+    if (da[0] == 0 && da[1] == 0 && da[2] == 0) {
+      plan.role[a] = kRoleSelf;
+      continue;
+    }
+    plan.role[a] = kRoleProbe;
+    for (int32_t b = a + 1; b < k; ++b) {
+      const int32_t* db = plan.d + 3 * b;
+      if (plan.role[b] < 0 && db[0] == -da[0] && db[1] == -da[1] && db[2] == -da[2]) {
+        plan.mirror[a] = static_cast<int16_t>(b);
+        plan.role[b] = kRoleMirror;
+        ++fill_count;
+        break;
+      }
+    }
+  }
+  hash_clear_kernel<<<clear_grid, kThreads, 0, stream>>>(table, cap, flags, nmap, n, fill_count,
+                                                         plan);
   if (!cuda_ok(cudaGetLastError(), "hash_clear_kernel launch", &st)) return st;
 
   const unsigned grid = static_cast<unsigned>((n + kThreads - 1) / kThreads);
   hash_insert_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, flags);
   if (!cuda_ok(cudaGetLastError(), "hash_insert_kernel launch", &st)) return st;
 
-  nmap_query_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, offs, k, nmap);
+  nmap_query_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, plan, k, nmap);
   if (!cuda_ok(cudaGetLastError(), "nmap_query_kernel launch", &st)) return st;
 
   int host_flags = 0;
