@@ -59,6 +59,12 @@ constexpr int kRing = 16;              // neighbour-index ring rows
 constexpr int kChunk = 64;             // bf16 elements per 128-byte row
 constexpr int kKPerMma = 16;
 constexpr uint32_t kWBlockBytes = 128 * 128;  // one M block of weights per stage (16 KB)
+// Descriptor start-address steps, in 16-byte units: an M block of weights,
+// one K step of the channel-major weights (16 rows x 128 B) and one K step of
+// the K-major gathered rows (32 B within each 128-byte row).
+constexpr uint64_t kWBlockUnits = kWBlockBytes >> 4;
+constexpr uint64_t kAStepUnits = (kKPerMma * 128) >> 4;
+constexpr uint64_t kBStepUnits = (kKPerMma * 2) >> 4;
 constexpr int kMaxStages = 8;
 constexpr int kMaxSmem = 232448;       // 227 KB opt-in limit per block
 
@@ -339,6 +345,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // Descriptors of stage 0; a stage or K step only moves the start
+      // address (the low 14 bits, in 16-byte units), so advancing is one add.
+      const uint64_t adesc0 = sw128_desc(smem_addr(smem), 8192u, 1024u);
+      const uint64_t bdesc0 = sw128_desc(smem_addr(smem) + p.w_bytes, 16u, 1024u);
+      const uint64_t stage_units = p.stage_bytes >> 4;
+      const uint32_t idesc = p.idesc;
       uint32_t stage = 0, st_phase = 0, consumed = 0, tile_i = 0, buf = 0;
       uint32_t d_tmem = tmem_base;
       bool open = false;
@@ -366,17 +378,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           open = true;
         }
         const int steps = static_cast<int>((m >> 8) & 0xFFu);
-        const uint32_t w0 = smem_addr(smem + stage * p.stage_bytes);
-        const uint32_t f0 = w0 + p.w_bytes;
-        for (int s = 0; s < steps; ++s) {
-          const uint64_t bdesc = sw128_desc(f0 + s * 32u, 16u, 1024u);
-          const uint32_t acc = (s > 0 || (m & kMetaFirst) == 0u) ? 1u : 0u;
+        const uint64_t ad = adesc0 + stage * stage_units;
+        const uint64_t bd = bdesc0 + stage * stage_units;
+        const uint32_t acc0 = (m & kMetaFirst) == 0u ? 1u : 0u;
+        if (steps == kChunk / kKPerMma) {
 #pragma unroll
-          for (int mb = 0; mb < MBLK; ++mb) {
-            const uint64_t adesc =
-                sw128_desc(w0 + mb * kWBlockBytes + s * (kKPerMma * 128u), 8192u, 1024u);
-            umma_f16(d_tmem + mb * TILE_N, adesc, bdesc, p.idesc, acc);
-          }
+          for (int s = 0; s < kChunk / kKPerMma; ++s)
+#pragma unroll
+            for (int mb = 0; mb < MBLK; ++mb)
+              umma_f16(d_tmem + mb * TILE_N, ad + mb * kWBlockUnits + s * kAStepUnits,
+                       bd + s * kBStepUnits, idesc, s > 0 ? 1u : acc0);
+        } else {
+          for (int s = 0; s < steps; ++s)
+#pragma unroll
+            for (int mb = 0; mb < MBLK; ++mb)
+              umma_f16(d_tmem + mb * TILE_N, ad + mb * kWBlockUnits + s * kAStepUnits,
+                       bd + s * kBStepUnits, idesc, s > 0 ? 1u : acc0);
         }
         umma_commit(smem_addr(&empty[stage]));
         ++consumed;
