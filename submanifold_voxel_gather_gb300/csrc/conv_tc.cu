@@ -8,8 +8,8 @@
 //
 //     out^T[co, n] += w[k]^T[co, ci] * gathered_feats_k^T[ci, n]
 //
-// with M = 128 output channels (one or two M blocks), N = TILE_N voxels (256
-// when Co <= 128, else 128) and K = 16 input channels per instruction.  A wide
+// with M = 128 output channels (one or two M blocks), N = 256 voxels and K =
+// 16 input channels per instruction.  A wide
 // N keeps the tensor core fed: an M=128 x N=256 x K=16 bf16 MMA reads 12 KB of
 // shared memory in 128 cycles, where the M=128 x N=128 shape reads 8 KB in 64.
 // It also halves the weight traffic per voxel.  A persistent CTA per SM runs a
@@ -27,8 +27,10 @@
 //   warp 0     weight producer: loads w[k]'s chunk (channel-major, 128-byte
 //              swizzle) with tiled TMA and writes the stage metadata.
 //   warp 1     MMA issuer (one thread): fp32 accumulator in tensor memory,
-//              double-buffered so one tile's epilogue overlaps the next
-//              tile's main loop.
+//              double-buffered for Co <= 128 so one tile's epilogue overlaps
+//              the next tile's main loop (two M blocks fill all 512 columns
+//              with one buffer: measured faster than N = 128 with two, which
+//              doubles the weight traffic per voxel).
 //   warps 4-7  epilogue: tcgen05.ld (lane = channel, column = voxel), + bias,
 //              one rounding to bf16, transpose through shared memory,
 //              coalesced 16-byte stores.
@@ -129,6 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kIdxPerLane = kRowsPerWarp / 4;  // 4 rows per warp instruction
   constexpr int kLoaderPerLane = TILE_N / 32;
   constexpr int kOutStride = MBLK * 128;         // staged output row, elements
+  // Two accumulator buffers (the epilogue of one tile overlaps the next) when
+  // they fit in the 512 tensor-memory columns, else one.
+  constexpr uint32_t kAccBufs = (2 * MBLK * TILE_N <= 512) ? 2u : 1u;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -371,8 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if ((m & kMetaFirst) != 0u) {
-          buf = tile_i & 1u;
-          if (!mbar_wait(smem_addr(&tmem_empty[buf]), ((tile_i >> 1) & 1u) ^ 1u)) break;
+          buf = tile_i % kAccBufs;
+          if (!mbar_wait(smem_addr(&tmem_empty[buf]), ((tile_i / kAccBufs) & 1u) ^ 1u)) break;
           tc_fence_after();
           d_tmem = tmem_base + buf * static_cast<uint32_t>(MBLK * TILE_N);
           open = true;
@@ -414,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int chunks_per_row = p.co_count / 8;                           // 16-byte chunks
     uint32_t tile_i = 0;
     for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tile_i) {
-      const uint32_t buf = tile_i & 1u;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(smem_addr(&tmem_full[buf]), (tile_i >> 1) & 1u));
+      const uint32_t buf = tile_i % kAccBufs;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(smem_addr(&tmem_full[buf]), (tile_i / kAccBufs) & 1u));
       if (!epilogue_all(got)) break;
       tc_fence_after();
       const int64_t n0 = t * TILE_N;
@@ -496,7 +501,7 @@ spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t str
   const int grid = static_cast<int>(p.num_tiles < sms ? p.num_tiles : sms);
   p.w_bytes = MBLK * kWBlockBytes;
   p.stage_bytes = p.w_bytes + TILE_N * 128u;
-  p.tmem_cols = 2u * MBLK * TILE_N;  // 512: two accumulator buffers
+  p.tmem_cols = 512u;  // kAccBufs accumulator buffers of MBLK x TILE_N columns
   // D f32, A and B bf16, A (weights) channel-major, B (gathered rows) K-major.
   p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) |
             ((static_cast<uint32_t>(TILE_N) >> 3) << 17) | ((128u >> 4) << 24);
@@ -584,7 +589,7 @@ spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_
     p.co_base = co_base;
     p.co_count = (co - co_base) < 256 ? (co - co_base) : 256;
     p.num_chunks = (ci + kChunk - 1) / kChunk;
-    st = p.co_count <= 128 ? launch_shape<256, 1>(tm_w, p, stream) : launch_shape<128, 2>(tm_w, p, stream);
+    st = p.co_count <= 128 ? launch_shape<256, 1>(tm_w, p, stream) : launch_shape<256, 2>(tm_w, p, stream);
     if (st != SPCONV_OK) return st;
   }
   return SPCONV_OK;
