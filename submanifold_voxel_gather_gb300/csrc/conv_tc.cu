@@ -124,7 +124,10 @@ __device__ __forceinline__ bool issue_row(uint32_t flag, int kk, int k_count, bo
   return flag != 0u || (kk == k_count - 1 && !issued);
 }
 
-template <int TILE_N, int MBLK>
+// kHoist: the per-row source index and byte count are computed once per
+// offset instead of once per chunk (used when an offset has two or more
+// 128-byte chunks; with one chunk the in-loop form is measured faster).
+template <int TILE_N, int MBLK, bool kHoist>
 __global__ void __launch_bounds__(kThreads, 1)
     submconv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const TcParams p) {
   constexpr int kRowsPerWarp = TILE_N / 4;       // gathered rows per producer warp
@@ -221,8 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool any = false;
 #pragma unroll
           for (int j = 0; j < kLoaderPerLane; ++j) {
-            any |= (v[b][j] >= 0 && v[b][j] < n_rows);
-            ring[e * TILE_N + lane + 32 * j] = v[b][j];
+            // normalised: a valid index, or -1 for every kind of invalid entry
+            const int32_t nv = (v[b][j] >= 0 && v[b][j] < n_rows) ? v[b][j] : -1;
+            any |= nv >= 0;
+            ring[e * TILE_N + lane + 32 * j] = nv;
           }
           const uint32_t ballot = __ballot_sync(0xffffffffu, any);
           if (lane == 0) ring_flag[e] = ballot != 0u ? 1u : 0u;
@@ -240,7 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sub_row = static_cast<int>(lane >> 3);
     const int chunk16 = static_cast<int>(lane & 7);
     const char* feats = reinterpret_cast<const char*>(p.feats);
-    const int64_t row_bytes = static_cast<int64_t>(p.ci) * 2;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.ci) * 2u;
+    // Row-independent part of the destination: this lane's row group and its
+    // swizzled 16-byte slot (rows 4 j + sub_row alternate between two
+    // swizzle phases).  The producer loop is issue-bound, so its per-row
+    // work is kept to an address multiply-add and the copy itself.
+    const uint32_t dst_lane = (aw * kRowsPerWarp + static_cast<uint32_t>(sub_row)) * 128u;
+    const uint32_t sw_even = static_cast<uint32_t>(chunk16 ^ sub_row) << 4;
+    const uint32_t sw_odd = static_cast<uint32_t>(chunk16 ^ (sub_row + 4)) << 4;
     uint32_t stage = 0, st_phase = 0, e = 0, ephase = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
@@ -251,11 +263,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const bool go = issue_row(ring_flag[e], kk, k_count, issued);
-        int32_t idx[kIdxPerLane];
+        int32_t idx[kIdxPerLane];   // a valid index or -1
+        uint32_t vi[kIdxPerLane];   // kHoist: index, 0 where invalid
+        uint32_t valid_bits = 0;    // kHoist: bit j set where row j is valid
         if (go) {
 #pragma unroll
-          for (int j = 0; j < kIdxPerLane; ++j)
+          for (int j = 0; j < kIdxPerLane; ++j) {
             idx[j] = ring[e * TILE_N + static_cast<int>(aw) * kRowsPerWarp + 4 * j + sub_row];
+            if constexpr (kHoist) {
+              vi[j] = idx[j] >= 0 ? static_cast<uint32_t>(idx[j]) : 0u;
+              valid_bits |= (idx[j] >= 0 ? 1u : 0u) << j;
+            }
+          }
         }
         mbar_arrive(smem_addr(&ring_empty[e]));
         if (++e == kRing) {
@@ -269,18 +288,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const int64_t col_byte = static_cast<int64_t>(c) * 128 + chunk16 * 16;
+          const uint32_t col_byte = static_cast<uint32_t>(c) * 128u + static_cast<uint32_t>(chunk16) * 16u;
           const bool col_ok = col_byte < row_bytes;
-          const uint32_t f_dst = smem_addr(smem + stage * p.stage_bytes) + p.w_bytes;
+          const char* chunk_base = feats + col_byte;
+          const uint32_t f_dst = smem_addr(smem + stage * p.stage_bytes) + p.w_bytes + dst_lane;
+          if constexpr (kHoist) {
+            const uint32_t live = col_ok ? valid_bits : 0u;
 #pragma unroll
-          for (int j = 0; j < kIdxPerLane; ++j) {
-            const int row = static_cast<int>(aw) * kRowsPerWarp + 4 * j + sub_row;
-            const int32_t v = idx[j];
-            const bool valid = col_ok && v >= 0 && v < n_rows;
-            const char* src = valid ? feats + static_cast<int64_t>(v) * row_bytes + col_byte : feats;
-            const uint32_t d = f_dst + static_cast<uint32_t>(row) * 128u +
-                               (static_cast<uint32_t>(chunk16 ^ (row & 7)) << 4);
-            cp_async_16<false>(d, src, valid ? 16u : 0u);
+            for (int j = 0; j < kIdxPerLane; ++j)
+              cp_async_16<false>(f_dst + 512u * j + ((j & 1) ? sw_odd : sw_even),
+                                 chunk_base + static_cast<uint64_t>(vi[j]) * row_bytes, ((live >> j) & 1u) << 4);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kIdxPerLane; ++j) {
+              const bool valid = col_ok && idx[j] >= 0;
+              const uint32_t v = valid ? static_cast<uint32_t>(idx[j]) : 0u;
+              cp_async_16<false>(f_dst + 512u * j + ((j & 1) ? sw_odd : sw_even),
+                                 chunk_base + static_cast<uint64_t>(v) * row_bytes, valid ? 16u : 0u);
+            }
           }
           cp_async_arrive_noinc(smem_addr(&full[stage]));
           if (++stage == S) {
@@ -493,7 +518,7 @@ EncodeTiledFn encode_fn(spconv_status* st) {
   return fn;
 }
 
-template <int TILE_N, int MBLK>
+template <int TILE_N, int MBLK, bool kHoist>
 spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t stream) {
   const int sms = sm_count();
   if (sms <= 0) return fail(SPCONV_ERR_CUDA, "could not query the SM count");
@@ -528,7 +553,7 @@ spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t str
   off += (2u * stages + 2u * kRing + 5u) * 8u + 16u;
   const uint32_t smem_bytes = off + 1024u;  // slack for the 1024-byte alignment
 
-  auto kern = submconv_tc_kernel<TILE_N, MBLK>;
+  auto kern = submconv_tc_kernel<TILE_N, MBLK, kHoist>;
   spconv_status st = SPCONV_OK;
   if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem_bytes)),
@@ -589,7 +614,11 @@ spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_
     p.co_base = co_base;
     p.co_count = (co - co_base) < 256 ? (co - co_base) : 256;
     p.num_chunks = (ci + kChunk - 1) / kChunk;
-    st = p.co_count <= 128 ? launch_shape<256, 1>(tm_w, p, stream) : launch_shape<256, 2>(tm_w, p, stream);
+    const bool hoist = p.num_chunks >= 2;
+    if (p.co_count <= 128)
+      st = hoist ? launch_shape<256, 1, true>(tm_w, p, stream) : launch_shape<256, 1, false>(tm_w, p, stream);
+    else
+      st = hoist ? launch_shape<256, 2, true>(tm_w, p, stream) : launch_shape<256, 2, false>(tm_w, p, stream);
     if (st != SPCONV_OK) return st;
   }
   return SPCONV_OK;
