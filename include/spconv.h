@@ -168,13 +168,104 @@ spconv_status spconv_build_nmap_noalloc(const int32_t* coords_dev, int64_t N,
  * in a CUDA graph.  Tensor-core paths multiply the zero rows that stand for
  * missing neighbours inside a partly valid tile, so a non-finite weight can
  * turn such an output into NaN where an exact skip would not; offsets that
- * are missing for every voxel of a 128-voxel tile are skipped outright.
+ * are missing for every voxel of a tile (256 voxels on the tensor-core
+ * path, 64 on the fp32 path) are skipped outright.
  * Internal kernel errors (a pipeline wait that timed out) are reported by
  * spconv_device_status().
  */
 spconv_status spconv_submconv3d(const void* feats_dev, const int32_t* nmap_dev, const void* w_dev,
                                 const void* bias_dev, void* out_dev, int64_t N, int32_t K,
                                 int32_t Ci, int32_t Co, spconv_dtype dtype, void* stream);
+
+/* Activation applied by spconv_submconv3d_ex (after bias and residual). */
+typedef enum spconv_activation {
+    SPCONV_ACT_NONE = 0,
+    SPCONV_ACT_RELU = 1, /* max(x, 0) */
+    SPCONV_ACT_SILU = 2  /* x / (1 + exp(-x)), evaluated in fp32 with expf */
+} spconv_activation;
+
+/*
+ * The convolution with a fused epilogue for chaining layers:
+ *
+ *     out[n, co] = act(conv[n, co] + bias[co] + residual[n, co])
+ *
+ * where conv[n, co] = sum_k sum_ci feats[nmap[k, n], ci] * w[k, ci, co] is
+ * the sum of spconv_submconv3d.  The page ("sparse_conv_metal.py", module
+ * docstring) runs this convolution layer after layer inside decoders; it
+ * defines no epilogue beyond the bias (wrapper), so the residual add and the
+ * activation are an extension: they are applied in fp32 to the accumulator
+ * before the single cast to the storage type, instead of by separate passes
+ * over (N, Co) in device memory.
+ *
+ *  residual_dev  (N, Co) storage type, or NULL for none, aligned like
+ *                out_dev.  It may be the same buffer as out_dev (an in-place
+ *                residual update); it must not overlap feats_dev.
+ *  act           SPCONV_ACT_NONE, SPCONV_ACT_RELU or SPCONV_ACT_SILU; any
+ *                other value gives SPCONV_ERR_INVALID_ARG.
+ *  Every other argument, requirement and property is as for
+ *  spconv_submconv3d; with residual_dev == NULL and SPCONV_ACT_NONE the two
+ *  calls compute the same result.
+ */
+spconv_status spconv_submconv3d_ex(const void* feats_dev, const int32_t* nmap_dev,
+                                   const void* w_dev, const void* bias_dev,
+                                   const void* residual_dev, void* out_dev, int64_t N, int32_t K,
+                                   int32_t Ci, int32_t Co, spconv_dtype dtype,
+                                   spconv_activation act, void* stream);
+
+/*
+ * Gradient of the convolution with respect to its input features:
+ *
+ *     dfeats[m, ci] = sum over entries nmap[k, n] == m of
+ *                     sum_co dout[n, co] * w[k, ci, co]
+ *
+ * (the chain rule applied to the formula of spconv_submconv3d; the page
+ * computes the forward pass only).  The map must come from a point-symmetric
+ * offset list in mirrored order, offsets[K-1-k] == -offsets[k] (true of the
+ * lexicographic 3x3x3 list and of every cube list): then nmap[k, n] == m
+ * exactly when nmap[K-1-k, m] == n, and the gradient is the forward
+ * convolution of dout over the same map with the weights of offset k taken
+ * as w[K-1-k] transposed.  Those weights are read in place from w's forward
+ * (K, Ci, Co) layout; nothing is copied.
+ *
+ *  dout_dev    (N, Co) storage type.
+ *  nmap_dev    (K, N) int32, as for spconv_submconv3d (built from a
+ *              point-symmetric, mirrored offset list).
+ *  w_dev       (K, Ci, Co) storage type: the forward weights.
+ *  dfeats_dev  (N, Ci) storage type, written (must not overlap the inputs).
+ *  N, K, Ci, Co, dtype, stream   the forward layer's sizes; requirements,
+ *              tolerance and asynchrony as for spconv_submconv3d (bf16 on
+ *              the tensor cores, f32 / tf32 exact fp32).
+ */
+spconv_status spconv_submconv3d_dgrad(const void* dout_dev, const int32_t* nmap_dev,
+                                      const void* w_dev, void* dfeats_dev, int64_t N, int32_t K,
+                                      int32_t Ci, int32_t Co, spconv_dtype dtype, void* stream);
+
+/*
+ * Gradients with respect to the weights and the bias:
+ *
+ *     dw[k, ci, co] = sum over valid entries m = nmap[k, n] of feats[m, ci] * dout[n, co]
+ *     dbias[co]     = sum_n dout[n, co]
+ *
+ * (the chain rule applied to the formula of spconv_submconv3d and to the
+ * wrapper's bias add; the page computes the forward pass only).  Any offset
+ * list.  Computed exactly in fp32 on CUDA cores from the stored values
+ * (bf16 widened exactly); dw and dbias are fp32 and are overwritten.
+ * Partial sums of voxel slices are combined with fp32 atomic adds, so the
+ * last bits may differ from run to run.
+ *
+ *  feats_dev  (N, Ci) storage type: the forward input.
+ *  dout_dev   (N, Co) storage type: the gradient of the forward output.
+ *  nmap_dev   (K, N) int32, as for spconv_submconv3d.
+ *  dw_dev     (K, Ci, Co) float32, written.
+ *  dbias_dev  (Co,) float32, written, or NULL to skip it.
+ *  N >= 0, K, Ci, Co >= 1; dtype SPCONV_F32, SPCONV_TF32 (same as F32) or
+ *  SPCONV_BF16; feats and dout aligned to their element, dw and dbias to 4
+ *  bytes.  Asynchronous; no allocation, no workspace.
+ */
+spconv_status spconv_submconv3d_wgrad(const void* feats_dev, const void* dout_dev,
+                                      const int32_t* nmap_dev, float* dw_dev, float* dbias_dev,
+                                      int64_t N, int32_t K, int32_t Ci, int32_t Co, spconv_dtype dtype,
+                                      void* stream);
 
 /*
  * Count the entries v of a (K, N) map with 0 <= v < N (the valid pairs that

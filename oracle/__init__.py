@@ -15,6 +15,13 @@ with gcc on first use.  What it follows on the page "sparse_conv_metal.py"
   an entry that is not a valid row contributes nothing, plus the bias the
   wrapper adds.  Returns the exact (fp64) result and the per-output scale
   sum |terms| that the acceptance tolerance is measured against.
+* ``dgrad`` / ``wgrad`` - gradients of ``conv`` with respect to the features
+  and the weights (the chain rule applied to the formula; the page has no
+  backward pass), plain sums in fp64.
+* ``conv_fused`` - ``conv`` followed by the library's fused epilogue,
+  act(conv + bias + residual) with act ReLU or SiLU.  The page defines no
+  epilogue beyond the bias (the conv runs layer after layer inside decoders,
+  module docstring); this is the plain definition of the extension, in fp64.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
 things other than itself: a brute-force neighbour search, a library dense
@@ -82,6 +89,10 @@ def _load():
             lib.oracle_nmap_rows.restype = ctypes.c_int
             lib.oracle_conv.argtypes = [vp, i32, vp, vp, vp, i64, i32, i32, i32, vp, i64, vp, vp]
             lib.oracle_conv.restype = ctypes.c_int
+            lib.oracle_dgrad.argtypes = [vp, i32, vp, vp, i64, i32, i32, i32, vp, i64, vp, vp]
+            lib.oracle_dgrad.restype = ctypes.c_int
+            lib.oracle_wgrad.argtypes = [vp, vp, i32, vp, i64, i32, i32, i32, vp, i64, vp, vp]
+            lib.oracle_wgrad.restype = ctypes.c_int
             lib.oracle_count_valid_pairs.argtypes = [vp, i64, i32]
             lib.oracle_count_valid_pairs.restype = ctypes.c_int64
             _lib = lib
@@ -167,6 +178,117 @@ def conv(feats: np.ndarray, nmap: np.ndarray, w: np.ndarray, bias, dtype: str,
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])), range(threads)))
     return out, sabs
+
+
+# Largest slope of each activation: the error of the pre-activation value is
+# multiplied by at most this much.  SiLU's derivative peaks at ~1.0998
+# (x ~ 2.40).
+ACT_LIPSCHITZ = {"none": 1.0, "relu": 1.0, "silu": 1.1}
+
+
+def widen(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Stored values (float32, or uint16 bf16 bit patterns) as exact float64."""
+    a = np.asarray(a)
+    if dtype == "bf16":
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float32).astype(np.float64)
+
+
+def conv_fused(feats: np.ndarray, nmap: np.ndarray, w: np.ndarray, bias, dtype: str,
+               residual=None, act: str = "none", rows=None, threads: int = 1):
+    """act(conv + bias + residual), exact in fp64.
+
+    ``residual`` (N, Co) holds stored values like ``feats`` (or None);
+    ``act`` is "none", "relu" (max(x, 0)) or "silu" (x / (1 + exp(-x))).
+    Returns ``(out, scale)``: scale = slope bound of ``act`` x (sum |terms| +
+    |bias| + |residual|), the size the acceptance tolerance multiplies.
+    """
+    if act not in ACT_LIPSCHITZ:
+        raise ValueError(f"unknown activation {act!r}")
+    pre, sabs = conv(feats, nmap, w, bias, dtype, rows=rows, threads=threads)
+    if residual is not None:
+        res = widen(residual, dtype)
+        if rows is not None:
+            res = res[np.asarray(rows, dtype=np.int64)]
+        pre = pre + res
+        sabs = sabs + np.abs(res)
+    if act == "relu":
+        out = np.maximum(pre, 0.0)
+    elif act == "silu":
+        with np.errstate(over="ignore"):
+            out = pre / (1.0 + np.exp(-pre))
+    else:
+        out = pre
+    return out, ACT_LIPSCHITZ[act] * sabs
+
+
+def dgrad(dout: np.ndarray, nmap: np.ndarray, w: np.ndarray, dtype: str, rows=None,
+          threads: int = 1):
+    """dfeats[m, ci] = sum over valid entries m = nmap[k, n] of
+    sum_co dout[n, co] * w[k, ci, co], exact (fp64).  ``rows`` selects rows of
+    dfeats (default all).  Returns ``(dfeats, sum |terms|)``."""
+    lib = _load()
+    code = DTYPE_CODE[dtype]
+    sdt = np.uint16 if dtype == "bf16" else np.float32
+    dout = np.ascontiguousarray(dout, dtype=sdt)
+    w = np.ascontiguousarray(w, dtype=sdt)
+    nmap = np.ascontiguousarray(nmap, dtype=np.int32)
+    K, N = nmap.shape
+    Ci, Co = w.shape[1], w.shape[2]
+    if dout.shape != (N, Co) or w.shape[0] != K:
+        raise ValueError("oracle.dgrad: inconsistent shapes")
+    rows = np.arange(N, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    R = rows.shape[0]
+    out = np.empty((R, Ci), dtype=np.float64)
+    dabs = np.empty((R, Ci), dtype=np.float64)
+    if R == 0:
+        return out, dabs
+
+    def run(a, b):
+        rc = lib.oracle_dgrad(_ptr(dout), code, _ptr(nmap), _ptr(w), N, K, Ci, Co, _ptr(rows[a:b]),
+                              b - a, _ptr(out[a:b]), _ptr(dabs[a:b]))
+        if rc != OK:
+            raise OracleError(rc, "dgrad")
+
+    threads = max(1, min(int(threads), R))
+    if threads == 1:
+        run(0, R)
+    else:
+        bounds = np.linspace(0, R, threads + 1).astype(np.int64)
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1])), range(threads)))
+    return out, dabs
+
+
+def wgrad(feats: np.ndarray, dout: np.ndarray, nmap: np.ndarray, dtype: str, entries=None):
+    """dw[k, ci, co] = sum over valid entries of feats[nmap[k, n], ci] *
+    dout[n, co], exact (fp64).  With ``entries`` (flat indices into (K, Ci,
+    Co)) only those values are computed.  Returns ``(dw, sum |terms|)``, of
+    shape (K, Ci, Co) or (len(entries),)."""
+    lib = _load()
+    code = DTYPE_CODE[dtype]
+    sdt = np.uint16 if dtype == "bf16" else np.float32
+    feats = np.ascontiguousarray(feats, dtype=sdt)
+    dout = np.ascontiguousarray(dout, dtype=sdt)
+    nmap = np.ascontiguousarray(nmap, dtype=np.int32)
+    K, N = nmap.shape
+    Ci, Co = feats.shape[1], dout.shape[1]
+    if feats.shape[0] != N or dout.shape[0] != N:
+        raise ValueError("oracle.wgrad: inconsistent shapes")
+    if entries is None:
+        out = np.empty((K, Ci, Co), dtype=np.float64)
+        dabs = np.empty((K, Ci, Co), dtype=np.float64)
+        rc = lib.oracle_wgrad(_ptr(feats), _ptr(dout), code, _ptr(nmap), N, K, Ci, Co, None, 0,
+                              _ptr(out), _ptr(dabs))
+    else:
+        entries = np.ascontiguousarray(entries, dtype=np.int64)
+        out = np.empty(entries.shape[0], dtype=np.float64)
+        dabs = np.empty(entries.shape[0], dtype=np.float64)
+        rc = lib.oracle_wgrad(_ptr(feats), _ptr(dout), code, _ptr(nmap), N, K, Ci, Co, _ptr(entries),
+                              entries.shape[0], _ptr(out), _ptr(dabs))
+    if rc != OK:
+        raise OracleError(rc, "wgrad")
+    return out, dabs
 
 
 def count_valid_pairs(nmap: np.ndarray) -> int:

@@ -29,6 +29,15 @@
  *                      sum |term|, the scale the acceptance tolerance is
  *                      measured against.
  *
+ *   oracle_dgrad       d out / d feats, the adjoint of the formula above:
+ *                      dfeats[m, ci] = sum over valid entries m = nmap[k, n]
+ *                      of sum_co dout[n, co] * w[k, ci, co].
+ *   oracle_wgrad       d out / d w: dw[k, ci, co] = sum over valid entries
+ *                      of feats[nmap[k, n], ci] * dout[n, co].
+ *                      The page computes the forward pass only; these two
+ *                      are the chain rule applied to its formula, written
+ *                      out as plain sums in fp64 (with sum |term| scales).
+ *
  * Readings where the page is silent: a neighbour lies at coords[n] +
  * offsets[k] (cross-correlation); an entry is valid iff 0 <= v < N (the page
  * skips v >= N; negative values are treated the same way instead of being
@@ -220,4 +229,115 @@ int64_t oracle_count_valid_pairs(const int32_t* nmap, int64_t N, int32_t K)
     for (size_t i = 0; i < (size_t)K * (size_t)N; ++i)
         if (nmap[i] >= 0 && nmap[i] < N) ++total;
     return total;
+}
+
+/*
+ * Input gradient.  Computes the rows of dfeats listed in `rows` (all N rows
+ * when rows == NULL): one pass over the whole map picks every valid entry
+ * m = nmap[k, n] whose target m is listed and adds its terms
+ * dout[n, co] * w[k, ci, co].  dabs receives sum |term|.
+ */
+int oracle_dgrad(const void* dout, int32_t dtype, const int32_t* nmap, const void* w, int64_t N,
+                 int32_t K, int32_t Ci, int32_t Co, const int64_t* rows, int64_t n_rows,
+                 double* out, double* dabs)
+{
+    if (N < 1 || K < 1 || Ci < 1 || Co < 1 || dout == NULL || nmap == NULL || w == NULL ||
+        out == NULL || dabs == NULL)
+        return ORACLE_ERR_INVALID_ARG;
+    if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return ORACLE_ERR_INVALID_ARG;
+    int64_t count = rows != NULL ? n_rows : N;
+    int64_t* slot = (int64_t*)malloc((size_t)N * sizeof(int64_t));
+    if (slot == NULL) return ORACLE_ERR_NOMEM;
+    for (int64_t m = 0; m < N; ++m) slot[m] = rows != NULL ? -1 : m;
+    if (rows != NULL) {
+        for (int64_t r = 0; r < count; ++r) {
+            if (rows[r] < 0 || rows[r] >= N) {
+                free(slot);
+                return ORACLE_ERR_INVALID_ARG;
+            }
+            slot[rows[r]] = r;
+        }
+    }
+    memset(out, 0, (size_t)count * (size_t)Ci * sizeof(double));
+    memset(dabs, 0, (size_t)count * (size_t)Ci * sizeof(double));
+    for (int32_t k = 0; k < K; ++k) {
+        for (int64_t n = 0; n < N; ++n) {
+            int64_t m = nmap[(size_t)k * (size_t)N + (size_t)n];
+            if (m < 0 || m >= N || slot[m] < 0) continue;
+            double* o = out + (size_t)slot[m] * (size_t)Ci;
+            double* a = dabs + (size_t)slot[m] * (size_t)Ci;
+            for (int32_t ci = 0; ci < Ci; ++ci) {
+                double acc = 0.0, mag = 0.0;
+                for (int32_t co = 0; co < Co; ++co) {
+                    double g = oracle_widen(dout, dtype, (size_t)n * (size_t)Co + (size_t)co);
+                    double v = oracle_widen(w, dtype,
+                                            ((size_t)k * (size_t)Ci + (size_t)ci) * (size_t)Co +
+                                                (size_t)co);
+                    acc += g * v;
+                    mag += fabs(g * v);
+                }
+                o[ci] += acc;
+                a[ci] += mag;
+            }
+        }
+    }
+    free(slot);
+    return ORACLE_OK;
+}
+
+/*
+ * Weight gradient.  With entries == NULL computes all K * Ci * Co values of
+ * dw (out laid out (K, Ci, Co)); otherwise the listed flat indices
+ * (k * Ci + ci) * Co + co, one sum over all N voxels each.  dabs receives
+ * sum |term|.
+ */
+int oracle_wgrad(const void* feats, const void* dout, int32_t dtype, const int32_t* nmap,
+                 int64_t N, int32_t K, int32_t Ci, int32_t Co, const int64_t* entries,
+                 int64_t n_entries, double* out, double* dabs)
+{
+    if (N < 1 || K < 1 || Ci < 1 || Co < 1 || feats == NULL || dout == NULL || nmap == NULL ||
+        out == NULL || dabs == NULL)
+        return ORACLE_ERR_INVALID_ARG;
+    if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return ORACLE_ERR_INVALID_ARG;
+    if (entries == NULL) {
+        size_t total = (size_t)K * (size_t)Ci * (size_t)Co;
+        memset(out, 0, total * sizeof(double));
+        memset(dabs, 0, total * sizeof(double));
+        for (int32_t k = 0; k < K; ++k) {
+            for (int64_t n = 0; n < N; ++n) {
+                int64_t m = nmap[(size_t)k * (size_t)N + (size_t)n];
+                if (m < 0 || m >= N) continue;
+                for (int32_t ci = 0; ci < Ci; ++ci) {
+                    double f = oracle_widen(feats, dtype, (size_t)m * (size_t)Ci + (size_t)ci);
+                    double* o = out + ((size_t)k * (size_t)Ci + (size_t)ci) * (size_t)Co;
+                    double* a = dabs + ((size_t)k * (size_t)Ci + (size_t)ci) * (size_t)Co;
+                    for (int32_t co = 0; co < Co; ++co) {
+                        double t = f * oracle_widen(dout, dtype, (size_t)n * (size_t)Co + (size_t)co);
+                        o[co] += t;
+                        a[co] += fabs(t);
+                    }
+                }
+            }
+        }
+        return ORACLE_OK;
+    }
+    for (int64_t e = 0; e < n_entries; ++e) {
+        int64_t flat = entries[e];
+        if (flat < 0 || flat >= (int64_t)K * Ci * Co) return ORACLE_ERR_INVALID_ARG;
+        int32_t co = (int32_t)(flat % Co);
+        int32_t ci = (int32_t)((flat / Co) % Ci);
+        int32_t k = (int32_t)(flat / ((int64_t)Co * Ci));
+        double acc = 0.0, mag = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            int64_t m = nmap[(size_t)k * (size_t)N + (size_t)n];
+            if (m < 0 || m >= N) continue;
+            double t = oracle_widen(feats, dtype, (size_t)m * (size_t)Ci + (size_t)ci) *
+                       oracle_widen(dout, dtype, (size_t)n * (size_t)Co + (size_t)co);
+            acc += t;
+            mag += fabs(t);
+        }
+        out[e] = acc;
+        dabs[e] = mag;
+    }
+    return ORACLE_OK;
 }

@@ -78,6 +78,13 @@ def load_library() -> ctypes.CDLL:
         lib.spconv_build_nmap.restype = ctypes.c_int
         lib.spconv_submconv3d.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, ctypes.c_int, vp]
         lib.spconv_submconv3d.restype = ctypes.c_int
+        lib.spconv_submconv3d_ex.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, ctypes.c_int,
+                                             ctypes.c_int, vp]
+        lib.spconv_submconv3d_ex.restype = ctypes.c_int
+        lib.spconv_submconv3d_dgrad.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, ctypes.c_int, vp]
+        lib.spconv_submconv3d_dgrad.restype = ctypes.c_int
+        lib.spconv_submconv3d_wgrad.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, ctypes.c_int, vp]
+        lib.spconv_submconv3d_wgrad.restype = ctypes.c_int
         lib.spconv_count_valid_pairs.argtypes = [vp, i64, i32, vp, vp]
         lib.spconv_count_valid_pairs.restype = ctypes.c_int
         lib.spconv_device_status.argtypes = [vp]
@@ -182,11 +189,19 @@ def _dtype_code(t, dtype):
     return code
 
 
-def submconv3d(feats, nmap, w, bias=None, out=None, dtype=None, stream=None):
+ACTIVATIONS = {None: 0, "none": 0, "relu": 1, "silu": 2}
+
+
+def submconv3d(feats, nmap, w, bias=None, out=None, dtype=None, stream=None, residual=None,
+               activation=None):
     """Fused submanifold convolution.  feats (N, Ci), w (K, Ci, Co), bias (Co,)
     or None, all in one storage dtype (float32 or bfloat16); nmap (K, N) int32.
     ``dtype``: None (float32 -> exact "f32", bfloat16 -> "bf16") or "tf32"
-    for float32 storage with tf32 tensor-core products.  Returns out (N, Co)."""
+    for float32 storage with tf32 tensor-core products.  Returns out (N, Co).
+
+    ``residual`` (N, Co) and ``activation`` ("relu" or "silu") select the
+    fused epilogue out = act(conv + bias + residual) (spconv_submconv3d_ex);
+    ``out`` may be the residual tensor itself."""
     torch = _torch()
     code = _dtype_code(feats, dtype)
     _require_cuda(feats, "feats", feats.dtype)
@@ -202,6 +217,12 @@ def submconv3d(feats, nmap, w, bias=None, out=None, dtype=None, stream=None):
         raise ValueError("inconsistent shapes")
     if bias is not None and tuple(bias.shape) != (co,):
         raise ValueError("bias must have shape (Co,)")
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(a for a in ACTIVATIONS if a)}")
+    if residual is not None:
+        _require_cuda(residual, "residual", feats.dtype)
+        if tuple(residual.shape) != (n, co):
+            raise ValueError("residual must have shape (N, Co)")
     if out is None:
         out = torch.empty((n, co), dtype=feats.dtype, device=feats.device)
     else:
@@ -209,9 +230,61 @@ def submconv3d(feats, nmap, w, bias=None, out=None, dtype=None, stream=None):
         if tuple(out.shape) != (n, co):
             raise ValueError("out must have shape (N, Co)")
     lib = load_library()
-    _check(lib.spconv_submconv3d(_ptr(feats), _ptr(nmap), _ptr(w), _ptr(bias), _ptr(out), n, k, ci,
-                                 co, code, _stream_handle(stream)))
+    act = ACTIVATIONS[activation]
+    if residual is None and act == 0:
+        _check(lib.spconv_submconv3d(_ptr(feats), _ptr(nmap), _ptr(w), _ptr(bias), _ptr(out), n, k,
+                                     ci, co, code, _stream_handle(stream)))
+    else:
+        _check(lib.spconv_submconv3d_ex(_ptr(feats), _ptr(nmap), _ptr(w), _ptr(bias), _ptr(residual),
+                                        _ptr(out), n, k, ci, co, code, act, _stream_handle(stream)))
     return out
+
+
+def submconv3d_dgrad(dout, nmap, w, out=None, dtype=None, stream=None):
+    """Input gradient of submconv3d: dfeats (N, Ci) from dout (N, Co), the
+    forward weights w (K, Ci, Co) and a map built from a point-symmetric,
+    mirrored offset list (such as the default 3x3x3 list)."""
+    torch = _torch()
+    code = _dtype_code(dout, dtype)
+    _require_cuda(dout, "dout", dout.dtype)
+    _require_cuda(nmap, "nmap", torch.int32)
+    _require_cuda(w, "w", dout.dtype)
+    if dout.dim() != 2 or w.dim() != 3 or nmap.dim() != 2:
+        raise ValueError("expected dout (N, Co), nmap (K, N), w (K, Ci, Co)")
+    n, co = dout.shape
+    k, ci = w.shape[0], w.shape[1]
+    if tuple(nmap.shape) != (k, n) or w.shape[2] != co:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((n, ci), dtype=dout.dtype, device=dout.device)
+    else:
+        _require_cuda(out, "out", dout.dtype)
+        if tuple(out.shape) != (n, ci):
+            raise ValueError("out must have shape (N, Ci)")
+    _check(load_library().spconv_submconv3d_dgrad(_ptr(dout), _ptr(nmap), _ptr(w), _ptr(out), n, k, ci,
+                                                   co, code, _stream_handle(stream)))
+    return out
+
+
+def submconv3d_wgrad(feats, dout, nmap, k=None, with_bias=True, stream=None):
+    """Weight (and bias) gradients of submconv3d: returns dw (K, Ci, Co) and,
+    if ``with_bias``, dbias (Co,), both float32, from the forward input feats
+    (N, Ci), dout (N, Co) and the map (K, N)."""
+    torch = _torch()
+    code = _dtype_code(feats, None)
+    _require_cuda(feats, "feats", feats.dtype)
+    _require_cuda(dout, "dout", feats.dtype)
+    _require_cuda(nmap, "nmap", torch.int32)
+    n, ci = feats.shape
+    kk, n2 = nmap.shape
+    if dout.dim() != 2 or dout.shape[0] != n or n2 != n:
+        raise ValueError("expected feats (N, Ci), dout (N, Co), nmap (K, N)")
+    co = dout.shape[1]
+    dw = torch.empty((kk, ci, co), dtype=torch.float32, device=feats.device)
+    db = torch.empty((co,), dtype=torch.float32, device=feats.device) if with_bias else None
+    _check(load_library().spconv_submconv3d_wgrad(_ptr(feats), _ptr(dout), _ptr(nmap), _ptr(dw), _ptr(db),
+                                                   n, kk, ci, co, code, _stream_handle(stream)))
+    return (dw, db) if with_bias else dw
 
 
 def count_valid_pairs(nmap, stream=None) -> int:

@@ -7,9 +7,15 @@
 // tile; for each offset k it stages the 64 neighbour indices, skips k when
 // none is valid, gathers the rows chunk by chunk into shared memory (rows
 // that are not valid become zeros) and accumulates with FFMA, 4 x 4 outputs
-// per thread.  Each output accumulates over k, then ci, in order.
+// per thread.  Each output accumulates over k, then ci, in order.  The
+// epilogue adds the bias and, for the fused-epilogue entry point, a residual
+// row and an activation, in fp32.  With `dgrad` set the same loop computes
+// the input gradient: the gathered rows are dout rows and the weights of
+// offset k are w[K-1-k] transposed, read in place from the (K, Ci, Co)
+// forward layout (here ci counts dout channels and co dfeats channels).
 #include <cuda_runtime.h>
 
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace spconv {
@@ -23,8 +29,8 @@ constexpr int kThreads = 256;
 __global__ void __launch_bounds__(kThreads)
     submconv_simt_f32_kernel(const float* __restrict__ feats, const int32_t* __restrict__ nmap,
                              const float* __restrict__ w, const float* __restrict__ bias,
-                             float* __restrict__ out, int64_t n, int32_t k_count, int32_t ci,
-                             int32_t co) {
+                             const float* residual, float* out, int64_t n, int32_t k_count,
+                             int32_t ci, int32_t co, int act, int dgrad) {
   __shared__ int32_t idx[kBM];
   __shared__ float as[kBK][kBM + 4];
   __shared__ float bs[kBK][kBN];
@@ -69,7 +75,8 @@ __global__ void __launch_bounds__(kThreads)
         const int c = e % kBN;
         float v = 0.0f;
         if (c0 + r < ci && col0 + c < co)
-          v = w[(static_cast<int64_t>(k) * ci + c0 + r) * co + col0 + c];
+          v = dgrad ? w[(static_cast<int64_t>(k_count - 1 - k) * co + col0 + c) * ci + c0 + r]
+                    : w[(static_cast<int64_t>(k) * ci + c0 + r) * co + col0 + c];
         bs[r][c] = v;
       }
       __syncthreads();
@@ -96,7 +103,12 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int c = col0 + tc * 4 + j;
-      if (c < co) out[r * co + c] = acc[i][j] + (bias != nullptr ? bias[c] : 0.0f);
+      if (c >= co) continue;
+      // residual may be the same buffer as out: each element is read and
+      // then written by this thread only.
+      float x = acc[i][j] + (bias != nullptr ? bias[c] : 0.0f);
+      if (residual != nullptr) x += residual[r * co + c];
+      out[r * co + c] = apply_activation(x, act);
     }
   }
 }
@@ -104,14 +116,16 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 
 spconv_status launch_conv_simt_f32(const float* feats, const int32_t* nmap, const float* w,
-                                   const float* bias, float* out, int64_t n, int32_t k,
-                                   int32_t ci, int32_t co, cudaStream_t stream) {
+                                   const float* bias, const float* residual, float* out,
+                                   int64_t n, int32_t k, int32_t ci, int32_t co,
+                                   spconv_activation act, bool dgrad, cudaStream_t stream) {
   const int64_t gx = (n + kBM - 1) / kBM;
   const int gy = (co + kBN - 1) / kBN;
   if (gx > 0x7fffffff || gy > 65535)
     return fail(SPCONV_ERR_UNSUPPORTED, "problem too large for the fp32 grid");
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
-  submconv_simt_f32_kernel<<<grid, kThreads, 0, stream>>>(feats, nmap, w, bias, out, n, k, ci, co);
+  submconv_simt_f32_kernel<<<grid, kThreads, 0, stream>>>(feats, nmap, w, bias, residual, out, n, k, ci,
+                                                          co, static_cast<int>(act), dgrad ? 1 : 0);
   spconv_status st = SPCONV_OK;
   if (!cuda_ok(cudaGetLastError(), "submconv_simt_f32_kernel launch", &st)) return st;
   return SPCONV_OK;

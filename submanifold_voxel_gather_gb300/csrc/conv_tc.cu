@@ -31,8 +31,9 @@
 //              the next tile's main loop (two M blocks fill all 512 columns
 //              with one buffer: measured faster than N = 128 with two, which
 //              doubles the weight traffic per voxel).
-//   warps 4-7  epilogue: tcgen05.ld (lane = channel, column = voxel), + bias,
-//              one rounding to bf16, transpose through shared memory,
+//   warps 4-7  epilogue: tcgen05.ld (lane = channel, column = voxel), + bias
+//              (+ residual row and activation for the fused-epilogue entry
+//              point), one rounding to bf16, transpose through shared memory,
 //              coalesced 16-byte stores.
 //
 // The gathered (K, N, Ci) operand only ever exists one stage at a time in
@@ -47,6 +48,7 @@
 
 #include <mutex>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -76,6 +78,7 @@ struct TcParams {
   const __nv_bfloat16* feats;
   const int32_t* nmap;
   const __nv_bfloat16* bias;
+  const __nv_bfloat16* residual;  // (N, co) or null; may alias out
   __nv_bfloat16* out;
   int64_t n;
   int64_t num_tiles;
@@ -84,6 +87,8 @@ struct TcParams {
   int32_t co;        // row stride of out
   int32_t co_base;   // first output channel of this launch
   int32_t co_count;  // channels of this launch (<= 256)
+  int32_t act;       // spconv_activation
+  int32_t dgrad;     // input gradient: selects the kDgrad instantiation
   int32_t num_chunks;
   uint32_t stages;
   uint32_t stage_bytes;
@@ -127,7 +132,9 @@ __device__ __forceinline__ bool issue_row(uint32_t flag, int kk, int k_count, bo
 // kHoist: the per-row source index and byte count are computed once per
 // offset instead of once per chunk (used when an offset has two or more
 // 128-byte chunks; with one chunk the in-loop form is measured faster).
-template <int TILE_N, int MBLK, bool kHoist>
+// kDgrad: input gradient; the weights of offset k are w[K-1-k] transposed,
+// read from the forward layout as a K-major operand.
+template <int TILE_N, int MBLK, bool kHoist, bool kDgrad>
 __global__ void __launch_bounds__(kThreads, 1)
     submconv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const TcParams p) {
   constexpr int kRowsPerWarp = TILE_N / 4;       // gathered rows per producer warp
@@ -350,10 +357,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(fullb, p.w_bytes);
           }
           __syncwarp();
-          if (static_cast<int>(lane) < 2 * MBLK) {
-            const int mb = static_cast<int>(lane) >> 1, half = static_cast<int>(lane) & 1;
-            tma_load_3d(smem_addr(smem + stage * p.stage_bytes) + mb * kWBlockBytes + half * 8192u,
-                        &tm_w, p.co_base + mb * 128 + half * 64, c * kChunk, kk, fullb);
+          if constexpr (!kDgrad) {
+            // forward: w[k] channel-major, two 64-channel boxes per M block
+            if (static_cast<int>(lane) < 2 * MBLK) {
+              const int mb = static_cast<int>(lane) >> 1, half = static_cast<int>(lane) & 1;
+              tma_load_3d(smem_addr(smem + stage * p.stage_bytes) + mb * kWBlockBytes + half * 8192u,
+                          &tm_w, p.co_base + mb * 128 + half * 64, c * kChunk, kk, fullb);
+            }
+          } else if (static_cast<int>(lane) < MBLK) {
+            // input gradient: rows of w[K-1-k] (output channel = forward ci)
+            // with 64 of their forward-co entries each, K-major
+            const int mb = static_cast<int>(lane);
+            tma_load_3d(smem_addr(smem + stage * p.stage_bytes) + mb * kWBlockBytes, &tm_w, c * kChunk,
+                        p.co_base + mb * 128, k_count - 1 - kk, fullb);
           }
           issued = true;
           ++fills;
@@ -377,7 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // Descriptors of stage 0; a stage or K step only moves the start
       // address (the low 14 bits, in 16-byte units), so advancing is one add.
-      const uint64_t adesc0 = sw128_desc(smem_addr(smem), 8192u, 1024u);
+      // Weights channel-major (forward) or K-major (input gradient).
+      const uint64_t adesc0 = sw128_desc(smem_addr(smem), kDgrad ? 16u : 8192u, 1024u);
+      constexpr uint64_t a_step = kDgrad ? kBStepUnits : kAStepUnits;
       const uint64_t bdesc0 = sw128_desc(smem_addr(smem) + p.w_bytes, 16u, 1024u);
       const uint64_t stage_units = p.stage_bytes >> 4;
       const uint32_t idesc = p.idesc;
@@ -416,13 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int s = 0; s < kChunk / kKPerMma; ++s)
 #pragma unroll
             for (int mb = 0; mb < MBLK; ++mb)
-              umma_f16(d_tmem + mb * TILE_N, ad + mb * kWBlockUnits + s * kAStepUnits,
+              umma_f16(d_tmem + mb * TILE_N, ad + mb * kWBlockUnits + s * a_step,
                        bd + s * kBStepUnits, idesc, s > 0 ? 1u : acc0);
         } else {
           for (int s = 0; s < steps; ++s)
 #pragma unroll
             for (int mb = 0; mb < MBLK; ++mb)
-              umma_f16(d_tmem + mb * TILE_N, ad + mb * kWBlockUnits + s * kAStepUnits,
+              umma_f16(d_tmem + mb * TILE_N, ad + mb * kWBlockUnits + s * a_step,
                        bd + s * kBStepUnits, idesc, s > 0 ? 1u : acc0);
         }
         umma_commit(smem_addr(&empty[stage]));
@@ -442,6 +460,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sub = warp & 3u;
     const int et = static_cast<int>(threadIdx.x) - kEpilogueWarp0 * 32;  // 0..127
     const int chunks_per_row = p.co_count / 8;                           // 16-byte chunks
+    const bool fused = p.residual != nullptr || p.act != SPCONV_ACT_NONE;
+    // Fused epilogue (residual and/or activation): one 128-channel block at a
+    // time is staged in fp32 (32 rows x 128, 16 KB), and the store phase adds
+    // the residual, read as 16-byte pieces of its rows (coalesced, few load
+    // instructions: the load/store pipe is shared with the gather), applies
+    // the activation and rounds once.  Each thread reads and writes the same
+    // (row, piece) pairs, residual first, so the residual may be the output.
+    // The next chunk's pieces are loaded as soon as the current ones are used.
+    float* stage_f = reinterpret_cast<float*>(stage_out);
+    uint4 res[MBLK][4];
+    auto load_residual = [&](int mb, int64_t nb) {
+      const int ppr = min(128, p.co_count - mb * 128) / 8;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int q = et + 128 * j;
+        res[mb][j] = make_uint4(0u, 0u, 0u, 0u);
+        if (p.residual != nullptr && q < 32 * ppr) {
+          const int r = q / ppr;
+          const int c8 = q - r * ppr;
+          if (nb + r < n_rows)
+            res[mb][j] = __ldg(reinterpret_cast<const uint4*>(p.residual + (nb + r) * p.co + p.co_base +
+                                                              mb * 128 + c8 * 8));
+        }
+      }
+    };
     uint32_t tile_i = 0;
     for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tile_i) {
       const uint32_t buf = tile_i % kAccBufs;
@@ -450,29 +493,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int64_t n0 = t * TILE_N;
       const uint32_t tcol = tmem_base + ((sub * 32u) << 16) + buf * static_cast<uint32_t>(MBLK * TILE_N);
-      for (int vc = 0; vc < TILE_N / 32; ++vc) {
-        epilogue_bar();  // the previous chunk's staged rows have been stored
+      if (!fused) {
+        for (int vc = 0; vc < TILE_N / 32; ++vc) {
+          epilogue_bar();  // the previous chunk's staged rows have been stored
 #pragma unroll
-        for (int mb = 0; mb < MBLK; ++mb) {
-          const int co_l = mb * 128 + static_cast<int>(sub) * 32 + static_cast<int>(lane);
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tcol + mb * TILE_N + vc * 32, v);
-          tmem_ld_wait();
-          if (co_l < p.co_count) {
-            const float b = bias_s[co_l];
+          for (int mb = 0; mb < MBLK; ++mb) {
+            const int co_l = mb * 128 + static_cast<int>(sub) * 32 + static_cast<int>(lane);
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tcol + mb * TILE_N + vc * 32, v);
+            tmem_ld_wait();
+            if (co_l < p.co_count) {
+              const float b = bias_s[co_l];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              stage_out[i * kOutStride + co_l] = __float2bfloat16_rn(__uint_as_float(v[i]) + b);
+              for (int i = 0; i < 32; ++i)
+                stage_out[i * kOutStride + co_l] = __float2bfloat16_rn(__uint_as_float(v[i]) + b);
+            }
+          }
+          epilogue_bar();
+          for (int q = et; q < 32 * chunks_per_row; q += 128) {
+            const int r = q / chunks_per_row;
+            const int c8 = q - r * chunks_per_row;
+            const int64_t n = n0 + vc * 32 + r;
+            if (n < n_rows)
+              *reinterpret_cast<uint4*>(p.out + n * p.co + p.co_base + c8 * 8) =
+                  *reinterpret_cast<const uint4*>(stage_out + r * kOutStride + c8 * 8);
           }
         }
-        epilogue_bar();
-        for (int q = et; q < 32 * chunks_per_row; q += 128) {
-          const int r = q / chunks_per_row;
-          const int c8 = q - r * chunks_per_row;
-          const int64_t n = n0 + vc * 32 + r;
-          if (n < n_rows)
-            *reinterpret_cast<uint4*>(p.out + n * p.co + p.co_base + c8 * 8) =
-                *reinterpret_cast<const uint4*>(stage_out + r * kOutStride + c8 * 8);
+      } else {
+#pragma unroll
+        for (int mb = 0; mb < MBLK; ++mb) load_residual(mb, n0);
+        for (int vc = 0; vc < TILE_N / 32; ++vc) {
+          const int64_t nb = n0 + vc * 32;
+#pragma unroll
+          for (int mb = 0; mb < MBLK; ++mb) {
+            const int ppr = min(128, p.co_count - mb * 128) / 8;
+            const int co_s = static_cast<int>(sub) * 32 + static_cast<int>(lane);
+            epilogue_bar();  // the staging buffer is free
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tcol + mb * TILE_N + vc * 32, v);
+            tmem_ld_wait();
+            const float b = bias_s[mb * 128 + co_s];  // zero beyond co_count
+#pragma unroll
+            for (int i = 0; i < 32; ++i) stage_f[i * 128 + co_s] = __uint_as_float(v[i]) + b;
+            epilogue_bar();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int q = et + 128 * j;
+              if (q >= 32 * ppr) continue;
+              const int r = q / ppr;
+              const int c8 = q - r * ppr;
+              if (nb + r >= n_rows) continue;
+              const float4 a0 = *reinterpret_cast<const float4*>(stage_f + r * 128 + c8 * 8);
+              const float4 a1 = *reinterpret_cast<const float4*>(stage_f + r * 128 + c8 * 8 + 4);
+              const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+              const uint32_t rw[4] = {res[mb][j].x, res[mb][j].y, res[mb][j].z, res[mb][j].w};
+              uint32_t o[4];
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const float lo = apply_activation_bf16(x[2 * h] + __uint_as_float(rw[h] << 16), p.act);
+                const float hi =
+                    apply_activation_bf16(x[2 * h + 1] + __uint_as_float(rw[h] & 0xFFFF0000u), p.act);
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+                o[h] = *reinterpret_cast<const uint32_t*>(&pr);
+              }
+              *reinterpret_cast<uint4*>(p.out + (nb + r) * p.co + p.co_base + mb * 128 + c8 * 8) =
+                  make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            if (vc + 1 < TILE_N / 32) load_residual(mb, nb + 32);
+          }
         }
       }
       tc_fence_before();
@@ -518,7 +606,7 @@ EncodeTiledFn encode_fn(spconv_status* st) {
   return fn;
 }
 
-template <int TILE_N, int MBLK, bool kHoist>
+template <int TILE_N, int MBLK, bool kHoist, bool kDgrad>
 spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t stream) {
   const int sms = sm_count();
   if (sms <= 0) return fail(SPCONV_ERR_CUDA, "could not query the SM count");
@@ -527,12 +615,17 @@ spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t str
   p.w_bytes = MBLK * kWBlockBytes;
   p.stage_bytes = p.w_bytes + TILE_N * 128u;
   p.tmem_cols = 512u;  // kAccBufs accumulator buffers of MBLK x TILE_N columns
-  // D f32, A and B bf16, A (weights) channel-major, B (gathered rows) K-major.
-  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) |
+  // D f32, A and B bf16, B (gathered rows) K-major; A (weights) channel-major
+  // for the forward pass, K-major for the input gradient.
+  const uint32_t a_mn_major = kDgrad ? 0u : 1u;
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major << 15) |
             ((static_cast<uint32_t>(TILE_N) >> 3) << 17) | ((128u >> 4) << 24);
 
   const uint32_t ring_bytes = kRing * TILE_N * 4u;
-  const uint32_t stage_out_bytes = 32u * MBLK * 128u * 2u;
+  // 32 staged output rows: bf16 for all channels, or fp32 for one 128-channel
+  // block (fused epilogue); the larger of the two.
+  const uint32_t stage_out_bytes = (32u * MBLK * 128u * 2u > 32u * 128u * 4u) ? 32u * MBLK * 128u * 2u
+                                                                              : 32u * 128u * 4u;
   const uint32_t fixed = ring_bytes + stage_out_bytes + 256u * 4u + (kMaxStages + kRing) * 4u +
                          (2u * kMaxStages + 2u * kRing + 5u) * 8u + 16u + 1024u;
   uint32_t stages = (kMaxSmem - fixed) / p.stage_bytes;
@@ -553,7 +646,7 @@ spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t str
   off += (2u * stages + 2u * kRing + 5u) * 8u + 16u;
   const uint32_t smem_bytes = off + 1024u;  // slack for the 1024-byte alignment
 
-  auto kern = submconv_tc_kernel<TILE_N, MBLK, kHoist>;
+  auto kern = submconv_tc_kernel<TILE_N, MBLK, kHoist, kDgrad>;
   spconv_status st = SPCONV_OK;
   if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem_bytes)),
@@ -562,6 +655,12 @@ spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t str
   kern<<<grid, kThreads, smem_bytes, stream>>>(tm_w, p);
   if (!cuda_ok(cudaGetLastError(), "submconv_tc_kernel launch", &st)) return st;
   return SPCONV_OK;
+}
+
+template <int MBLK, bool kHoist>
+spconv_status launch_dir(const CUtensorMap& tm_w, const TcParams& p, cudaStream_t stream) {
+  return p.dgrad != 0 ? launch_shape<256, MBLK, kHoist, true>(tm_w, p, stream)
+                      : launch_shape<256, MBLK, kHoist, false>(tm_w, p, stream);
 }
 
 }  // namespace
@@ -580,20 +679,25 @@ spconv_status read_and_clear_device_error(cudaStream_t stream, unsigned int* bit
 }
 
 spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_t* nmap,
-                             const void* w, const void* bias, void* out, int64_t n, int32_t k,
-                             int32_t ci, int32_t co, cudaStream_t stream) {
+                             const void* w, const void* bias, const void* residual, void* out,
+                             int64_t n, int32_t k, int32_t ci, int32_t co, spconv_activation act,
+                             bool dgrad, cudaStream_t stream) {
   if (dtype != SPCONV_BF16) return fail(SPCONV_ERR_UNSUPPORTED, "tensor-core path supports bf16 only");
   spconv_status st = SPCONV_OK;
   EncodeTiledFn encode = encode_fn(&st);
   if (encode == nullptr) return st;
 
-  // w viewed as (K, Ci, Co): box = 64 channels x 64 input channels of one
-  // offset, 128-byte swizzle (the channel-major UMMA operand layout).
+  // w viewed as its (K, Ci_fwd, Co_fwd) layout, innermost Co_fwd.  Forward:
+  // box = 64 output channels x 64 input channels of one offset (the
+  // channel-major UMMA operand).  Input gradient (ci = Co_fwd, co = Ci_fwd):
+  // box = 64 forward-co x 128 forward-ci, i.e. 128 output rows with 64 input
+  // channels each (the K-major operand).  128-byte swizzle in both.
+  const cuuint64_t wi = static_cast<cuuint64_t>(dgrad ? co : ci);  // forward Ci
+  const cuuint64_t wo = static_cast<cuuint64_t>(dgrad ? ci : co);  // forward Co
   CUtensorMap tm_w;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(co), static_cast<cuuint64_t>(ci),
-                        static_cast<cuuint64_t>(k)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(co) * 2, static_cast<cuuint64_t>(ci) * co * 2};
-  cuuint32_t box[3] = {64, 64, 1};
+  cuuint64_t dims[3] = {wo, wi, static_cast<cuuint64_t>(k)};
+  cuuint64_t strides[2] = {wo * 2, wi * wo * 2};
+  cuuint32_t box[3] = {64, dgrad ? 128u : 64u, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides,
                       box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -606,6 +710,9 @@ spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_
     p.feats = static_cast<const __nv_bfloat16*>(feats);
     p.nmap = nmap;
     p.bias = static_cast<const __nv_bfloat16*>(bias);
+    p.residual = static_cast<const __nv_bfloat16*>(residual);
+    p.act = static_cast<int32_t>(act);
+    p.dgrad = dgrad ? 1 : 0;
     p.out = static_cast<__nv_bfloat16*>(out);
     p.n = n;
     p.k = k;
@@ -616,9 +723,9 @@ spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_
     p.num_chunks = (ci + kChunk - 1) / kChunk;
     const bool hoist = p.num_chunks >= 2;
     if (p.co_count <= 128)
-      st = hoist ? launch_shape<256, 1, true>(tm_w, p, stream) : launch_shape<256, 1, false>(tm_w, p, stream);
+      st = hoist ? launch_dir<1, true>(tm_w, p, stream) : launch_dir<1, false>(tm_w, p, stream);
     else
-      st = hoist ? launch_shape<256, 2, true>(tm_w, p, stream) : launch_shape<256, 2, false>(tm_w, p, stream);
+      st = hoist ? launch_dir<2, true>(tm_w, p, stream) : launch_dir<2, false>(tm_w, p, stream);
     if (st != SPCONV_OK) return st;
   }
   return SPCONV_OK;

@@ -36,13 +36,22 @@ spconv_status launch_count_valid_pairs(const int32_t* nmap, int64_t n, int32_t k
 
 // ---- exact fp32 convolution on CUDA cores (conv_simt.cu)
 spconv_status launch_conv_simt_f32(const float* feats, const int32_t* nmap, const float* w,
-                                   const float* bias, float* out, int64_t n, int32_t k,
-                                   int32_t ci, int32_t co, cudaStream_t stream);
+                                   const float* bias, const float* residual, float* out,
+                                   int64_t n, int32_t k, int32_t ci, int32_t co,
+                                   spconv_activation act, bool dgrad, cudaStream_t stream);
 
-// ---- tensor-core convolution (conv_tc.cu); dtype is SPCONV_BF16 or SPCONV_TF32
+// ---- tensor-core convolution (conv_tc.cu); dtype is SPCONV_BF16.  With
+// dgrad, ci/co are the dout/dfeats widths (forward Co/Ci), feats is dout and
+// the weights of offset k are w[K-1-k] transposed (forward layout in place).
 spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_t* nmap,
-                             const void* w, const void* bias, void* out, int64_t n, int32_t k,
-                             int32_t ci, int32_t co, cudaStream_t stream);
+                             const void* w, const void* bias, const void* residual, void* out,
+                             int64_t n, int32_t k, int32_t ci, int32_t co, spconv_activation act,
+                             bool dgrad, cudaStream_t stream);
+
+// ---- weight / bias gradients, exact fp32 on CUDA cores (wgrad_simt.cu)
+spconv_status launch_wgrad_simt(spconv_dtype dtype, const void* feats, const void* dout,
+                                const int32_t* nmap, float* dw, float* dbias, int64_t n, int32_t k,
+                                int32_t ci, int32_t co, cudaStream_t stream);
 
 // ---- device error word (ptx.cuh declares the symbol)
 spconv_status read_and_clear_device_error(cudaStream_t stream, unsigned int* bits);

@@ -154,44 +154,120 @@ spconv_status spconv_build_nmap_noalloc(const int32_t* coords_dev, int64_t N,
   return st == SPCONV_OK ? spconv::ok() : st;
 }
 
-spconv_status spconv_submconv3d(const void* feats_dev, const int32_t* nmap_dev, const void* w_dev,
-                                const void* bias_dev, void* out_dev, int64_t N, int32_t K,
-                                int32_t Ci, int32_t Co, spconv_dtype dtype, void* stream) {
+namespace spconv {
+namespace {
+
+// Shared validation and dispatch of spconv_submconv3d, _ex and _dgrad.  Ci
+// and Co are the widths of the gathered input rows and of the output rows
+// (for the input gradient: the forward Co and Ci).
+spconv_status submconv3d_impl(const void* feats_dev, const int32_t* nmap_dev, const void* w_dev,
+                              const void* bias_dev, const void* residual_dev, void* out_dev, int64_t N,
+                              int32_t K, int32_t Ci, int32_t Co, spconv_dtype dtype,
+                              spconv_activation act, bool dgrad, void* stream) {
   if (N < 0 || N >= INT32_MAX) return fail(SPCONV_ERR_INVALID_ARG, "N must satisfy 0 <= N < 2^31-1");
   if (K < 1 || Ci < 1 || Co < 1) return fail(SPCONV_ERR_INVALID_ARG, "K, Ci and Co must be >= 1");
   if (dtype != SPCONV_F32 && dtype != SPCONV_TF32 && dtype != SPCONV_BF16)
     return fail(SPCONV_ERR_INVALID_ARG, "unknown dtype");
-  if (N == 0) return spconv::ok();
+  if (act != SPCONV_ACT_NONE && act != SPCONV_ACT_RELU && act != SPCONV_ACT_SILU)
+    return fail(SPCONV_ERR_INVALID_ARG, "unknown activation");
+  if (N == 0) return ok();
   if (feats_dev == nullptr || nmap_dev == nullptr || w_dev == nullptr || out_dev == nullptr)
     return fail(SPCONV_ERR_INVALID_ARG, "feats, nmap, w and out must be non-NULL");
-  if (!spconv::aligned(nmap_dev, 4)) return fail(SPCONV_ERR_INVALID_ARG, "nmap must be 4-byte aligned");
+  if (!aligned(nmap_dev, 4)) return fail(SPCONV_ERR_INVALID_ARG, "nmap must be 4-byte aligned");
   const size_t elem = dtype == SPCONV_BF16 ? 2 : 4;
   if (static_cast<uint64_t>(N) * static_cast<uint64_t>(K) > (1ull << 40))
     return fail(SPCONV_ERR_UNSUPPORTED, "K * N too large");
+  if (residual_dev != nullptr && !aligned(residual_dev, dtype == SPCONV_F32 ? 4 : 16))
+    return fail(SPCONV_ERR_INVALID_ARG, "residual is misaligned (needs the alignment of out)");
   if (dtype == SPCONV_F32) {
-    if (!spconv::aligned(feats_dev, 4) || !spconv::aligned(w_dev, 4) || !spconv::aligned(out_dev, 4) ||
-        (bias_dev != nullptr && !spconv::aligned(bias_dev, 4)))
+    if (!aligned(feats_dev, 4) || !aligned(w_dev, 4) || !aligned(out_dev, 4) ||
+        (bias_dev != nullptr && !aligned(bias_dev, 4)))
       return fail(SPCONV_ERR_INVALID_ARG, "fp32 arrays must be 4-byte aligned");
   } else {
     if (Ci % 16 != 0 || Co % 16 != 0)
       return fail(SPCONV_ERR_UNSUPPORTED, "bf16/tf32 need Ci and Co to be multiples of 16");
-    if (!spconv::aligned(feats_dev, 16) || !spconv::aligned(w_dev, 16) || !spconv::aligned(out_dev, 16))
+    if (!aligned(feats_dev, 16) || !aligned(w_dev, 16) || !aligned(out_dev, 16))
       return fail(SPCONV_ERR_INVALID_ARG, "feats, w and out must be 16-byte aligned");
-    if (bias_dev != nullptr && !spconv::aligned(bias_dev, elem))
+    if (bias_dev != nullptr && !aligned(bias_dev, elem))
       return fail(SPCONV_ERR_INVALID_ARG, "bias is misaligned");
   }
-  spconv_status st = spconv::check_device();
+  spconv_status st = check_device();
   if (st != SPCONV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // SPCONV_TF32 runs the exact fp32 kernel for now (its results are within
   // the tf32 tolerance); the tensor-core tf32 variant is not enabled.
   if (dtype == SPCONV_F32 || dtype == SPCONV_TF32)
-    st = spconv::launch_conv_simt_f32(static_cast<const float*>(feats_dev), nmap_dev,
-                                      static_cast<const float*>(w_dev),
-                                      static_cast<const float*>(bias_dev), static_cast<float*>(out_dev),
-                                      N, K, Ci, Co, s);
+    st = launch_conv_simt_f32(static_cast<const float*>(feats_dev), nmap_dev,
+                              static_cast<const float*>(w_dev), static_cast<const float*>(bias_dev),
+                              static_cast<const float*>(residual_dev), static_cast<float*>(out_dev), N,
+                              K, Ci, Co, act, dgrad, s);
   else
-    st = spconv::launch_conv_tc(dtype, feats_dev, nmap_dev, w_dev, bias_dev, out_dev, N, K, Ci, Co, s);
+    st = launch_conv_tc(dtype, feats_dev, nmap_dev, w_dev, bias_dev, residual_dev, out_dev, N, K, Ci,
+                        Co, act, dgrad, s);
+  return st == SPCONV_OK ? ok() : st;
+}
+
+}  // namespace
+}  // namespace spconv
+
+spconv_status spconv_submconv3d(const void* feats_dev, const int32_t* nmap_dev, const void* w_dev,
+                                const void* bias_dev, void* out_dev, int64_t N, int32_t K,
+                                int32_t Ci, int32_t Co, spconv_dtype dtype, void* stream) {
+  return spconv::submconv3d_impl(feats_dev, nmap_dev, w_dev, bias_dev, nullptr, out_dev, N, K, Ci, Co,
+                                 dtype, SPCONV_ACT_NONE, false, stream);
+}
+
+spconv_status spconv_submconv3d_ex(const void* feats_dev, const int32_t* nmap_dev,
+                                   const void* w_dev, const void* bias_dev,
+                                   const void* residual_dev, void* out_dev, int64_t N, int32_t K,
+                                   int32_t Ci, int32_t Co, spconv_dtype dtype,
+                                   spconv_activation act, void* stream) {
+  return spconv::submconv3d_impl(feats_dev, nmap_dev, w_dev, bias_dev, residual_dev, out_dev, N, K, Ci,
+                                 Co, dtype, act, false, stream);
+}
+
+spconv_status spconv_submconv3d_dgrad(const void* dout_dev, const int32_t* nmap_dev,
+                                      const void* w_dev, void* dfeats_dev, int64_t N, int32_t K,
+                                      int32_t Ci, int32_t Co, spconv_dtype dtype, void* stream) {
+  // The same convolution over dout with the weights of offset k taken as
+  // w[K-1-k] transposed: rows of width Co in, rows of width Ci out.
+  return spconv::submconv3d_impl(dout_dev, nmap_dev, w_dev, nullptr, nullptr, dfeats_dev, N, K, Co, Ci,
+                                 dtype, SPCONV_ACT_NONE, true, stream);
+}
+
+spconv_status spconv_submconv3d_wgrad(const void* feats_dev, const void* dout_dev,
+                                      const int32_t* nmap_dev, float* dw_dev, float* dbias_dev,
+                                      int64_t N, int32_t K, int32_t Ci, int32_t Co, spconv_dtype dtype,
+                                      void* stream) {
+  if (N < 0 || N >= INT32_MAX) return fail(SPCONV_ERR_INVALID_ARG, "N must satisfy 0 <= N < 2^31-1");
+  if (K < 1 || Ci < 1 || Co < 1) return fail(SPCONV_ERR_INVALID_ARG, "K, Ci and Co must be >= 1");
+  if (dtype != SPCONV_F32 && dtype != SPCONV_TF32 && dtype != SPCONV_BF16)
+    return fail(SPCONV_ERR_INVALID_ARG, "unknown dtype");
+  if (dw_dev == nullptr) return fail(SPCONV_ERR_INVALID_ARG, "dw must be non-NULL");
+  if (N > 0 && (feats_dev == nullptr || dout_dev == nullptr || nmap_dev == nullptr))
+    return fail(SPCONV_ERR_INVALID_ARG, "feats, dout and nmap must be non-NULL");
+  const size_t elem = dtype == SPCONV_BF16 ? 2 : 4;
+  if (!spconv::aligned(feats_dev, elem) || !spconv::aligned(dout_dev, elem) ||
+      !spconv::aligned(nmap_dev, 4) || !spconv::aligned(dw_dev, 4) ||
+      (dbias_dev != nullptr && !spconv::aligned(dbias_dev, 4)))
+    return fail(SPCONV_ERR_INVALID_ARG, "misaligned array");
+  if (static_cast<uint64_t>(N) * static_cast<uint64_t>(K) > (1ull << 40))
+    return fail(SPCONV_ERR_UNSUPPORTED, "K * N too large");
+  spconv_status st = spconv::check_device();
+  if (st != SPCONV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    // no voxels: the gradients are zero
+    if (!spconv::cuda_ok(cudaMemsetAsync(dw_dev, 0, static_cast<size_t>(K) * Ci * Co * sizeof(float), s),
+                         "cudaMemsetAsync(dw)", &st))
+      return st;
+    if (dbias_dev != nullptr &&
+        !spconv::cuda_ok(cudaMemsetAsync(dbias_dev, 0, static_cast<size_t>(Co) * sizeof(float), s),
+                         "cudaMemsetAsync(dbias)", &st))
+      return st;
+    return spconv::ok();
+  }
+  st = spconv::launch_wgrad_simt(dtype, feats_dev, dout_dev, nmap_dev, dw_dev, dbias_dev, N, K, Ci, Co, s);
   return st == SPCONV_OK ? spconv::ok() : st;
 }
 

@@ -30,7 +30,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("spconv_build_nmap", "spconv_submconv3d", "spconv_build_nmap_workspace_size",
                      "spconv_last_error", "spconv_version", "spconv_count_valid_pairs",
-                     "spconv_device_status"):
+                     "spconv_device_status", "spconv_submconv3d_ex", "spconv_submconv3d_dgrad",
+                     "spconv_submconv3d_wgrad"):
         assert required in names
 
 
@@ -79,6 +80,27 @@ def test_argument_validation_without_gpu(lib):
     assert code == -1 and "aligned" in msg
     assert _status(lib.spconv_submconv3d(None, fake, fake, None, fake, 10, 27, 16, 16, 0, None))[0] == -1
     assert _status(lib.spconv_submconv3d(None, None, None, None, None, 0, 27, 16, 16, 2, None))[0] == 0
+    # submconv3d_ex: same checks plus the activation code and residual alignment
+    ex = lib.spconv_submconv3d_ex
+    assert _status(ex(fake, fake, fake, None, None, fake, 10, 27, 16, 16, 2, 3, None))[0] == -1
+    assert _status(ex(fake, fake, fake, None, None, fake, 10, 27, 16, 16, 2, -1, None))[0] == -1
+    code, msg = _status(ex(fake, fake, fake, None, ctypes.c_void_p(0x100001), fake, 10, 27, 16, 16, 2, 1,
+                           None))
+    assert code == -1 and "residual" in msg
+    assert _status(ex(fake, fake, fake, None, None, fake, -5, 27, 16, 16, 2, 0, None))[0] == -1
+    assert _status(ex(None, None, None, None, None, None, 0, 27, 16, 16, 2, 2, None))[0] == 0
+    # submconv3d_dgrad: forward sizes, same checks
+    dg = lib.spconv_submconv3d_dgrad
+    assert _status(dg(fake, fake, fake, fake, -1, 27, 16, 16, 2, None))[0] == -1
+    assert _status(dg(fake, fake, fake, fake, 10, 27, 24, 16, 2, None))[0] == -2
+    assert _status(dg(None, fake, fake, fake, 10, 27, 16, 16, 2, None))[0] == -1
+    assert _status(dg(None, None, None, None, 0, 27, 16, 16, 2, None))[0] == 0
+    # submconv3d_wgrad
+    wg = lib.spconv_submconv3d_wgrad
+    assert _status(wg(fake, fake, fake, None, None, 10, 27, 16, 16, 2, None))[0] == -1
+    assert _status(wg(fake, fake, fake, fake, None, 10, 27, 16, 16, 9, None))[0] == -1
+    assert _status(wg(fake, fake, fake, ctypes.c_void_p(0x100002), None, 10, 27, 16, 16, 2, None))[0] == -1
+    assert _status(wg(None, fake, fake, fake, None, 10, 27, 16, 16, 2, None))[0] == -1
     # count
     assert _status(lib.spconv_count_valid_pairs(fake, 10, 27, None, None))[0] == -1
 

@@ -349,3 +349,165 @@ def test_nmap_rows_equals_full_map_columns(oracle_mod):
     full = brute_force_nmap(coords, offs)
     rows = np.array([0, len(coords) - 1, 5, 5, len(coords) // 2], dtype=np.int64)
     np.testing.assert_array_equal(oracle_mod.nmap_rows(coords, offs, rows), full[:, rows])
+
+
+# ---------------------------------------------------------------- fused epilogue
+# conv_fused = act(conv + bias + residual).  Pinned by values of the two
+# activations fixed by their definitions, by a library logistic function
+# (scipy.special.expit, an independent formula for SiLU = x * logistic(x)),
+# and by the library dense cross-correlation with the residual and torch's
+# own activations applied.
+
+def test_activation_closed_form_values(oracle_mod):
+    # centre offset only, w = identity, no bias: conv = feats exactly
+    feats = np.array([[0.0, 1.0, -1.0, 2.5], [-30.0, 40.0, 0.5, -0.25]], dtype=np.float32)
+    nmap = np.array([[0, 1]], dtype=np.int32)
+    w = np.eye(4, dtype=np.float32)[None]
+    out, _ = oracle_mod.conv_fused(feats, nmap, w, None, "f32", act="silu")
+    assert out[0, 0] == 0.0
+    assert abs(out[0, 1] - 0.7310585786300049) < 1e-15   # 1 / (1 + e^-1)
+    assert abs(out[0, 2] + 0.2689414213699951) < 1e-15   # -1 / (1 + e)
+    assert abs(out[1, 0]) < 1e-11 and abs(out[1, 1] - 40.0) < 1e-15
+    out, _ = oracle_mod.conv_fused(feats, nmap, w, None, "f32", act="relu")
+    np.testing.assert_array_equal(out, np.maximum(feats, 0).astype(np.float64))
+
+
+def test_fused_epilogue_matches_library_logistic(oracle_mod):
+    special = pytest.importorskip("scipy.special")
+    coords = W.random_occupancy(10, 0.3, 21)
+    N = len(coords)
+    nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    feats = W.values(51, 1, (N, 16), "f32")
+    w = W.values(51, 2, (27, 16, 8), "f32", 0.1)
+    bias = W.values(51, 3, (8,), "f32")
+    res = W.values(51, 4, (N, 8), "f32")
+    pre, _ = oracle_mod.conv(feats, nmap, w, bias, "f32")
+    pre = pre + res.astype(np.float64)
+    out, scale = oracle_mod.conv_fused(feats, nmap, w, bias, "f32", residual=res, act="silu")
+    np.testing.assert_allclose(out, pre * special.expit(pre), rtol=1e-13, atol=1e-13)
+    out, _ = oracle_mod.conv_fused(feats, nmap, w, bias, "f32", residual=res, act="relu")
+    np.testing.assert_array_equal(out, np.where(pre > 0, pre, 0.0))
+    assert np.all(scale >= 1.1 * np.abs(res) - 1e-12)
+
+
+@pytest.mark.parametrize("act", ["relu", "silu"])
+def test_fused_epilogue_equals_dense_xcorr(oracle_mod, act):
+    torch = pytest.importorskip("torch")
+    side = 9
+    coords = W.random_occupancy(side, 0.35, 31)
+    N = len(coords)
+    nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    feats = W.values(52, 1, (N, 8), "f32")
+    w = W.values(52, 2, (27, 8, 16), "f32", 0.2)
+    bias = W.values(52, 3, (16,), "f32")
+    res = W.values(52, 4, (N, 16), "f32")
+    dense = dense_xcorr_at_sites(coords, side, f64(feats, "f32"), f64(w, "f32"), f64(bias, "f32"))
+    pre = torch.from_numpy(dense + res.astype(np.float64))
+    ref = (torch.nn.functional.silu(pre) if act == "silu" else torch.nn.functional.relu(pre)).numpy()
+    out, _ = oracle_mod.conv_fused(feats, nmap, w, bias, "f32", residual=res, act=act)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    # activation before the residual add is a different (wrong) order
+    wrong = (torch.nn.functional.silu(torch.from_numpy(dense)) if act == "silu"
+             else torch.nn.functional.relu(torch.from_numpy(dense))).numpy() + res
+    assert not np.allclose(out, wrong, rtol=1e-6, atol=1e-6)
+
+
+def test_fused_epilogue_without_extras_is_conv(oracle_mod):
+    coords = W.random_occupancy(8, 0.4, 41)
+    N = len(coords)
+    nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    feats = W.values(53, 1, (N, 16), "f32")
+    w = W.values(53, 2, (27, 16, 16), "f32")
+    a, sa = oracle_mod.conv(feats, nmap, w, None, "f32")
+    b, sb = oracle_mod.conv_fused(feats, nmap, w, None, "f32")
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(sa, sb)
+
+
+# ---------------------------------------------------------------- backward
+# dgrad / wgrad are the chain rule applied to the forward formula.  Pinned by
+# torch autograd through the library dense cross-correlation (gradients read
+# at the active sites, with the output gradient zero off them), and by the
+# exact adjoint identities against the (already pinned) forward sum:
+#   <y, conv(x; w)> = <dgrad(y; w), x> = <wgrad(x, y), w>   (no bias).
+
+def _backward_case(oracle_mod, side, frac, seed, ci, co, dtype="f32"):
+    coords = W.random_occupancy(side, frac, seed)
+    n = len(coords)
+    nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    x = W.values(seed, 1, (n, ci), dtype)
+    w = W.values(seed, 2, (27, ci, co), dtype, 0.3)
+    y = W.values(seed, 3, (n, co), dtype)
+    return coords, nmap, x, w, y
+
+
+def test_backward_equals_dense_autograd(oracle_mod):
+    torch = pytest.importorskip("torch")
+    side = 8
+    coords, nmap, x, w, y = _backward_case(oracle_mod, side, 0.4, 101, 6, 5)
+    ci, co = x.shape[1], y.shape[1]
+    grid = torch.zeros((1, ci, side, side, side), dtype=torch.float64)
+    grid[0, :, coords[:, 0], coords[:, 1], coords[:, 2]] = torch.from_numpy(f64(x, "f32").T)
+    grid.requires_grad_(True)
+    weight = torch.zeros((co, ci, 3, 3, 3), dtype=torch.float64)
+    for k, (dz, dy, dx) in enumerate(W.offsets_3x3x3()):
+        weight[:, :, dz + 1, dy + 1, dx + 1] = torch.from_numpy(f64(w, "f32")[k].T)
+    weight.requires_grad_(True)
+    out = torch.nn.functional.conv3d(grid, weight, padding=1)
+    ymask = torch.zeros_like(out)
+    ymask[0, :, coords[:, 0], coords[:, 1], coords[:, 2]] = torch.from_numpy(f64(y, "f32").T)
+    gx, gw = torch.autograd.grad((out * ymask).sum(), (grid, weight))
+    ref_dx = gx[0, :, coords[:, 0], coords[:, 1], coords[:, 2]].T.numpy()
+    ref_dw = np.stack([gw[:, :, dz + 1, dy + 1, dx + 1].T.numpy()
+                       for dz, dy, dx in W.offsets_3x3x3()])
+    dx_, _ = oracle_mod.dgrad(y, nmap, w, "f32")
+    dw_, _ = oracle_mod.wgrad(x, y, nmap, "f32")
+    np.testing.assert_allclose(dx_, ref_dx, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dw_, ref_dw, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_backward_adjoint_identities(oracle_mod, dtype):
+    coords, nmap, x, w, y = _backward_case(oracle_mod, 11, 0.3, 102, 16, 24, dtype)
+    fwd, _ = oracle_mod.conv(x, nmap, w, None, dtype)
+    dx_, _ = oracle_mod.dgrad(y, nmap, w, dtype)
+    dw_, _ = oracle_mod.wgrad(x, y, nmap, dtype)
+    lhs = float(np.sum(f64(y, dtype) * fwd))
+    assert abs(lhs - float(np.sum(dx_ * f64(x, dtype)))) <= 1e-9 * max(1.0, abs(lhs))
+    assert abs(lhs - float(np.sum(dw_ * f64(w, dtype)))) <= 1e-9 * max(1.0, abs(lhs))
+
+
+def test_dgrad_is_flipped_transposed_conv_on_symmetric_offsets(oracle_mod):
+    """With offsets[K-1-k] = -offsets[k] the input gradient is a forward
+    convolution of dout with weights w[K-1-k]^T (the form the GPU uses)."""
+    _, nmap, _, w, y = _backward_case(oracle_mod, 10, 0.35, 103, 8, 12)
+    offs = W.offsets_3x3x3()
+    assert np.array_equal(offs[::-1], -offs)
+    dx_, _ = oracle_mod.dgrad(y, nmap, w, "f32")
+    wt = np.ascontiguousarray(np.transpose(w[::-1], (0, 2, 1)))
+    via_fwd, _ = oracle_mod.conv(y, nmap, wt, None, "f32")
+    np.testing.assert_allclose(dx_, via_fwd, rtol=1e-12, atol=1e-12)
+
+
+def test_backward_row_and_entry_selection(oracle_mod):
+    _, nmap, x, w, y = _backward_case(oracle_mod, 9, 0.4, 104, 16, 16)
+    n = x.shape[0]
+    rows = np.array([0, 3, n // 2, n - 1], dtype=np.int64)
+    full, fabs_ = oracle_mod.dgrad(y, nmap, w, "f32")
+    part, pabs = oracle_mod.dgrad(y, nmap, w, "f32", rows=rows, threads=2)
+    np.testing.assert_array_equal(part, full[rows])
+    np.testing.assert_array_equal(pabs, fabs_[rows])
+    dw_full, _ = oracle_mod.wgrad(x, y, nmap, "f32")
+    entries = np.array([0, 17, 27 * 16 * 16 - 1, 5 * 256 + 3 * 16 + 9], dtype=np.int64)
+    dw_part, _ = oracle_mod.wgrad(x, y, nmap, "f32", entries=entries)
+    np.testing.assert_allclose(dw_part, dw_full.reshape(-1)[entries], rtol=1e-13, atol=1e-13)
+
+
+def test_backward_planted_mistake_fails_adjoint(oracle_mod):
+    """Feeding dgrad the unflipped map direction (nmap rows reversed) breaks
+    the adjoint identity, so that pin would catch an offset-order slip."""
+    _, nmap, x, w, y = _backward_case(oracle_mod, 10, 0.35, 105, 8, 8)
+    fwd, _ = oracle_mod.conv(x, nmap, w, None, "f32")
+    bad, _ = oracle_mod.dgrad(y, np.ascontiguousarray(nmap[::-1]), w, "f32")
+    lhs = float(np.sum(f64(y, "f32") * fwd))
+    assert abs(lhs - float(np.sum(bad * f64(x, "f32")))) > 1e-6 * max(1.0, abs(lhs))
