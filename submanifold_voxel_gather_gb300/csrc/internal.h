@@ -53,6 +53,14 @@ spconv_status launch_wgrad_simt(spconv_dtype dtype, const void* feats, const voi
                                 const int32_t* nmap, float* dw, float* dbias, int64_t n, int32_t k,
                                 int32_t ci, int32_t co, cudaStream_t stream);
 
+spconv_status launch_dbias(spconv_dtype dtype, const void* dout, float* dbias, int64_t n, int32_t co,
+                           cudaStream_t stream);
+
+// ---- weight gradient on the tensor cores, bf16 (wgrad_tc.cu); needs Ci and
+// Co multiples of 16 and 16-byte aligned feats and dout
+spconv_status launch_wgrad_tc(const void* feats, const void* dout, const int32_t* nmap, float* dw,
+                              int64_t n, int32_t k, int32_t ci, int32_t co, cudaStream_t stream);
+
 // ---- device error word (ptx.cuh declares the symbol)
 spconv_status read_and_clear_device_error(cudaStream_t stream, unsigned int* bits);
 

@@ -267,7 +267,16 @@ spconv_status spconv_submconv3d_wgrad(const void* feats_dev, const void* dout_de
       return st;
     return spconv::ok();
   }
-  st = spconv::launch_wgrad_simt(dtype, feats_dev, dout_dev, nmap_dev, dw_dev, dbias_dev, N, K, Ci, Co, s);
+  // bf16 with tensor-core-friendly shapes runs on the tensor cores; every
+  // other case on the exact CUDA-core kernel.
+  const bool tc = dtype == SPCONV_BF16 && Ci % 16 == 0 && Co % 16 == 0 && spconv::aligned(feats_dev, 16) &&
+                  spconv::aligned(dout_dev, 16);
+  if (tc) {
+    st = spconv::launch_wgrad_tc(feats_dev, dout_dev, nmap_dev, dw_dev, N, K, Ci, Co, s);
+    if (st == SPCONV_OK && dbias_dev != nullptr) st = spconv::launch_dbias(dtype, dout_dev, dbias_dev, N, Co, s);
+  } else {
+    st = spconv::launch_wgrad_simt(dtype, feats_dev, dout_dev, nmap_dev, dw_dev, dbias_dev, N, K, Ci, Co, s);
+  }
   return st == SPCONV_OK ? spconv::ok() : st;
 }
 

@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 template <typename T>
-spconv_status launch_typed(const T* feats, const T* dout, const int32_t* nmap, float* dw, float* dbias,
+spconv_status launch_typed(const T* feats, const T* dout, const int32_t* nmap, float* dw, float*,
                            int64_t n, int32_t k, int32_t ci, int32_t co, cudaStream_t stream) {
   spconv_status st = SPCONV_OK;
   const size_t dw_bytes = static_cast<size_t>(k) * ci * co * sizeof(float);
@@ -127,27 +127,39 @@ spconv_status launch_typed(const T* feats, const T* dout, const int32_t* nmap, f
   wgrad_simt_kernel<T><<<dim3(gx, gy, static_cast<unsigned>(gz)), kThreads, 0, stream>>>(
       feats, dout, nmap, dw, n, ci, co, static_cast<int32_t>(slices));
   if (!cuda_ok(cudaGetLastError(), "wgrad_simt_kernel launch", &st)) return st;
-  if (dbias != nullptr) {
-    if (!cuda_ok(cudaMemsetAsync(dbias, 0, static_cast<size_t>(co) * sizeof(float), stream),
-                 "cudaMemsetAsync(dbias)", &st))
-      return st;
-    dbias_kernel<T><<<dim3((co + kThreads - 1) / kThreads, static_cast<unsigned>(slices)), kThreads, 0,
-                      stream>>>(dout, dbias, n, co);
-    if (!cuda_ok(cudaGetLastError(), "dbias_kernel launch", &st)) return st;
-  }
   return SPCONV_OK;
 }
 
 }  // namespace
 
+spconv_status launch_dbias(spconv_dtype dtype, const void* dout, float* dbias, int64_t n, int32_t co,
+                           cudaStream_t stream) {
+  spconv_status st = SPCONV_OK;
+  if (!cuda_ok(cudaMemsetAsync(dbias, 0, static_cast<size_t>(co) * sizeof(float), stream),
+               "cudaMemsetAsync(dbias)", &st))
+    return st;
+  const int64_t slices = (n + kSlice - 1) / kSlice;
+  if (slices > 65535) return fail(SPCONV_ERR_UNSUPPORTED, "problem too large for the dbias grid");
+  const dim3 grid((co + kThreads - 1) / kThreads, static_cast<unsigned>(slices));
+  if (dtype == SPCONV_BF16)
+    dbias_kernel<<<grid, kThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(dout), dbias, n, co);
+  else
+    dbias_kernel<<<grid, kThreads, 0, stream>>>(static_cast<const float*>(dout), dbias, n, co);
+  if (!cuda_ok(cudaGetLastError(), "dbias_kernel launch", &st)) return st;
+  return SPCONV_OK;
+}
+
 spconv_status launch_wgrad_simt(spconv_dtype dtype, const void* feats, const void* dout,
                                 const int32_t* nmap, float* dw, float* dbias, int64_t n, int32_t k,
                                 int32_t ci, int32_t co, cudaStream_t stream) {
-  if (dtype == SPCONV_BF16)
-    return launch_typed(static_cast<const __nv_bfloat16*>(feats), static_cast<const __nv_bfloat16*>(dout),
-                        nmap, dw, dbias, n, k, ci, co, stream);
-  return launch_typed(static_cast<const float*>(feats), static_cast<const float*>(dout), nmap, dw, dbias,
-                      n, k, ci, co, stream);
+  spconv_status st =
+      dtype == SPCONV_BF16
+          ? launch_typed(static_cast<const __nv_bfloat16*>(feats), static_cast<const __nv_bfloat16*>(dout),
+                         nmap, dw, dbias, n, k, ci, co, stream)
+          : launch_typed(static_cast<const float*>(feats), static_cast<const float*>(dout), nmap, dw, dbias,
+                         n, k, ci, co, stream);
+  if (st != SPCONV_OK || dbias == nullptr) return st;
+  return launch_dbias(dtype, dout, dbias, n, co, stream);
 }
 
 }  // namespace spconv
