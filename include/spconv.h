@@ -108,6 +108,21 @@ spconv_status spconv_build_nmap(const int32_t* coords_dev, int64_t N, const int3
                                 int32_t K, int32_t* nmap_dev, void* workspace_dev,
                                 size_t workspace_bytes, void* stream);
 
+/*
+ * The map build without the host wait: identical to spconv_build_nmap
+ * except that the verdict of the device-side checks (coordinate range,
+ * duplicates, table overflow) is written as an spconv_status (0 = OK) to
+ * status_dev, an int32 in device memory, on `stream`.  The call returns
+ * after enqueueing; argument errors found on the host are still returned
+ * directly.  For pipelines that keep several steps in flight (copies of
+ * the next step overlapping this step's kernels); check status_dev before
+ * trusting nmap.  With N == 0 it writes 0.  No counterpart on the page.
+ */
+spconv_status spconv_build_nmap_async(const int32_t* coords_dev, int64_t N,
+                                      const int32_t* offsets_host, int32_t K, int32_t* nmap_dev,
+                                      void* workspace_dev, size_t workspace_bytes,
+                                      int32_t* status_dev, void* stream);
+
 /* Largest N spconv_build_nmap_noalloc accepts (its fixed table holds
  * 2 * SPCONV_NOALLOC_MAX_VOXELS slots). */
 #define SPCONV_NOALLOC_MAX_VOXELS (1 << 20)

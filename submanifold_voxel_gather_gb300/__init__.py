@@ -23,7 +23,8 @@ import numpy as np
 
 __all__ = [
     "SpconvError", "load_library", "library_path", "version", "workspace_size", "build_nmap",
-    "submconv3d", "count_valid_pairs", "device_status", "default_offsets",
+    "submconv3d", "submconv3d_dgrad", "submconv3d_wgrad", "count_valid_pairs", "device_status",
+    "default_offsets", "ACTIVATIONS",
     "F32", "TF32", "BF16",
 ]
 
@@ -76,6 +77,8 @@ def load_library() -> ctypes.CDLL:
         lib.spconv_build_nmap_workspace_size.restype = ctypes.c_size_t
         lib.spconv_build_nmap.argtypes = [vp, i64, vp, i32, vp, vp, ctypes.c_size_t, vp]
         lib.spconv_build_nmap.restype = ctypes.c_int
+        lib.spconv_build_nmap_async.argtypes = [vp, i64, vp, i32, vp, vp, ctypes.c_size_t, vp, vp]
+        lib.spconv_build_nmap_async.restype = ctypes.c_int
         lib.spconv_submconv3d.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, ctypes.c_int, vp]
         lib.spconv_submconv3d.restype = ctypes.c_int
         lib.spconv_submconv3d_ex.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, ctypes.c_int,
@@ -141,14 +144,17 @@ def _require_cuda(t, name, dtype=None):
         raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
 
 
-def build_nmap(coords, offsets=None, workspace=None, stream=None, out=None):
+def build_nmap(coords, offsets=None, workspace=None, stream=None, out=None, status=None):
     """Neighbour map (K, N) int32 of ``coords`` ((N, 3) int32 CUDA tensor,
     (z, y, x), distinct, components in [0, 2^20)).  ``offsets`` is a host
     (K, 3) integer array (default: ``default_offsets()``).  ``workspace`` is an
     optional uint8 CUDA tensor of at least ``workspace_size(N)`` bytes; if
     omitted one is taken from torch's allocator.  ``out`` is an optional
     (K, N) int32 CUDA tensor to write.  Waits for the stream once (to read
-    the duplicate/range flags)."""
+    the duplicate/range flags), unless ``status`` (a one-element int32 CUDA
+    tensor) is given: then the verdict (0 = OK, else a negative status code)
+    is written there on the stream and the call does not wait
+    (spconv_build_nmap_async)."""
     torch = _torch()
     _require_cuda(coords, "coords", torch.int32)
     if coords.dim() != 2 or coords.shape[1] != 3:
@@ -168,9 +174,17 @@ def build_nmap(coords, offsets=None, workspace=None, stream=None, out=None):
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=coords.device)
     _require_cuda(workspace, "workspace", torch.uint8)
     lib = load_library()
-    _check(lib.spconv_build_nmap(_ptr(coords), n, offs.ctypes.data_as(ctypes.c_void_p), k,
-                                 _ptr(nmap), _ptr(workspace), workspace.numel(),
-                                 _stream_handle(stream)))
+    if status is None:
+        _check(lib.spconv_build_nmap(_ptr(coords), n, offs.ctypes.data_as(ctypes.c_void_p), k,
+                                     _ptr(nmap), _ptr(workspace), workspace.numel(),
+                                     _stream_handle(stream)))
+    else:
+        _require_cuda(status, "status", torch.int32)
+        if status.numel() != 1:
+            raise ValueError("status must have one element")
+        _check(lib.spconv_build_nmap_async(_ptr(coords), n, offs.ctypes.data_as(ctypes.c_void_p), k,
+                                           _ptr(nmap), _ptr(workspace), workspace.numel(), _ptr(status),
+                                           _stream_handle(stream)))
     return nmap
 
 

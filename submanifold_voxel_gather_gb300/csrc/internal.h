@@ -26,8 +26,12 @@ struct BuildOffsets {
 };
 
 size_t hash_capacity(int64_t n);
+// With status_dev == nullptr the call waits for `stream` and returns the
+// build's verdict; otherwise it writes the verdict (an spconv_status) to
+// status_dev on the stream and returns without waiting.
 spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOffsets& offs,
-                                int32_t k, int32_t* nmap, void* workspace, cudaStream_t stream);
+                                int32_t k, int32_t* nmap, void* workspace, cudaStream_t stream,
+                                int32_t* status_dev = nullptr);
 // Device address of the allocation-free variant's static scratch on the
 // current device (looked up once per device).
 spconv_status noalloc_scratch(void** scratch);

@@ -181,8 +181,22 @@ size_t hash_capacity(int64_t n) {
   return cap;
 }
 
+namespace {
+// The build's error flags as a status code (the precedence of the host-side
+// check: coordinate range, then duplicates, then table overflow).
+__global__ void flags_to_status_kernel(const int* flags, int32_t* status) {
+  if (threadIdx.x != 0) return;
+  const int f = *flags;
+  *status = (f & kFlagRange) ? SPCONV_ERR_INVALID_ARG
+            : (f & kFlagDuplicate) ? SPCONV_ERR_DUPLICATE_COORD
+            : (f & kFlagFull) ? SPCONV_ERR_DEVICE
+                              : SPCONV_OK;
+}
+}  // namespace
+
 spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOffsets& offs,
-                                int32_t k, int32_t* nmap, void* workspace, cudaStream_t stream) {
+                                int32_t k, int32_t* nmap, void* workspace, cudaStream_t stream,
+                                int32_t* status_dev) {
   const size_t cap = hash_capacity(n);
   int* flags = static_cast<int*>(workspace);
   Slot* table = reinterpret_cast<Slot*>(static_cast<char*>(workspace) + kFlagBytes);
@@ -231,6 +245,12 @@ spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOff
   nmap_query_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, plan, k, nmap);
   if (!cuda_ok(cudaGetLastError(), "nmap_query_kernel launch", &st)) return st;
 
+  if (status_dev != nullptr) {
+    // Asynchronous form: the verdict goes to device memory, no host wait.
+    flags_to_status_kernel<<<1, 32, 0, stream>>>(flags, status_dev);
+    if (!cuda_ok(cudaGetLastError(), "flags_to_status_kernel launch", &st)) return st;
+    return SPCONV_OK;
+  }
   int host_flags = 0;
   if (!cuda_ok(cudaMemcpyAsync(&host_flags, flags, sizeof(int), cudaMemcpyDeviceToHost, stream),
                "flag readback", &st))

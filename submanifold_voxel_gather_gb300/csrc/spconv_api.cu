@@ -89,19 +89,33 @@ size_t spconv_build_nmap_workspace_size(int64_t N) {
   return 256 + spconv::hash_capacity(N) * 16;
 }
 
-spconv_status spconv_build_nmap(const int32_t* coords_dev, int64_t N, const int32_t* offsets_host,
-                                int32_t K, int32_t* nmap_dev, void* workspace_dev,
-                                size_t workspace_bytes, void* stream) {
+namespace spconv {
+namespace {
+
+spconv_status build_nmap_impl(const int32_t* coords_dev, int64_t N, const int32_t* offsets_host,
+                              int32_t K, int32_t* nmap_dev, void* workspace_dev, size_t workspace_bytes,
+                              int32_t* status_dev, void* stream) {
   if (N < 0 || N >= INT32_MAX) return fail(SPCONV_ERR_INVALID_ARG, "N must satisfy 0 <= N < 2^31-1");
   if (K < 1 || K > SPCONV_MAX_BUILD_OFFSETS)
     return fail(SPCONV_ERR_INVALID_ARG, "K must satisfy 1 <= K <= SPCONV_MAX_BUILD_OFFSETS");
   if (offsets_host == nullptr) return fail(SPCONV_ERR_INVALID_ARG, "offsets_host is NULL");
-  if (N == 0) return spconv::ok();
+  if (status_dev != nullptr && !aligned(status_dev, 4))
+    return fail(SPCONV_ERR_INVALID_ARG, "status must be 4-byte aligned");
+  spconv_status st = SPCONV_OK;
+  if (N == 0) {
+    if (status_dev == nullptr) return ok();
+    st = check_device();
+    if (st != SPCONV_OK) return st;
+    if (!cuda_ok(cudaMemsetAsync(status_dev, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)),
+                 "cudaMemsetAsync(status)", &st))
+      return st;
+    return ok();
+  }
   if (coords_dev == nullptr || nmap_dev == nullptr || workspace_dev == nullptr)
     return fail(SPCONV_ERR_INVALID_ARG, "coords, nmap and workspace must be non-NULL");
-  if (!spconv::aligned(coords_dev, 4) || !spconv::aligned(nmap_dev, 4))
+  if (!aligned(coords_dev, 4) || !aligned(nmap_dev, 4))
     return fail(SPCONV_ERR_INVALID_ARG, "coords and nmap must be 4-byte aligned");
-  if (!spconv::aligned(workspace_dev, 256))
+  if (!aligned(workspace_dev, 256))
     return fail(SPCONV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (workspace_bytes < spconv_build_nmap_workspace_size(N))
     return fail(SPCONV_ERR_WORKSPACE, "workspace smaller than spconv_build_nmap_workspace_size(N)");
@@ -110,14 +124,33 @@ spconv_status spconv_build_nmap(const int32_t* coords_dev, int64_t N, const int3
     if (d <= -SPCONV_COORD_LIMIT || d >= SPCONV_COORD_LIMIT)
       return fail(SPCONV_ERR_INVALID_ARG, "offset component out of range");
   }
-  spconv_status st = spconv::check_device();
+  st = check_device();
   if (st != SPCONV_OK) return st;
-  spconv::BuildOffsets offs;
+  BuildOffsets offs;
   std::memset(&offs, 0, sizeof offs);
   std::memcpy(offs.d, offsets_host, sizeof(int32_t) * 3 * static_cast<size_t>(K));
-  st = spconv::launch_build_nmap(coords_dev, N, offs, K, nmap_dev, workspace_dev,
-                                 static_cast<cudaStream_t>(stream));
-  return st == SPCONV_OK ? spconv::ok() : st;
+  st = launch_build_nmap(coords_dev, N, offs, K, nmap_dev, workspace_dev, static_cast<cudaStream_t>(stream),
+                         status_dev);
+  return st == SPCONV_OK ? ok() : st;
+}
+
+}  // namespace
+}  // namespace spconv
+
+spconv_status spconv_build_nmap(const int32_t* coords_dev, int64_t N, const int32_t* offsets_host,
+                                int32_t K, int32_t* nmap_dev, void* workspace_dev,
+                                size_t workspace_bytes, void* stream) {
+  return spconv::build_nmap_impl(coords_dev, N, offsets_host, K, nmap_dev, workspace_dev, workspace_bytes,
+                                 nullptr, stream);
+}
+
+spconv_status spconv_build_nmap_async(const int32_t* coords_dev, int64_t N,
+                                      const int32_t* offsets_host, int32_t K, int32_t* nmap_dev,
+                                      void* workspace_dev, size_t workspace_bytes,
+                                      int32_t* status_dev, void* stream) {
+  if (status_dev == nullptr) return fail(SPCONV_ERR_INVALID_ARG, "status must be non-NULL");
+  return spconv::build_nmap_impl(coords_dev, N, offsets_host, K, nmap_dev, workspace_dev, workspace_bytes,
+                                 status_dev, stream);
 }
 
 spconv_status spconv_build_nmap_noalloc(const int32_t* coords_dev, int64_t N,

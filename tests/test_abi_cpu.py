@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
     for required in ("spconv_build_nmap", "spconv_submconv3d", "spconv_build_nmap_workspace_size",
                      "spconv_last_error", "spconv_version", "spconv_count_valid_pairs",
                      "spconv_device_status", "spconv_submconv3d_ex", "spconv_submconv3d_dgrad",
-                     "spconv_submconv3d_wgrad"):
+                     "spconv_submconv3d_wgrad", "spconv_build_nmap_async"):
         assert required in names
 
 
@@ -101,6 +101,12 @@ def test_argument_validation_without_gpu(lib):
     assert _status(wg(fake, fake, fake, fake, None, 10, 27, 16, 16, 9, None))[0] == -1
     assert _status(wg(fake, fake, fake, ctypes.c_void_p(0x100002), None, 10, 27, 16, 16, 2, None))[0] == -1
     assert _status(wg(None, fake, fake, fake, None, 10, 27, 16, 16, 2, None))[0] == -1
+    # build_nmap_async: host-side checks as build_nmap, plus the status pointer
+    ba = lib.spconv_build_nmap_async
+    assert _status(ba(fake, 10, optr, 27, fake, fake, 1 << 30, None, None))[0] == -1
+    assert _status(ba(fake, 10, optr, 27, fake, fake, 1 << 30, ctypes.c_void_p(0x100002), None))[0] == -1
+    assert _status(ba(fake, 10, optr, 27, fake, fake, 100, fake, None))[0] == -3
+    assert _status(ba(fake, -1, optr, 27, fake, fake, 1 << 30, fake, None))[0] == -1
     # count
     assert _status(lib.spconv_count_valid_pairs(fake, 10, 27, None, None))[0] == -1
 

@@ -104,3 +104,32 @@ def test_nmap_large_configs(sv, oracle_mod, name):
     vp = int(((nm >= 0) & (nm < n)).sum().item())
     assert sv.count_valid_pairs(nm) == vp
     assert vp >= n
+
+
+def test_async_build_matches_and_reports_on_device(sv, oracle_mod):
+    """spconv_build_nmap_async: the same map, the verdict written to device
+    memory (no host wait); two builds in flight on two streams; a duplicate
+    coordinate gives SPCONV_ERR_DUPLICATE_COORD in the status word."""
+    import torch
+    a = W.coords_only("small")
+    b = W.random_occupancy(20, 0.3, 9)
+    b = b[W.permutation(len(b), 9)]
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    st = torch.full((2,), 123, dtype=torch.int32, device="cuda")
+    ca = torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    cb = torch.from_numpy(np.ascontiguousarray(b)).cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s1):
+        ma = sv.build_nmap(ca, status=st[0:1], stream=s1)
+    with torch.cuda.stream(s2):
+        mb = sv.build_nmap(cb, offsets=W.offsets_cube(2), status=st[1:2], stream=s2)
+    torch.cuda.synchronize()
+    assert st.tolist() == [0, 0]
+    np.testing.assert_array_equal(ma.cpu().numpy(), oracle_mod.build_nmap(a, W.offsets_3x3x3()))
+    np.testing.assert_array_equal(mb.cpu().numpy(), oracle_mod.build_nmap(b, W.offsets_cube(2)))
+    dup = torch.tensor([[1, 2, 3], [4, 5, 6], [1, 2, 3]], dtype=torch.int32, device="cuda")
+    sv.build_nmap(dup, status=st[0:1])
+    empty = torch.zeros((0, 3), dtype=torch.int32, device="cuda")
+    sv.build_nmap(empty, status=st[1:2])
+    torch.cuda.synchronize()
+    assert st.tolist() == [-4, 0]
