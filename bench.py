@@ -58,7 +58,70 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="approximate CPU work of the oracle baseline sample")
+    ap.add_argument("--materialized", action="store_true",
+                    help="also time the materialising gather + GEMM path (torch ops) with peak memory")
     return ap.parse_args()
+
+
+def materialized_baseline(torch, sv, feats, nmap, w, bias, out_fused, reps=3):
+    """The path the page replaces, on this GPU: the (K, N, Ci) gather is
+    materialised (torch index_select over feats with a zero pad row appended,
+    so the sentinel N selects zeros) and contracted with cuBLAS GEMMs (torch
+    matmul, bf16 in, fp32 accumulation across chunks).  Two variants: the
+    whole gather at once (one GEMM with K = 27 Ci) and chunks of two offsets,
+    as the page describes the stock layer.  Not part of the library: torch
+    ops only, for the time and peak-memory comparison.  Returns a dict of
+    ms, peak GB and the largest difference from the fused output relative
+    to its largest magnitude."""
+    k, n = nmap.shape
+    ci, co = w.shape[1], w.shape[2]
+    dev = feats.device
+
+    def run(chunk):
+        padded = torch.cat([feats, torch.zeros((1, ci), dtype=feats.dtype, device=dev)])
+        idx = torch.where((nmap >= 0) & (nmap < n), nmap, torch.full_like(nmap, n)).long()
+        acc = torch.zeros((n, co), dtype=torch.float32, device=dev)
+        for k0 in range(0, k, chunk):
+            k1 = min(k, k0 + chunk)
+            # voxel-major index order: the gather lands as (N, chunk * Ci) directly
+            g = padded.index_select(0, idx[k0:k1].t().reshape(-1)).view(n, (k1 - k0) * ci)
+            acc += (g @ w[k0:k1].reshape((k1 - k0) * ci, co)).float()
+            del g
+        return (acc + bias.float()).to(feats.dtype)
+
+    res = {}
+    for name, chunk in (("chunks_of_2_offsets", 2), ("whole_gather", k)):
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        got = run(chunk)
+        torch.cuda.synchronize(dev)
+        peak = torch.cuda.max_memory_allocated(dev) - base
+        diff = float((got.float() - out_fused.float()).abs().max() / out_fused.float().abs().max())
+        del got
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            r = run(chunk)
+            del r
+        e1.record()
+        torch.cuda.synchronize(dev)
+        res[name] = {"ms": e0.elapsed_time(e1) / reps, "peak_extra_gb": peak / 1e9,
+                     "max_rel_diff_vs_fused": diff}
+    # the fused call's own working set beyond its inputs and output: none
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        sv.submconv3d(feats, nmap, w, bias, out=out_fused)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    res["fused"] = {"ms": e0.elapsed_time(e1) / reps,
+                    "peak_extra_gb": (torch.cuda.max_memory_allocated(dev) - base) / 1e9}
+    return res
 
 
 def dist_env():
@@ -395,6 +458,10 @@ def run_ours(args):
             pg.destroy_process_group()
         return 0
 
+    materialized = None
+    if args.materialized and dtype == "bf16":
+        materialized = materialized_baseline(torch, sv, feats, nmap, w, bias, out)
+
     bf16_peak, hbm_peak, peak_kind = peaks()
     achieved = flops / (conv_avg_ms * 1e-3) / 1e12
     elem = 2 if dtype == "bf16" else 4
@@ -432,6 +499,7 @@ def run_ours(args):
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "generation_s": gen_s,
+        **({"materialized": materialized} if materialized is not None else {}),
     }
     print(json.dumps(line), flush=True)
     if pg is not None:
