@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     submconv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const TcParams p) {
   constexpr int kRowsPerWarp = TILE_N / 4;       // gathered rows per producer warp
   constexpr int kIdxPerLane = kRowsPerWarp / 4;  // 4 rows per warp instruction
+  static_assert(kRowsPerWarp == 64, "ring layout: 64 rows per gather producer warp");
   constexpr int kLoaderPerLane = TILE_N / 32;
   constexpr int kOutStride = MBLK * 128;         // staged output row, elements
   // Two accumulator buffers (the epilogue of one tile overlaps the next) when
@@ -234,7 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // normalised: a valid index, or -1 for every kind of invalid entry
             const int32_t nv = (v[b][j] >= 0 && v[b][j] < n_rows) ? v[b][j] : -1;
             any |= nv >= 0;
-            ring[e * TILE_N + lane + 32 * j] = nv;
+            // Row r is stored where its gather lane reads it: producer warp
+            // r / 64 takes rows 4 j + s (s = r % 4) as 16 consecutive words.
+            const int r = static_cast<int>(lane) + 32 * j;
+            ring[e * TILE_N + (r >> 6) * 64 + (r & 3) * 16 + ((r & 63) >> 2)] = nv;
           }
           const uint32_t ballot = __ballot_sync(0xffffffffu, any);
           if (lane == 0) ring_flag[e] = ballot != 0u ? 1u : 0u;
@@ -274,9 +278,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t vi[kIdxPerLane];   // kHoist: index, 0 where invalid
         uint32_t valid_bits = 0;    // kHoist: bit j set where row j is valid
         if (go) {
+          // this lane's 16 row indices are consecutive: four 16-byte loads
+          const int4* ip =
+              reinterpret_cast<const int4*>(ring + e * TILE_N + static_cast<int>(aw) * kRowsPerWarp + sub_row * 16);
+#pragma unroll
+          for (int q = 0; q < kIdxPerLane / 4; ++q) {
+            const int4 v4 = ip[q];
+            idx[4 * q] = v4.x;
+            idx[4 * q + 1] = v4.y;
+            idx[4 * q + 2] = v4.z;
+            idx[4 * q + 3] = v4.w;
+          }
 #pragma unroll
           for (int j = 0; j < kIdxPerLane; ++j) {
-            idx[j] = ring[e * TILE_N + static_cast<int>(aw) * kRowsPerWarp + 4 * j + sub_row];
             if constexpr (kHoist) {
               vi[j] = idx[j] >= 0 ? static_cast<uint32_t>(idx[j]) : 0u;
               valid_bits |= (idx[j] >= 0 ? 1u : 0u) << j;

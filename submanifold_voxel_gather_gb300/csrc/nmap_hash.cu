@@ -79,7 +79,9 @@ __global__ void hash_clear_kernel(Slot* table, unsigned long long cap, int* flag
                                   int64_t n, int32_t fill_count, const __grid_constant__ QueryPlan plan) {
   const unsigned long long stride = static_cast<unsigned long long>(gridDim.x) * blockDim.x;
   const unsigned long long tid = static_cast<unsigned long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (unsigned long long i = tid; i < cap; i += stride) table[i].key = kEmptyKey;
+  // whole 16-byte slots (EMPTY key, value -1): full-sector stores
+  int4* slots = reinterpret_cast<int4*>(table);
+  for (unsigned long long i = tid; i < cap; i += stride) slots[i] = make_int4(-1, -1, -1, -1);
   if (fill_count > 0) {
     const int32_t missing = static_cast<int32_t>(n);
     for (int32_t r = 0, seen = 0; seen < fill_count; ++r) {
