@@ -503,7 +503,10 @@ def run_ours(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        # per step: the map build's six kernels (flag reset, range/order
+        # check, table clear, insert, row query, voxel-hash query: the path
+        # not taken returns at once) and one conv launch (Co <= 256)
+        "gpu_launches": (6 + (co + 255) // 256) * args.steps,
         "clocks": clocks,
         "generation_s": gen_s,
         **({"materialized": materialized} if materialized is not None else {}),

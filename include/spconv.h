@@ -98,9 +98,14 @@ size_t spconv_build_nmap_workspace_size(int64_t N);
  *                 until this one returns.
  *  stream         cudaStream_t (as void*).
  *
- * The call enqueues three kernels (table clear, insert, query) and then
- * waits for the stream once to read the error flags, so it cannot be
- * captured into a CUDA graph.  Returns SPCONV_ERR_DUPLICATE_COORD if two
+ * The call enqueues its kernels and then waits for the stream once to read
+ * the error flags, so it cannot be captured into a CUDA graph.  A first
+ * kernel checks the coordinate range and whether the coordinates are
+ * strictly increasing in (z, y, x) order; the device then takes one of two
+ * paths (the other path's kernels return at once).  Strictly increasing
+ * input, as a voxeliser emits it, builds a hash of (z, y) rows and finds
+ * neighbours by searching rows; any other order builds a hash of voxels.
+ * Both give the same map.  Returns SPCONV_ERR_DUPLICATE_COORD if two
  * voxels share a coordinate and SPCONV_ERR_INVALID_ARG if a coordinate is
  * out of range; nmap is then undefined.
  */

@@ -3,9 +3,27 @@
 // The page "sparse_conv_metal.py" (trellis-2-mrp-mlx) consumes a (K, N) int32
 // map whose entry [k, n] is the row of the voxel at coords[n] + offsets[k]
 // and N where there is none (wrapper docstring, kernel body); it takes the
-// map as given.  This file builds it:
+// map as given.  This file builds it.  A first pass checks the coordinate
+// range and whether the coordinates are strictly increasing in (z, y, x)
+// order, and counts the (z, y) rows.  The rest of the build takes one of two
+// paths, chosen on the device from that verdict (every kernel of the other
+// path returns at once):
 //
-//   clear   every slot's key := EMPTY, error flags := 0
+// Sorted input (what a voxeliser emits).  Each (z, y) row of cells is a
+// contiguous run of voxels, so a hash of rows (row -> index of its first
+// voxel, table sized from the row count) is enough:
+//
+//   clear   the row table's slots := EMPTY
+//   insert  the first voxel of each row inserts the row with its length
+//   query   one thread per voxel, per (dz, dy) group of offsets: one row
+//           probe (first voxel and length), then a bisection over the row's
+//           x values for x + dx (in ascending dx, each search starting where
+//           the last one ended).  Consecutive voxels probe the same rows, so
+//           the table and coordinate reads mostly hit in cache.
+//
+// Any other order (or duplicates, which are never strictly increasing):
+//
+//   clear   every slot's key := EMPTY
 //   insert  one thread per voxel: linear probing with a 64-bit atomicCAS on
 //           the packed key (21 bits per axis); an equal key already present
 //           flags a duplicate coordinate
@@ -37,15 +55,25 @@ constexpr int kThreads = 256;
 constexpr unsigned long long kEmptyKey = ~0ull;
 constexpr size_t kFlagBytes = 256;
 
-enum : int { kFlagDuplicate = 1, kFlagRange = 2, kFlagFull = 4 };
+enum : int { kFlagDuplicate = 1, kFlagRange = 2, kFlagFull = 4, kFlagUnsorted = 8 };
 
 enum : int8_t { kRoleProbe = 0, kRoleMirror = 1, kRoleSelf = 2 };
 
-// Per-offset work of the query kernel (built on the host from the offsets).
+// Per-offset work of the query kernels (built on the host from the offsets).
 struct QueryPlan {
   int32_t d[3 * SPCONV_MAX_BUILD_OFFSETS];   // offsets (dz, dy, dx)
   int16_t mirror[SPCONV_MAX_BUILD_OFFSETS];  // probed offset: its opposite's row, or -1
   int8_t role[SPCONV_MAX_BUILD_OFFSETS];     // kRoleProbe / kRoleMirror / kRoleSelf
+  // Sorted-input path: the offsets grouped by (dz, dy); the members of group
+  // g are mem_k/mem_dx[grp_first[g] .. grp_first[g] + grp_count[g]), in
+  // ascending dx.
+  int32_t groups;
+  int32_t grp_dz[SPCONV_MAX_BUILD_OFFSETS];
+  int32_t grp_dy[SPCONV_MAX_BUILD_OFFSETS];
+  int16_t grp_first[SPCONV_MAX_BUILD_OFFSETS];
+  int16_t grp_count[SPCONV_MAX_BUILD_OFFSETS];
+  int16_t mem_k[SPCONV_MAX_BUILD_OFFSETS];
+  int32_t mem_dx[SPCONV_MAX_BUILD_OFFSETS];
 };
 
 struct alignas(16) Slot {
@@ -73,14 +101,81 @@ __device__ __forceinline__ bool in_grid(int v) {
   return v >= 0 && v < SPCONV_COORD_LIMIT;
 }
 
+__device__ __forceinline__ unsigned long long row_key(int z, int y) {
+  return (static_cast<unsigned long long>(z) << 21) | static_cast<unsigned long long>(y);
+}
+
+// Slots of the row table for `rows` rows: the next power of two >= 2 rows
+// (at least 64).  Never more than hash_capacity(N), as rows <= N.
+__device__ __forceinline__ unsigned long long row_capacity(unsigned int rows) {
+  const unsigned long long want = 2ull * rows;
+  if (want <= 64ull) return 64ull;
+  return 1ull << (64 - __clzll(want - 1ull));
+}
+
+__device__ __forceinline__ unsigned long long voxel_key(const int32_t* __restrict__ coords, int64_t j) {
+  return pack_coord(__ldg(coords + 3 * j), __ldg(coords + 3 * j + 1), __ldg(coords + 3 * j + 2));
+}
+
+// flags[0] := 0 (error and order bits), flags[1] := 0 (row count).
+__global__ void build_reset_kernel(int* flags) {
+  if (threadIdx.x == 0) {
+    flags[0] = 0;
+    flags[1] = 0;
+  }
+}
+
+// Coordinate range, strict (z, y, x) order and the number of (z, y) rows.
+// Verdicts are gathered per block and published with one atomic each.
+__global__ void __launch_bounds__(kThreads) order_check_kernel(const int32_t* __restrict__ coords, int64_t n,
+                                                               int* flags) {
+  __shared__ int bits;
+  __shared__ unsigned int rows;
+  if (threadIdx.x == 0) {
+    bits = 0;
+    rows = 0;
+  }
+  __syncthreads();
+  int my_bits = 0;
+  unsigned int my_rows = 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int z = __ldg(coords + 3 * i), y = __ldg(coords + 3 * i + 1), x = __ldg(coords + 3 * i + 2);
+    if (!in_grid(z) || !in_grid(y) || !in_grid(x)) my_bits |= kFlagRange;
+    if (i + 1 < n && !(pack_coord(z, y, x) < voxel_key(coords, i + 1))) my_bits |= kFlagUnsorted;
+    if (i == 0 || __ldg(coords + 3 * (i - 1)) != z || __ldg(coords + 3 * (i - 1) + 1) != y) ++my_rows;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    my_bits |= __shfl_xor_sync(0xffffffffu, my_bits, off);
+    my_rows += __shfl_xor_sync(0xffffffffu, my_rows, off);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    if (my_bits) atomicOr(&bits, my_bits);
+    if (my_rows) atomicAdd(&rows, my_rows);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (bits) atomicOr(flags, bits);
+    if (rows) atomicAdd(reinterpret_cast<unsigned int*>(flags + 1), rows);
+  }
+}
+
 // Clears the table and flags, and writes N into the map rows of the offsets
 // whose entries come from their opposite's hits (kRoleMirror).
 __global__ void hash_clear_kernel(Slot* table, unsigned long long cap, int* flags, int32_t* nmap,
                                   int64_t n, int32_t fill_count, const __grid_constant__ QueryPlan plan) {
+  const int f = flags[0];
+  if (f & kFlagRange) return;
   const unsigned long long stride = static_cast<unsigned long long>(gridDim.x) * blockDim.x;
   const unsigned long long tid = static_cast<unsigned long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   // whole 16-byte slots (EMPTY key, value -1): full-sector stores
   int4* slots = reinterpret_cast<int4*>(table);
+  if (!(f & kFlagUnsorted)) {  // sorted input: only the row table
+    const unsigned long long cap_r = row_capacity(static_cast<unsigned int>(flags[1]));
+    for (unsigned long long i = tid; i < cap_r; i += stride) slots[i] = make_int4(-1, -1, -1, -1);
+    return;
+  }
   for (unsigned long long i = tid; i < cap; i += stride) slots[i] = make_int4(-1, -1, -1, -1);
   if (fill_count > 0) {
     const int32_t missing = static_cast<int32_t>(n);
@@ -91,14 +186,55 @@ __global__ void hash_clear_kernel(Slot* table, unsigned long long cap, int* flag
       for (unsigned long long i = tid; i < static_cast<unsigned long long>(n); i += stride) row[i] = missing;
     }
   }
-  if (tid == 0) *flags = 0;
 }
 
 __global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n, Slot* table,
                                    unsigned long long mask, int* flags) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
+  const int f = flags[0];
+  if (f & kFlagRange) return;
   const int z = coords[3 * i], y = coords[3 * i + 1], x = coords[3 * i + 2];
+  if (!(f & kFlagUnsorted)) {
+    // sorted input: the first voxel of each (z, y) row inserts the row
+    if (i > 0 && coords[3 * (i - 1)] == z && coords[3 * (i - 1) + 1] == y) return;
+    const unsigned long long rmask = row_capacity(static_cast<unsigned int>(flags[1])) - 1ull;
+    const unsigned long long rk = row_key(z, y);
+    unsigned long long h = mix_hash(rk) & rmask;
+    for (unsigned long long probe = 0; probe <= rmask; ++probe) {
+      const unsigned long long prev = atomicCAS(&table[h].key, kEmptyKey, rk);
+      if (prev == kEmptyKey) {
+        // The row's first voxel and its length: the first index past i whose
+        // (z, y) differs, by doubling steps then bisection (once per row).
+        int64_t lo = i, hi = n, step = 1;  // row(lo) == (z, y)
+        while (true) {
+          const int64_t probe = lo + step;
+          if (probe >= n) break;
+          if (coords[3 * probe] != z || coords[3 * probe + 1] != y) {
+            hi = probe;
+            break;
+          }
+          lo = probe;
+          step <<= 1;
+        }
+        while (hi - lo > 1) {  // row(lo) == (z, y); hi == n or row(hi) != (z, y)
+          const int64_t mid = lo + (hi - lo) / 2;
+          if (coords[3 * mid] == z && coords[3 * mid + 1] == y) lo = mid;
+          else hi = mid;
+        }
+        table[h].val = static_cast<int32_t>(i);
+        table[h].pad = static_cast<int32_t>(hi - i);
+        return;
+      }
+      if (prev == rk) {  // a row starting twice: the input was not sorted after all
+        atomicOr(flags, kFlagDuplicate);
+        return;
+      }
+      h = (h + 1) & rmask;
+    }
+    atomicOr(flags, kFlagFull);
+    return;
+  }
   if (!in_grid(z) || !in_grid(y) || !in_grid(x)) {
     atomicOr(flags, kFlagRange);
     return;
@@ -120,10 +256,72 @@ __global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n
   atomicOr(flags, kFlagFull);
 }
 
+// Sorted input: nmap[k, n] for every offset, by row probe + search.
+__global__ void __launch_bounds__(kThreads)
+    nmap_query_rows_kernel(const int32_t* __restrict__ coords, int64_t n, const Slot* __restrict__ table,
+                           const int* __restrict__ flags, const __grid_constant__ QueryPlan plan,
+                           int32_t* __restrict__ nmap) {
+  const int f = flags[0];
+  if (f & (kFlagRange | kFlagUnsorted)) return;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const unsigned long long rmask = row_capacity(static_cast<unsigned int>(flags[1])) - 1ull;
+  const int z = __ldg(coords + 3 * i), y = __ldg(coords + 3 * i + 1), x = __ldg(coords + 3 * i + 2);
+  const int32_t missing = static_cast<int32_t>(n);
+  for (int32_t g = 0; g < plan.groups; ++g) {
+    const int zq = z + plan.grp_dz[g], yq = y + plan.grp_dy[g];
+    const int m0 = plan.grp_first[g], m1 = m0 + plan.grp_count[g];
+    int64_t start = -1;  // first voxel of row (zq, yq)
+    int64_t end = -1;    // one past its last voxel
+    if (in_grid(zq) && in_grid(yq)) {
+      const unsigned long long rk = row_key(zq, yq);
+      unsigned long long h = mix_hash(rk) & rmask;
+      for (unsigned long long probe = 0; probe <= rmask; ++probe) {
+        const int4 sl = __ldg(reinterpret_cast<const int4*>(table + h));
+        const unsigned long long sk =
+            (static_cast<unsigned long long>(static_cast<uint32_t>(sl.y)) << 32) | static_cast<uint32_t>(sl.x);
+        if (sk == rk) {
+          start = sl.z;
+          end = start + sl.w;
+          break;
+        }
+        if (sk == kEmptyKey) break;
+        h = (h + 1) & rmask;
+      }
+    }
+    // Within [start, end) the cells are one row, increasing in x: each search
+    // compares x only.  Members come in ascending dx, so each search starts
+    // where the last one ended.
+    int64_t cur = start;
+    for (int m = m0; m < m1; ++m) {
+      int32_t found = missing;
+      const int xq = x + plan.mem_dx[m];
+      if (start >= 0 && cur < end) {
+        int64_t lo = cur, hi = end;  // first j in [lo, end) with x_j >= xq
+        if (__ldg(coords + 3 * lo + 2) >= xq) {
+          hi = lo;
+        } else {
+          while (hi - lo > 1) {  // x_lo < xq; hi == end or x_hi >= xq
+            const int64_t mid = lo + (hi - lo) / 2;
+            if (__ldg(coords + 3 * mid + 2) >= xq) hi = mid;
+            else lo = mid;
+          }
+        }
+        if (hi < end && __ldg(coords + 3 * hi + 2) == xq) found = static_cast<int32_t>(hi);
+        cur = hi;
+      }
+      nmap[static_cast<int64_t>(plan.mem_k[m]) * n + i] = found;
+    }
+  }
+}
+
+// Any other input order: hash probes (one offset of each opposite pair).
 __global__ void __launch_bounds__(kThreads)
     nmap_query_kernel(const int32_t* __restrict__ coords, int64_t n, const Slot* __restrict__ table,
-                      unsigned long long mask, const __grid_constant__ QueryPlan plan,
-                      int32_t k_count, int32_t* __restrict__ nmap) {
+                      unsigned long long mask, const int* __restrict__ flags,
+                      const __grid_constant__ QueryPlan plan, int32_t k_count, int32_t* __restrict__ nmap) {
+  const int f = flags[0];
+  if ((f & kFlagRange) || !(f & kFlagUnsorted)) return;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const int z = coords[3 * i], y = coords[3 * i + 1], x = coords[3 * i + 2];
@@ -236,15 +434,60 @@ spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOff
       }
     }
   }
+  // Sorted-input path: offsets grouped by (dz, dy), members by ascending dx.
+  plan.groups = 0;
+  {
+    int32_t grp_of[SPCONV_MAX_BUILD_OFFSETS];
+    int32_t counts[SPCONV_MAX_BUILD_OFFSETS] = {};
+    for (int32_t a = 0; a < k; ++a) {
+      int32_t g = 0;
+      while (g < plan.groups && !(plan.grp_dz[g] == offs.d[3 * a] && plan.grp_dy[g] == offs.d[3 * a + 1])) ++g;
+      if (g == plan.groups) {
+        plan.grp_dz[g] = offs.d[3 * a];
+        plan.grp_dy[g] = offs.d[3 * a + 1];
+        ++plan.groups;
+      }
+      grp_of[a] = g;
+      ++counts[g];
+    }
+    int32_t first = 0;
+    for (int32_t g = 0; g < plan.groups; ++g) {
+      plan.grp_first[g] = static_cast<int16_t>(first);
+      plan.grp_count[g] = 0;
+      first += counts[g];
+    }
+    for (int32_t a = 0; a < k; ++a) {  // insertion in ascending dx within the group
+      const int32_t g = grp_of[a];
+      int32_t pos = plan.grp_first[g] + plan.grp_count[g];
+      const int32_t dx = offs.d[3 * a + 2];
+      while (pos > plan.grp_first[g] && plan.mem_dx[pos - 1] > dx) {
+        plan.mem_dx[pos] = plan.mem_dx[pos - 1];
+        plan.mem_k[pos] = plan.mem_k[pos - 1];
+        --pos;
+      }
+      plan.mem_dx[pos] = dx;
+      plan.mem_k[pos] = static_cast<int16_t>(a);
+      ++plan.grp_count[g];
+    }
+  }
+
+  const unsigned grid = static_cast<unsigned>((n + kThreads - 1) / kThreads);
+  const unsigned check_grid = grid < 16u * static_cast<unsigned>(sms) ? grid : 16u * static_cast<unsigned>(sms);
+  build_reset_kernel<<<1, 32, 0, stream>>>(flags);
+  if (!cuda_ok(cudaGetLastError(), "build_reset_kernel launch", &st)) return st;
+  order_check_kernel<<<check_grid, kThreads, 0, stream>>>(coords, n, flags);
+  if (!cuda_ok(cudaGetLastError(), "order_check_kernel launch", &st)) return st;
+
   hash_clear_kernel<<<clear_grid, kThreads, 0, stream>>>(table, cap, flags, nmap, n, fill_count,
                                                          plan);
   if (!cuda_ok(cudaGetLastError(), "hash_clear_kernel launch", &st)) return st;
 
-  const unsigned grid = static_cast<unsigned>((n + kThreads - 1) / kThreads);
   hash_insert_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, flags);
   if (!cuda_ok(cudaGetLastError(), "hash_insert_kernel launch", &st)) return st;
 
-  nmap_query_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, plan, k, nmap);
+  nmap_query_rows_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, flags, plan, nmap);
+  if (!cuda_ok(cudaGetLastError(), "nmap_query_rows_kernel launch", &st)) return st;
+  nmap_query_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, flags, plan, k, nmap);
   if (!cuda_ok(cudaGetLastError(), "nmap_query_kernel launch", &st)) return st;
 
   if (status_dev != nullptr) {

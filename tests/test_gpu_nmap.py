@@ -133,3 +133,37 @@ def test_async_build_matches_and_reports_on_device(sv, oracle_mod):
     sv.build_nmap(empty, status=st[1:2])
     torch.cuda.synchronize()
     assert st.tolist() == [-4, 0]
+
+
+def test_nmap_sorted_row_path_cases(sv, oracle_mod):
+    """Strictly (z, y, x)-sorted input takes the row-table path, any other
+    order the voxel-hash path; both must give the oracle's map exactly.
+    Cases aimed at the row path: long dense rows, rows at the grid limits,
+    one single row, offset lists with duplicates and large dx, and inputs
+    that are sorted except for one swapped pair (hash path)."""
+    rng = np.random.default_rng(11)
+    hi = (1 << 20) - 1
+    dense_row = np.stack([np.full(1000, 3), np.full(1000, 4), np.arange(1000)], axis=1)
+    two_runs = np.stack([np.full(40, 3), np.full(40, 5), np.r_[np.arange(20), 500 + np.arange(20)]], axis=1)
+    stack = np.stack([np.repeat([2, 3, 4], 300), np.tile(np.repeat([4, 5, 6], 100), 3),
+                      np.tile(np.arange(100), 9)], axis=1)
+    edges = np.array([[0, 0, 0], [0, 0, 1], [0, 1, 0], [hi, hi, hi - 1], [hi, hi, hi]])
+    single = np.stack([np.zeros(64, int), np.zeros(64, int), np.sort(rng.choice(5000, 64, replace=False))], axis=1)
+    offset_sets = [
+        W.offsets_3x3x3(),
+        W.offsets_cube(2),
+        np.array([[0, 0, 1], [0, 0, 1], [0, 0, -7], [1, 0, 0], [0, 0, 0], [-1, 2, 3], [0, 0, 7]], np.int32),
+    ]
+    for coords in (np.concatenate([dense_row, two_runs]), stack, edges, single):
+        coords = np.unique(coords.astype(np.int32), axis=0)  # sorted, distinct
+        for offs in offset_sets:
+            np.testing.assert_array_equal(gpu_nmap(sv, coords, offs), oracle_mod.build_nmap(coords, offs))
+        if len(coords) > 2:
+            swapped = coords.copy()
+            swapped[[0, 1]] = swapped[[1, 0]]
+            np.testing.assert_array_equal(gpu_nmap(sv, swapped), oracle_mod.build_nmap(swapped, W.offsets_3x3x3()))
+    import torch
+    sorted_dup = torch.tensor([[1, 2, 3], [1, 2, 3], [1, 2, 4]], dtype=torch.int32, device="cuda")
+    with pytest.raises(sv.SpconvError) as e:
+        sv.build_nmap(sorted_dup)
+    assert e.value.code == -4
