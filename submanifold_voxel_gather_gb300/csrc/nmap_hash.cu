@@ -42,6 +42,8 @@
 // sequences are short; every probe loop is still bounded by the capacity.
 #include <cuda_runtime.h>
 
+#include <climits>
+
 #include <mutex>
 #include <string>
 
@@ -111,6 +113,51 @@ __device__ __forceinline__ unsigned long long row_capacity(unsigned int rows) {
   const unsigned long long want = 2ull * rows;
   if (want <= 64ull) return 64ull;
   return 1ull << (64 - __clzll(want - 1ull));
+}
+
+// Home slot of row (z, y): a 32-bit integer hash of the row (multiply,
+// xor-shift rounds; the table never exceeds 2^32 slots as N < 2^31).
+__device__ __forceinline__ uint32_t row_home(int z, int y, uint32_t rmask) {
+  uint32_t h = static_cast<uint32_t>(z) * 0x9E3779B1u + static_cast<uint32_t>(y);
+  h ^= h >> 16;
+  h *= 0x7FEB352Du;
+  h ^= h >> 15;
+  h *= 0x846CA68Bu;
+  h ^= h >> 16;
+  return h & rmask;
+}
+
+// Row (zq, yq) of the row table: [start, end), or start = -1 if absent.
+__device__ __forceinline__ void find_row(const Slot* __restrict__ table, uint32_t rmask, int zq, int yq,
+                                         int32_t& start, int32_t& end) {
+  start = -1;
+  end = -1;
+  const unsigned long long rk = row_key(zq, yq);
+  uint32_t h = row_home(zq, yq, rmask);
+  for (uint32_t probe = 0; probe <= rmask; ++probe) {
+    const int4 sl = __ldg(reinterpret_cast<const int4*>(table + h));
+    const unsigned long long sk =
+        (static_cast<unsigned long long>(static_cast<uint32_t>(sl.y)) << 32) | static_cast<uint32_t>(sl.x);
+    if (sk == rk) {
+      start = sl.z;
+      end = sl.z + sl.w;
+      return;
+    }
+    if (sk == kEmptyKey) return;
+    h = (h + 1u) & rmask;
+  }
+}
+
+// First j in [lo, hi) whose x is >= t (hi if none); x values increase over
+// the range (one row of sorted input).
+__device__ __forceinline__ int32_t row_lower_bound(const int32_t* __restrict__ xs, int32_t lo, int32_t hi,
+                                                   int t) {
+  while (lo < hi) {
+    const int32_t mid = static_cast<int32_t>((static_cast<uint32_t>(lo) + static_cast<uint32_t>(hi)) >> 1);
+    if (__ldg(xs + 3 * static_cast<int64_t>(mid)) < t) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
 }
 
 __device__ __forceinline__ unsigned long long voxel_key(const int32_t* __restrict__ coords, int64_t j) {
@@ -198,10 +245,10 @@ __global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n
   if (!(f & kFlagUnsorted)) {
     // sorted input: the first voxel of each (z, y) row inserts the row
     if (i > 0 && coords[3 * (i - 1)] == z && coords[3 * (i - 1) + 1] == y) return;
-    const unsigned long long rmask = row_capacity(static_cast<unsigned int>(flags[1])) - 1ull;
+    const uint32_t rmask = static_cast<uint32_t>(row_capacity(static_cast<unsigned int>(flags[1])) - 1ull);
     const unsigned long long rk = row_key(z, y);
-    unsigned long long h = mix_hash(rk) & rmask;
-    for (unsigned long long probe = 0; probe <= rmask; ++probe) {
+    uint32_t h = row_home(z, y, rmask);
+    for (uint32_t probe = 0; probe <= rmask; ++probe) {
       const unsigned long long prev = atomicCAS(&table[h].key, kEmptyKey, rk);
       if (prev == kEmptyKey) {
         // The row's first voxel and its length: the first index past i whose
@@ -230,7 +277,7 @@ __global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n
         atomicOr(flags, kFlagDuplicate);
         return;
       }
-      h = (h + 1) & rmask;
+      h = (h + 1u) & rmask;
     }
     atomicOr(flags, kFlagFull);
     return;
@@ -256,61 +303,84 @@ __global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n
   atomicOr(flags, kFlagFull);
 }
 
-// Sorted input: nmap[k, n] for every offset, by row probe + search.
+// Sorted input: nmap[k, n] for every offset, by row probe + search.  The
+// loop is short on instructions (this kernel is issue-bound): 32-bit
+// indices, a 32-bit row hash, and for the lexicographic 3x3x3 offset list
+// (kStd27) everything unrolled: per (dz, dy) row one probe, one bisection
+// for x - 1, then direct checks for x and x + 1; the voxel's own row needs
+// no probe (x - 1 and x + 1 can only be its neighbours in the array).
+template <bool kStd27>
 __global__ void __launch_bounds__(kThreads)
     nmap_query_rows_kernel(const int32_t* __restrict__ coords, int64_t n, const Slot* __restrict__ table,
                            const int* __restrict__ flags, const __grid_constant__ QueryPlan plan,
                            int32_t* __restrict__ nmap) {
   const int f = flags[0];
   if (f & (kFlagRange | kFlagUnsorted)) return;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int32_t i = static_cast<int32_t>(blockIdx.x) * static_cast<int32_t>(blockDim.x) + static_cast<int32_t>(threadIdx.x);
   if (i >= n) return;
-  const unsigned long long rmask = row_capacity(static_cast<unsigned int>(flags[1])) - 1ull;
-  const int z = __ldg(coords + 3 * i), y = __ldg(coords + 3 * i + 1), x = __ldg(coords + 3 * i + 2);
-  const int32_t missing = static_cast<int32_t>(n);
-  for (int32_t g = 0; g < plan.groups; ++g) {
-    const int zq = z + plan.grp_dz[g], yq = y + plan.grp_dy[g];
-    const int m0 = plan.grp_first[g], m1 = m0 + plan.grp_count[g];
-    int64_t start = -1;  // first voxel of row (zq, yq)
-    int64_t end = -1;    // one past its last voxel
-    if (in_grid(zq) && in_grid(yq)) {
-      const unsigned long long rk = row_key(zq, yq);
-      unsigned long long h = mix_hash(rk) & rmask;
-      for (unsigned long long probe = 0; probe <= rmask; ++probe) {
-        const int4 sl = __ldg(reinterpret_cast<const int4*>(table + h));
-        const unsigned long long sk =
-            (static_cast<unsigned long long>(static_cast<uint32_t>(sl.y)) << 32) | static_cast<uint32_t>(sl.x);
-        if (sk == rk) {
-          start = sl.z;
-          end = start + sl.w;
-          break;
-        }
-        if (sk == kEmptyKey) break;
-        h = (h + 1) & rmask;
-      }
-    }
-    // Within [start, end) the cells are one row, increasing in x: each search
-    // compares x only.  Members come in ascending dx, so each search starts
-    // where the last one ended.
-    int64_t cur = start;
-    for (int m = m0; m < m1; ++m) {
-      int32_t found = missing;
-      const int xq = x + plan.mem_dx[m];
-      if (start >= 0 && cur < end) {
-        int64_t lo = cur, hi = end;  // first j in [lo, end) with x_j >= xq
-        if (__ldg(coords + 3 * lo + 2) >= xq) {
-          hi = lo;
+  const int32_t n32 = static_cast<int32_t>(n);
+  const uint32_t rmask = static_cast<uint32_t>(row_capacity(static_cast<unsigned int>(flags[1])) - 1ull);
+  const int32_t* xs = coords + 2;
+  const int z = __ldg(coords + 3 * static_cast<int64_t>(i)), y = __ldg(coords + 3 * static_cast<int64_t>(i) + 1);
+  const int x = __ldg(xs + 3 * static_cast<int64_t>(i));
+  const int32_t missing = n32;
+  if constexpr (kStd27) {
+#pragma unroll
+    for (int dz = -1; dz <= 1; ++dz) {
+#pragma unroll
+      for (int dy = -1; dy <= 1; ++dy) {
+        const int k0 = 9 * (dz + 1) + 3 * (dy + 1);  // offset (dz, dy, -1); +1, +2 follow
+        int32_t r0 = missing, r1 = missing, r2 = missing;
+        if (dz == 0 && dy == 0) {
+          r1 = i;
+          if (i > 0 && __ldg(xs + 3 * static_cast<int64_t>(i - 1)) == x - 1 &&
+              __ldg(coords + 3 * static_cast<int64_t>(i - 1)) == z &&
+              __ldg(coords + 3 * static_cast<int64_t>(i - 1) + 1) == y)
+            r0 = i - 1;
+          if (i + 1 < n32 && __ldg(xs + 3 * static_cast<int64_t>(i + 1)) == x + 1 &&
+              __ldg(coords + 3 * static_cast<int64_t>(i + 1)) == z &&
+              __ldg(coords + 3 * static_cast<int64_t>(i + 1) + 1) == y)
+            r2 = i + 1;
         } else {
-          while (hi - lo > 1) {  // x_lo < xq; hi == end or x_hi >= xq
-            const int64_t mid = lo + (hi - lo) / 2;
-            if (__ldg(coords + 3 * mid + 2) >= xq) hi = mid;
-            else lo = mid;
+          const int zq = z + dz, yq = y + dy;
+          int32_t start = -1, end = -1;
+          if (in_grid(zq) && in_grid(yq)) find_row(table, rmask, zq, yq, start, end);
+          if (start >= 0) {
+            int32_t j = row_lower_bound(xs, start, end, x - 1);
+            int xj = j < end ? __ldg(xs + 3 * static_cast<int64_t>(j)) : INT_MAX;
+            if (xj == x - 1) {
+              r0 = j++;
+              xj = j < end ? __ldg(xs + 3 * static_cast<int64_t>(j)) : INT_MAX;
+            }
+            if (xj == x) {
+              r1 = j++;
+              xj = j < end ? __ldg(xs + 3 * static_cast<int64_t>(j)) : INT_MAX;
+            }
+            if (xj == x + 1) r2 = j;
           }
         }
-        if (hi < end && __ldg(coords + 3 * hi + 2) == xq) found = static_cast<int32_t>(hi);
-        cur = hi;
+        nmap[static_cast<int64_t>(k0) * n + i] = r0;
+        nmap[static_cast<int64_t>(k0 + 1) * n + i] = r1;
+        nmap[static_cast<int64_t>(k0 + 2) * n + i] = r2;
       }
-      nmap[static_cast<int64_t>(plan.mem_k[m]) * n + i] = found;
+    }
+  } else {
+    for (int32_t g = 0; g < plan.groups; ++g) {
+      const int zq = z + plan.grp_dz[g], yq = y + plan.grp_dy[g];
+      const int m0 = plan.grp_first[g], m1 = m0 + plan.grp_count[g];
+      int32_t start = -1, end = -1;
+      if (in_grid(zq) && in_grid(yq)) find_row(table, rmask, zq, yq, start, end);
+      // Members come in ascending dx: each search starts where the last ended.
+      int32_t cur = start;
+      for (int m = m0; m < m1; ++m) {
+        int32_t found = missing;
+        if (start >= 0 && cur < end) {
+          const int xq = x + plan.mem_dx[m];
+          cur = row_lower_bound(xs, cur, end, xq);
+          if (cur < end && __ldg(xs + 3 * static_cast<int64_t>(cur)) == xq) found = cur;
+        }
+        nmap[static_cast<int64_t>(plan.mem_k[m]) * n + i] = found;
+      }
     }
   }
 }
@@ -485,7 +555,13 @@ spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOff
   hash_insert_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, flags);
   if (!cuda_ok(cudaGetLastError(), "hash_insert_kernel launch", &st)) return st;
 
-  nmap_query_rows_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, flags, plan, nmap);
+  bool std27 = k == 27;
+  for (int32_t a = 0; a < k && std27; ++a)
+    std27 = offs.d[3 * a] == a / 9 - 1 && offs.d[3 * a + 1] == (a / 3) % 3 - 1 && offs.d[3 * a + 2] == a % 3 - 1;
+  if (std27)
+    nmap_query_rows_kernel<true><<<grid, kThreads, 0, stream>>>(coords, n, table, flags, plan, nmap);
+  else
+    nmap_query_rows_kernel<false><<<grid, kThreads, 0, stream>>>(coords, n, table, flags, plan, nmap);
   if (!cuda_ok(cudaGetLastError(), "nmap_query_rows_kernel launch", &st)) return st;
   nmap_query_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, flags, plan, k, nmap);
   if (!cuda_ok(cudaGetLastError(), "nmap_query_kernel launch", &st)) return st;
