@@ -23,7 +23,8 @@ import numpy as np
 
 __all__ = [
     "SpconvError", "load_library", "library_path", "version", "workspace_size", "build_nmap",
-    "submconv3d", "submconv3d_dgrad", "submconv3d_wgrad", "count_valid_pairs", "device_status",
+    "submconv3d", "submconv3d_dgrad", "submconv3d_wgrad", "tile_order", "count_valid_pairs",
+    "device_status",
     "default_offsets", "ACTIVATIONS",
     "F32", "TF32", "BF16",
 ]
@@ -88,6 +89,11 @@ def load_library() -> ctypes.CDLL:
         lib.spconv_submconv3d_dgrad.restype = ctypes.c_int
         lib.spconv_submconv3d_wgrad.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, ctypes.c_int, vp]
         lib.spconv_submconv3d_wgrad.restype = ctypes.c_int
+        lib.spconv_submconv3d_ordered.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, ctypes.c_int,
+                                                  vp]
+        lib.spconv_submconv3d_ordered.restype = ctypes.c_int
+        lib.spconv_tile_order.argtypes = [vp, i64, i32, vp, vp]
+        lib.spconv_tile_order.restype = ctypes.c_int
         lib.spconv_count_valid_pairs.argtypes = [vp, i64, i32, vp, vp]
         lib.spconv_count_valid_pairs.restype = ctypes.c_int
         lib.spconv_device_status.argtypes = [vp]
@@ -207,7 +213,7 @@ ACTIVATIONS = {None: 0, "none": 0, "relu": 1, "silu": 2}
 
 
 def submconv3d(feats, nmap, w, bias=None, out=None, dtype=None, stream=None, residual=None,
-               activation=None):
+               activation=None, order=None):
     """Fused submanifold convolution.  feats (N, Ci), w (K, Ci, Co), bias (Co,)
     or None, all in one storage dtype (float32 or bfloat16); nmap (K, N) int32.
     ``dtype``: None (float32 -> exact "f32", bfloat16 -> "bf16") or "tf32"
@@ -215,7 +221,11 @@ def submconv3d(feats, nmap, w, bias=None, out=None, dtype=None, stream=None, res
 
     ``residual`` (N, Co) and ``activation`` ("relu" or "silu") select the
     fused epilogue out = act(conv + bias + residual) (spconv_submconv3d_ex);
-    ``out`` may be the residual tensor itself."""
+    ``out`` may be the residual tensor itself.
+
+    ``order`` (N,) int32, a permutation from ``tile_order``, forms the tiles
+    along it (spconv_submconv3d_ordered): the same result, fewer empty rows
+    gathered for scattered inputs.  Not combined with the fused epilogue."""
     torch = _torch()
     code = _dtype_code(feats, dtype)
     _require_cuda(feats, "feats", feats.dtype)
@@ -245,7 +255,15 @@ def submconv3d(feats, nmap, w, bias=None, out=None, dtype=None, stream=None, res
             raise ValueError("out must have shape (N, Co)")
     lib = load_library()
     act = ACTIVATIONS[activation]
-    if residual is None and act == 0:
+    if order is not None:
+        _require_cuda(order, "order", torch.int32)
+        if tuple(order.shape) != (n,):
+            raise ValueError("order must have shape (N,)")
+        if residual is not None or act != 0:
+            raise ValueError("order is not combined with the fused epilogue")
+        _check(lib.spconv_submconv3d_ordered(_ptr(feats), _ptr(nmap), _ptr(order), _ptr(w), _ptr(bias),
+                                             _ptr(out), n, k, ci, co, code, _stream_handle(stream)))
+    elif residual is None and act == 0:
         _check(lib.spconv_submconv3d(_ptr(feats), _ptr(nmap), _ptr(w), _ptr(bias), _ptr(out), n, k,
                                      ci, co, code, _stream_handle(stream)))
     else:
@@ -299,6 +317,23 @@ def submconv3d_wgrad(feats, dout, nmap, k=None, with_bias=True, stream=None):
     _check(load_library().spconv_submconv3d_wgrad(_ptr(feats), _ptr(dout), _ptr(nmap), _ptr(dw), _ptr(db),
                                                    n, kk, ci, co, code, _stream_handle(stream)))
     return (dw, db) if with_bias else dw
+
+
+def tile_order(nmap, out=None, stream=None):
+    """A tile order for ``submconv3d(..., order=...)``: (N,) int32, a
+    permutation of the voxels; within chunks of 4096 consecutive voxels they
+    are sorted by neighbour mask (spconv_tile_order)."""
+    torch = _torch()
+    _require_cuda(nmap, "nmap", torch.int32)
+    k, n = nmap.shape
+    if out is None:
+        out = torch.empty(n, dtype=torch.int32, device=nmap.device)
+    else:
+        _require_cuda(out, "out", torch.int32)
+        if tuple(out.shape) != (n,):
+            raise ValueError("out must have shape (N,)")
+    _check(load_library().spconv_tile_order(_ptr(nmap), n, k, _ptr(out), _stream_handle(stream)))
+    return out
 
 
 def count_valid_pairs(nmap, stream=None) -> int:

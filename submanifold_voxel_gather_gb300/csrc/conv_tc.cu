@@ -80,6 +80,7 @@ struct TcParams {
   const __nv_bfloat16* bias;
   const __nv_bfloat16* residual;  // (N, co) or null; may alias out
   __nv_bfloat16* out;
+  const int32_t* order;  // tile slot -> voxel (a permutation of 0..N-1), or null for identity
   int64_t n;
   int64_t num_tiles;
   int32_t k;
@@ -120,6 +121,16 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
       : "r"(static_cast<uint32_t>(v))
       : "memory");
   return r != 0u;
+}
+
+// Voxel (map column, output row) of tile slot `slot`, or -1: the identity,
+// or the caller's tile order.  Entries of the order outside [0, N) are
+// treated as empty slots.
+__device__ __forceinline__ int64_t slot_voxel(const int32_t* order, int64_t slot, int64_t n) {
+  if (slot >= n) return -1;
+  if (order == nullptr) return slot;
+  const int32_t v = __ldg(order + slot);
+  return (v >= 0 && v < n) ? v : -1;
 }
 
 // Kept offsets: every row with a valid entry, and the last offset of a tile
@@ -211,16 +222,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
       const int64_t n0 = t * TILE_N;
+      int64_t col[kLoaderPerLane];  // map column of each of this lane's slots, or -1
+#pragma unroll
+      for (int j = 0; j < kLoaderPerLane; ++j) col[j] = slot_voxel(p.order, n0 + lane + 32 * j, n_rows);
       for (int k0 = 0; k0 < k_count && ok; k0 += 4) {
         int32_t v[4][kLoaderPerLane];
 #pragma unroll
         for (int b = 0; b < 4; ++b)
 #pragma unroll
           for (int j = 0; j < kLoaderPerLane; ++j) {
-            const int64_t n = n0 + lane + 32 * j;
             v[b][j] = -1;
-            if (k0 + b < k_count && n < n_rows)
-              v[b][j] = __ldg(p.nmap + static_cast<int64_t>(k0 + b) * n_rows + n);
+            if (k0 + b < k_count && col[j] >= 0)
+              v[b][j] = __ldg(p.nmap + static_cast<int64_t>(k0 + b) * n_rows + col[j]);
           }
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
@@ -493,8 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.residual != nullptr && q < 32 * ppr) {
           const int r = q / ppr;
           const int c8 = q - r * ppr;
-          if (nb + r < n_rows)
-            res[mb][j] = __ldg(reinterpret_cast<const uint4*>(p.residual + (nb + r) * p.co + p.co_base +
+          const int64_t row = slot_voxel(p.order, nb + r, n_rows);
+          if (row >= 0)
+            res[mb][j] = __ldg(reinterpret_cast<const uint4*>(p.residual + row * p.co + p.co_base +
                                                               mb * 128 + c8 * 8));
         }
       }
@@ -527,8 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = et; q < 32 * chunks_per_row; q += 128) {
             const int r = q / chunks_per_row;
             const int c8 = q - r * chunks_per_row;
-            const int64_t n = n0 + vc * 32 + r;
-            if (n < n_rows)
+            const int64_t n = slot_voxel(p.order, n0 + vc * 32 + r, n_rows);
+            if (n >= 0)
               *reinterpret_cast<uint4*>(p.out + n * p.co + p.co_base + c8 * 8) =
                   *reinterpret_cast<const uint4*>(stage_out + r * kOutStride + c8 * 8);
           }
@@ -556,7 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (q >= 32 * ppr) continue;
               const int r = q / ppr;
               const int c8 = q - r * ppr;
-              if (nb + r >= n_rows) continue;
+              const int64_t row = slot_voxel(p.order, nb + r, n_rows);
+              if (row < 0) continue;
               const float4 a0 = *reinterpret_cast<const float4*>(stage_f + r * 128 + c8 * 8);
               const float4 a1 = *reinterpret_cast<const float4*>(stage_f + r * 128 + c8 * 8 + 4);
               const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
@@ -570,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
                 o[h] = *reinterpret_cast<const uint32_t*>(&pr);
               }
-              *reinterpret_cast<uint4*>(p.out + (nb + r) * p.co + p.co_base + mb * 128 + c8 * 8) =
+              *reinterpret_cast<uint4*>(p.out + row * p.co + p.co_base + mb * 128 + c8 * 8) =
                   make_uint4(o[0], o[1], o[2], o[3]);
             }
             if (vc + 1 < TILE_N / 32) load_residual(mb, nb + 32);
@@ -695,7 +710,7 @@ spconv_status read_and_clear_device_error(cudaStream_t stream, unsigned int* bit
 spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_t* nmap,
                              const void* w, const void* bias, const void* residual, void* out,
                              int64_t n, int32_t k, int32_t ci, int32_t co, spconv_activation act,
-                             bool dgrad, cudaStream_t stream) {
+                             bool dgrad, cudaStream_t stream, const int32_t* order) {
   if (dtype != SPCONV_BF16) return fail(SPCONV_ERR_UNSUPPORTED, "tensor-core path supports bf16 only");
   spconv_status st = SPCONV_OK;
   EncodeTiledFn encode = encode_fn(&st);
@@ -728,6 +743,7 @@ spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_
     p.act = static_cast<int32_t>(act);
     p.dgrad = dgrad ? 1 : 0;
     p.out = static_cast<__nv_bfloat16*>(out);
+    p.order = order;
     p.n = n;
     p.k = k;
     p.ci = ci;

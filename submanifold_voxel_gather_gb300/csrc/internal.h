@@ -47,10 +47,18 @@ spconv_status launch_conv_simt_f32(const float* feats, const int32_t* nmap, cons
 // ---- tensor-core convolution (conv_tc.cu); dtype is SPCONV_BF16.  With
 // dgrad, ci/co are the dout/dfeats widths (forward Co/Ci), feats is dout and
 // the weights of offset k are w[K-1-k] transposed (forward layout in place).
+// `order`, if not null, is a permutation of 0..N-1: tile slot s gathers the
+// map column order[s] and writes output row order[s] (forward only).
 spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_t* nmap,
                              const void* w, const void* bias, const void* residual, void* out,
                              int64_t n, int32_t k, int32_t ci, int32_t co, spconv_activation act,
-                             bool dgrad, cudaStream_t stream);
+                             bool dgrad, cudaStream_t stream, const int32_t* order = nullptr);
+
+// ---- tile order (nmap_hash.cu): order[s] for s in chunks of kTileOrderChunk
+// consecutive voxels, each chunk's voxels sorted by neighbour mask
+constexpr int kTileOrderChunk = 4096;
+spconv_status launch_tile_order(const int32_t* nmap, int64_t n, int32_t k, int32_t* order,
+                                cudaStream_t stream);
 
 // ---- weight / bias gradients, exact fp32 on CUDA cores (wgrad_simt.cu)
 spconv_status launch_wgrad_simt(spconv_dtype dtype, const void* feats, const void* dout,

@@ -443,6 +443,51 @@ __global__ void count_valid_kernel(const int32_t* __restrict__ nmap, int64_t tot
 
 __global__ void zero_u64_kernel(unsigned long long* p) { *p = 0; }
 
+// Tile order: within each chunk of kTileOrderChunk consecutive voxels, the
+// voxels sorted by their neighbour mask (bit k set when nmap[k, n] is a
+// neighbour, for the first 32 offsets), ties by index.  Tiles then hold
+// voxels with like masks, so fewer of a tile's gathered rows are empty;
+// chunks keep the tiles spatially local.  One block per chunk: the keys
+// (mask, index) are sorted in shared memory with a bitonic network.
+constexpr int kOrderThreads = 1024;
+
+__global__ void __launch_bounds__(kOrderThreads)
+    tile_order_kernel(const int32_t* __restrict__ nmap, int64_t n, int32_t k, int32_t* __restrict__ order) {
+  __shared__ unsigned long long keys[kTileOrderChunk];
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kTileOrderChunk;
+  const int count = static_cast<int>(n - base < kTileOrderChunk ? n - base : kTileOrderChunk);
+  const int kk = k < 32 ? k : 32;
+  for (int t = threadIdx.x; t < kTileOrderChunk; t += kOrderThreads) {
+    unsigned long long key = ~0ull;  // padding sorts last
+    if (t < count) {
+      uint32_t mask = 0;
+      for (int j = 0; j < kk; ++j) {
+        const int32_t v = __ldg(nmap + static_cast<int64_t>(j) * n + base + t);
+        mask |= (v >= 0 && v < n ? 1u : 0u) << j;
+      }
+      key = (static_cast<unsigned long long>(mask) << 32) | static_cast<unsigned int>(t);
+    }
+    keys[t] = key;
+  }
+  __syncthreads();
+  for (int size = 2; size <= kTileOrderChunk; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = threadIdx.x; t < kTileOrderChunk / 2; t += kOrderThreads) {
+        const int i = 2 * t - (t & (stride - 1));  // first element of pair t
+        const int j = i + stride;
+        const unsigned long long a = keys[i], b = keys[j];
+        if ((a > b) == ((i & size) == 0)) {  // ascending where bit `size` of i is 0
+          keys[i] = b;
+          keys[j] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int t = threadIdx.x; t < count; t += kOrderThreads)
+    order[base + t] = static_cast<int32_t>(base + static_cast<int64_t>(keys[t] & 0xFFFFFFFFull));
+}
+
 }  // namespace
 
 size_t hash_capacity(int64_t n) {
@@ -582,6 +627,16 @@ spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOff
   if (host_flags & kFlagDuplicate)
     return fail(SPCONV_ERR_DUPLICATE_COORD, "two voxels share a coordinate");
   if (host_flags & kFlagFull) return fail(SPCONV_ERR_DEVICE, "hash table overflow");
+  return SPCONV_OK;
+}
+
+spconv_status launch_tile_order(const int32_t* nmap, int64_t n, int32_t k, int32_t* order,
+                                cudaStream_t stream) {
+  spconv_status st = SPCONV_OK;
+  if (n == 0) return SPCONV_OK;
+  const int64_t chunks = (n + kTileOrderChunk - 1) / kTileOrderChunk;
+  tile_order_kernel<<<static_cast<unsigned>(chunks), kOrderThreads, 0, stream>>>(nmap, n, k, order);
+  if (!cuda_ok(cudaGetLastError(), "tile_order_kernel launch", &st)) return st;
   return SPCONV_OK;
 }
 

@@ -196,7 +196,8 @@ namespace {
 spconv_status submconv3d_impl(const void* feats_dev, const int32_t* nmap_dev, const void* w_dev,
                               const void* bias_dev, const void* residual_dev, void* out_dev, int64_t N,
                               int32_t K, int32_t Ci, int32_t Co, spconv_dtype dtype,
-                              spconv_activation act, bool dgrad, void* stream) {
+                              spconv_activation act, bool dgrad, void* stream,
+                              const int32_t* order = nullptr) {
   if (N < 0 || N >= INT32_MAX) return fail(SPCONV_ERR_INVALID_ARG, "N must satisfy 0 <= N < 2^31-1");
   if (K < 1 || Ci < 1 || Co < 1) return fail(SPCONV_ERR_INVALID_ARG, "K, Ci and Co must be >= 1");
   if (dtype != SPCONV_F32 && dtype != SPCONV_TF32 && dtype != SPCONV_BF16)
@@ -236,7 +237,7 @@ spconv_status submconv3d_impl(const void* feats_dev, const int32_t* nmap_dev, co
                               K, Ci, Co, act, dgrad, s);
   else
     st = launch_conv_tc(dtype, feats_dev, nmap_dev, w_dev, bias_dev, residual_dev, out_dev, N, K, Ci,
-                        Co, act, dgrad, s);
+                        Co, act, dgrad, s, order);
   return st == SPCONV_OK ? ok() : st;
 }
 
@@ -248,6 +249,30 @@ spconv_status spconv_submconv3d(const void* feats_dev, const int32_t* nmap_dev, 
                                 int32_t Ci, int32_t Co, spconv_dtype dtype, void* stream) {
   return spconv::submconv3d_impl(feats_dev, nmap_dev, w_dev, bias_dev, nullptr, out_dev, N, K, Ci, Co,
                                  dtype, SPCONV_ACT_NONE, false, stream);
+}
+
+spconv_status spconv_submconv3d_ordered(const void* feats_dev, const int32_t* nmap_dev,
+                                        const int32_t* order_dev, const void* w_dev,
+                                        const void* bias_dev, void* out_dev, int64_t N, int32_t K,
+                                        int32_t Ci, int32_t Co, spconv_dtype dtype, void* stream) {
+  if (N > 0 && (order_dev == nullptr || !spconv::aligned(order_dev, 4)))
+    return fail(SPCONV_ERR_INVALID_ARG, "order must be non-NULL and 4-byte aligned");
+  return spconv::submconv3d_impl(feats_dev, nmap_dev, w_dev, bias_dev, nullptr, out_dev, N, K, Ci, Co,
+                                 dtype, SPCONV_ACT_NONE, false, stream, order_dev);
+}
+
+spconv_status spconv_tile_order(const int32_t* nmap_dev, int64_t N, int32_t K, int32_t* order_dev,
+                                void* stream) {
+  if (N < 0 || N >= INT32_MAX || K < 1) return fail(SPCONV_ERR_INVALID_ARG, "bad N or K");
+  if (N == 0) return spconv::ok();
+  if (nmap_dev == nullptr || order_dev == nullptr)
+    return fail(SPCONV_ERR_INVALID_ARG, "nmap and order must be non-NULL");
+  if (!spconv::aligned(nmap_dev, 4) || !spconv::aligned(order_dev, 4))
+    return fail(SPCONV_ERR_INVALID_ARG, "nmap and order must be 4-byte aligned");
+  spconv_status st = spconv::check_device();
+  if (st != SPCONV_OK) return st;
+  st = spconv::launch_tile_order(nmap_dev, N, K, order_dev, static_cast<cudaStream_t>(stream));
+  return st == SPCONV_OK ? spconv::ok() : st;
 }
 
 spconv_status spconv_submconv3d_ex(const void* feats_dev, const int32_t* nmap_dev,

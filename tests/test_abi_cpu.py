@@ -31,7 +31,8 @@ def test_header_declares_the_boundary():
     for required in ("spconv_build_nmap", "spconv_submconv3d", "spconv_build_nmap_workspace_size",
                      "spconv_last_error", "spconv_version", "spconv_count_valid_pairs",
                      "spconv_device_status", "spconv_submconv3d_ex", "spconv_submconv3d_dgrad",
-                     "spconv_submconv3d_wgrad", "spconv_build_nmap_async"):
+                     "spconv_submconv3d_wgrad", "spconv_build_nmap_async", "spconv_tile_order",
+                     "spconv_submconv3d_ordered"):
         assert required in names
 
 
@@ -109,6 +110,24 @@ def test_argument_validation_without_gpu(lib):
     assert _status(ba(fake, -1, optr, 27, fake, fake, 1 << 30, fake, None))[0] == -1
     # count
     assert _status(lib.spconv_count_valid_pairs(fake, 10, 27, None, None))[0] == -1
+
+
+def test_order_entry_points_validate_without_gpu(lib):
+    fake = ctypes.c_void_p(0x100000)  # never dereferenced: validation fails first
+    to = lib.spconv_tile_order
+    assert _status(to(fake, -1, 27, fake, None))[0] == -1
+    assert _status(to(fake, 10, 0, fake, None))[0] == -1
+    assert _status(to(None, 10, 27, fake, None))[0] == -1
+    assert _status(to(fake, 10, 27, None, None))[0] == -1
+    assert _status(to(fake, 10, 27, ctypes.c_void_p(0x100002), None))[0] == -1
+    assert _status(to(None, 0, 27, None, None))[0] == 0
+    od = lib.spconv_submconv3d_ordered
+    code, msg = _status(od(fake, fake, None, fake, None, fake, 10, 27, 16, 16, 2, None))
+    assert code == -1 and "order" in msg
+    code, msg = _status(od(fake, fake, ctypes.c_void_p(0x100002), fake, None, fake, 10, 27, 16, 16, 2, None))
+    assert code == -1 and "order" in msg
+    assert _status(od(fake, fake, fake, fake, None, fake, 10, 27, 24, 16, 2, None))[0] == -2
+    assert _status(od(None, None, None, None, None, None, 0, 27, 16, 16, 2, None))[0] == 0
 
 
 def test_python_binding_rejects_cpu_tensors(lib):
