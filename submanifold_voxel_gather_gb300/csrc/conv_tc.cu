@@ -91,6 +91,7 @@ struct TcParams {
   int32_t act;       // spconv_activation
   int32_t dgrad;     // input gradient: selects the kDgrad instantiation
   int32_t num_chunks;
+  int32_t cps;       // 64-channel chunks per stage: 2 when Ci % 128 == 0 and Co <= 128, else 1
   uint32_t stages;
   uint32_t stage_bytes;
   uint32_t w_bytes;  // weight bytes per stage (M blocks x 16 KB)
@@ -317,15 +318,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!go) continue;
         issued = true;
-        for (int c = 0; c < p.num_chunks; ++c) {
+        for (int cg = 0; cg < p.num_chunks; cg += p.cps) {
           if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&empty[stage]), st_phase ^ 1))) {
             ok = false;
             break;
           }
+          for (int sub = 0; sub < p.cps; ++sub) {  // the stage's chunks, one row block each
+          const int c = cg + sub;
           const uint32_t col_byte = static_cast<uint32_t>(c) * 128u + static_cast<uint32_t>(chunk16) * 16u;
           const bool col_ok = col_byte < row_bytes;
           const char* chunk_base = feats + col_byte;
-          const uint32_t f_dst = smem_addr(smem + stage * p.stage_bytes) + p.w_bytes + dst_lane;
+          const uint32_t f_dst = smem_addr(smem + stage * p.stage_bytes) + p.w_bytes +
+                                 static_cast<uint32_t>(sub) * (TILE_N * 128u) + dst_lane;
           if constexpr (kHoist) {
             const uint32_t live = col_ok ? valid_bits : 0u;
 #pragma unroll
@@ -340,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               cp_async_16<false>(f_dst + 512u * j + ((j & 1) ? sw_odd : sw_even),
                                  chunk_base + static_cast<uint64_t>(v) * row_bytes, valid ? 16u : 0u);
             }
+          }
           }
           cp_async_arrive_noinc(smem_addr(&full[stage]));
           if (++stage == S) {
@@ -372,31 +377,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           ephase ^= 1;
         }
         if (!go) continue;
-        for (int c = 0; c < p.num_chunks; ++c) {
+        for (int c = 0; c < p.num_chunks; c += p.cps) {
           if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&empty[stage]), st_phase ^ 1))) {
             ok = false;
             break;
           }
           const uint32_t fullb = smem_addr(&full[stage]);
           if (lane == 0) {
-            const int steps = min(kChunk, p.ci - c * kChunk) / kKPerMma;
+            const int steps = p.cps == 2 ? 2 * kChunk / kKPerMma : min(kChunk, p.ci - c * kChunk) / kKPerMma;
             meta[stage] = (static_cast<uint32_t>(steps) << 8) | (issued ? 0u : kMetaFirst);
             mbar_arrive_expect_tx(fullb, p.w_bytes);
           }
           __syncwarp();
           if constexpr (!kDgrad) {
             // forward: w[k] channel-major, two 64-channel boxes per M block
-            if (static_cast<int>(lane) < 2 * MBLK) {
+            // and chunk (with two chunks per stage, MBLK is 1: block = chunk)
+            if (static_cast<int>(lane) < 2 * MBLK * p.cps) {
               const int mb = static_cast<int>(lane) >> 1, half = static_cast<int>(lane) & 1;
+              const int sub = p.cps == 2 ? mb : 0, m = p.cps == 2 ? 0 : mb;
               tma_load_3d(smem_addr(smem + stage * p.stage_bytes) + mb * kWBlockBytes + half * 8192u,
-                          &tm_w, p.co_base + mb * 128 + half * 64, c * kChunk, kk, fullb);
+                          &tm_w, p.co_base + m * 128 + half * 64, (c + sub) * kChunk, kk, fullb);
             }
-          } else if (static_cast<int>(lane) < MBLK) {
+          } else if (static_cast<int>(lane) < MBLK * p.cps) {
             // input gradient: rows of w[K-1-k] (output channel = forward ci)
             // with 64 of their forward-co entries each, K-major
             const int mb = static_cast<int>(lane);
-            tma_load_3d(smem_addr(smem + stage * p.stage_bytes) + mb * kWBlockBytes, &tm_w, c * kChunk,
-                        p.co_base + mb * 128, k_count - 1 - kk, fullb);
+            const int sub = p.cps == 2 ? mb : 0, m = p.cps == 2 ? 0 : mb;
+            tma_load_3d(smem_addr(smem + stage * p.stage_bytes) + mb * kWBlockBytes, &tm_w, (c + sub) * kChunk,
+                        p.co_base + m * 128, k_count - 1 - kk, fullb);
           }
           issued = true;
           ++fills;
@@ -456,7 +464,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t ad = adesc0 + stage * stage_units;
         const uint64_t bd = bdesc0 + stage * stage_units;
         const uint32_t acc0 = (m & kMetaFirst) == 0u ? 1u : 0u;
-        if (steps == kChunk / kKPerMma) {
+        if (steps == 2 * kChunk / kKPerMma) {
+          // two chunks (MBLK == 1): weight block and row block of chunk 1
+          // follow those of chunk 0
+#pragma unroll
+          for (int s = 0; s < 2 * kChunk / kKPerMma; ++s) {
+            const int sub = s >> 2, ss = s & 3;
+            umma_f16(d_tmem, ad + sub * kWBlockUnits + ss * a_step,
+                     bd + sub * ((TILE_N * 128u) >> 4) + ss * kBStepUnits, idesc, s > 0 ? 1u : acc0);
+          }
+        } else if (steps == kChunk / kKPerMma) {
 #pragma unroll
           for (int s = 0; s < kChunk / kKPerMma; ++s)
 #pragma unroll
@@ -641,8 +658,8 @@ spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t str
   if (sms <= 0) return fail(SPCONV_ERR_CUDA, "could not query the SM count");
   p.num_tiles = (p.n + TILE_N - 1) / TILE_N;
   const int grid = static_cast<int>(p.num_tiles < sms ? p.num_tiles : sms);
-  p.w_bytes = MBLK * kWBlockBytes;
-  p.stage_bytes = p.w_bytes + TILE_N * 128u;
+  p.w_bytes = p.cps * MBLK * kWBlockBytes;
+  p.stage_bytes = p.w_bytes + p.cps * TILE_N * 128u;
   p.tmem_cols = 512u;  // kAccBufs accumulator buffers of MBLK x TILE_N columns
   // D f32, A and B bf16, B (gathered rows) K-major; A (weights) channel-major
   // for the forward pass, K-major for the input gradient.
@@ -751,6 +768,10 @@ spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_
     p.co_base = co_base;
     p.co_count = (co - co_base) < 256 ? (co - co_base) : 256;
     p.num_chunks = (ci + kChunk - 1) / kChunk;
+    // Two 64-channel chunks per stage where they fit (two 96 KB stages):
+    // a stage's cost is mostly fixed, so fewer, larger stages are faster
+    // (measured: decoder 8.3 -> 7.7 ms, medium 0.72 -> 0.64 ms).
+    p.cps = (ci % (2 * kChunk) == 0 && p.co_count <= 128) ? 2 : 1;
     const bool hoist = p.num_chunks >= 2;
     if (p.co_count <= 128)
       st = hoist ? launch_dir<1, true>(tm_w, p, stream) : launch_dir<1, false>(tm_w, p, stream);
