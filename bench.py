@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--workload", default="decoder")
     ap.add_argument("--layer", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-numa-bind", action="store_true",
+                    help="allocate the end-to-end pinned buffers without placing them near the GPU")
     ap.add_argument("--e2e-slots", type=int, default=3,
                     help="end-to-end steps in flight (one stream and buffer set each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -255,6 +257,33 @@ def to_device(torch, arr, dtype, dev):
     return torch.from_numpy(a).to(dev)
 
 
+def parse_cpulist(text):
+    """CPU ids of a Linux cpulist string such as "0-71,144-215"."""
+    cpus = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        lo, _, hi = part.partition("-")
+        cpus.update(range(int(lo), int(hi or lo) + 1))
+    return cpus
+
+
+def gpu_local_cpus(torch, dev):
+    """(NUMA node, CPU ids) of the host node nearest to `dev`, read from the
+    PCI device's sysfs entry, or None where that is not readable."""
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        bdf = "%04x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        base = os.path.join("/sys/bus/pci/devices", bdf)
+        with open(os.path.join(base, "numa_node")) as fh:
+            node = int(fh.read())
+        with open(os.path.join(base, "local_cpulist")) as fh:
+            cpus = parse_cpulist(fh.read())
+        return node, cpus
+    except (AttributeError, OSError, ValueError):
+        return None
+
+
 def host_pinned(torch, arr, dtype):
     a = np.ascontiguousarray(arr)
     t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if dtype == "bf16" else torch.from_numpy(a)
@@ -408,6 +437,20 @@ def run_ours(args):
     # ---- end to end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
+        # Pinned buffers are placed in the host memory nearest the GPU: the
+        # process runs on that node's CPUs while they are allocated (the
+        # kernel places their pages on the allocating CPU's node), then
+        # returns to its previous CPU set.
+        host_node = None
+        prev_cpus = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+        local = gpu_local_cpus(torch, dev) if not args.no_numa_bind else None
+        if local is not None and prev_cpus is not None:
+            node, cpus = local
+            cpus &= prev_cpus
+            bind = bool(cpus) and cpus != prev_cpus
+            if bind:
+                os.sched_setaffinity(0, cpus)
+            host_node = {"node": node, "local_cpus": len(cpus), "bound": bind}
         h_coords = torch.from_numpy(wl.coords).pin_memory()
         h_feats = host_pinned(torch, layer.feats, dtype)
         h_w = host_pinned(torch, layer.w, dtype)
@@ -432,6 +475,8 @@ def run_ours(args):
                 "nmap": torch.empty_like(nmap), "ws": torch.empty_like(ws), "out": torch.empty_like(out),
                 "status": torch.full((1,), -99, dtype=torch.int32, device=dev),
                 "h_out": torch.empty((n, co), dtype=feats.dtype).pin_memory()})
+        if host_node is not None and host_node["bound"]:
+            os.sched_setaffinity(0, prev_cpus)
 
         def e2e_step(i):
             sl, st = slots[i % nslots], streams[i % nslots]
@@ -469,7 +514,7 @@ def run_ours(args):
         d2h = slots[0]["h_out"].numel() * slots[0]["h_out"].element_size()
         e2e = {"value": job_tflops(world, flops, e2e_ms / args.steps), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e2e_ms / args.steps, "steps_in_flight": nslots}
+               "ms_per_step": e2e_ms / args.steps, "steps_in_flight": nslots, "host_node": host_node}
 
     if rank != 0:
         if pg is not None:
