@@ -33,7 +33,7 @@ def run_dgrad(sv, dout, nmap, w, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32", "tf32"])
-@pytest.mark.parametrize("ci,co", [(16, 16), (64, 64), (128, 128), (32, 80), (272, 64), (64, 256)])
+@pytest.mark.parametrize("ci,co", [(16, 16), (64, 64), (128, 128), (32, 80), (272, 64), (64, 256), (96, 384)])
 def test_dgrad_matches_oracle(sv, oracle_mod, dtype, ci, co):
     """Forward Ci (the dgrad output width) above 256 needs two launches; Co
     (the dgrad reduction width) not a multiple of 64 leaves a partial chunk."""

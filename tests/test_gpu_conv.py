@@ -68,11 +68,13 @@ def test_small_bf16_full(sv, oracle_mod):
 
 
 @pytest.mark.parametrize("ci,co", [(16, 16), (32, 48), (48, 80), (64, 64), (80, 128), (128, 256),
-                                   (256, 128), (64, 272), (16, 512)])
+                                   (256, 128), (384, 96), (64, 272), (16, 512)])
 @pytest.mark.parametrize("dtype", ["bf16", "tf32"])
 def test_channel_shapes(sv, oracle_mod, ci, co, dtype):
     """Ci / Co not multiples of the 64-element (bf16) or 32-element (tf32)
-    chunk, Co above 256 (several launches) and a ragged last tile."""
+    chunk, Co above 256 (several launches) and a ragged last tile.  In bf16,
+    Ci = 256 and 384 with Co <= 128 take two-chunk stages with per-chunk
+    barriers (two and three stages per offset)."""
     coords = W.random_occupancy(14, 0.25, ci + co)
     nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
     feats, w, b = layer_values(ci * 7 + co, len(coords), 27, ci, co, dtype)
