@@ -512,9 +512,35 @@ def run_ours(args):
             raise RuntimeError(f"map build reported status {bad} in the end-to-end loop")
         h2d = sum(t.numel() * t.element_size() for t in (h_coords, h_feats, h_w, h_bias))
         d2h = slots[0]["h_out"].numel() * slots[0]["h_out"].element_size()
+
+        # The same loop with the kernels left out (copies only), after the
+        # timed region: it tells the copies' own floor in this process from
+        # how well the loop overlaps them.
+        def copy_step(i):
+            sl, st = slots[i % nslots], streams[i % nslots]
+            with torch.cuda.stream(st):
+                sl["coords"].copy_(h_coords, non_blocking=True)
+                sl["feats"].copy_(h_feats, non_blocking=True)
+                sl["w"].copy_(h_w, non_blocking=True)
+                sl["bias"].copy_(h_bias, non_blocking=True)
+                sl["h_out"].copy_(sl["out"], non_blocking=True)
+
+        reps = max(nslots, min(args.steps, 6))
+        torch.cuda.synchronize(dev)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(main)
+        for st in streams:
+            st.wait_event(c0)
+        for i in range(reps):
+            copy_step(i)
+        for st in streams:
+            main.wait_stream(st)
+        c1.record(main)
+        torch.cuda.synchronize(dev)
         e2e = {"value": job_tflops(world, flops, e2e_ms / args.steps), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e2e_ms / args.steps, "steps_in_flight": nslots, "host_node": host_node}
+               "ms_per_step": e2e_ms / args.steps, "steps_in_flight": nslots, "host_node": host_node,
+               "copies_only_ms_per_step": c0.elapsed_time(c1) / reps}
 
     if rank != 0:
         if pg is not None:
