@@ -73,7 +73,13 @@ spconv_status launch_dbias(spconv_dtype dtype, const void* dout, float* dbias, i
 spconv_status launch_wgrad_tc(const void* feats, const void* dout, const int32_t* nmap, float* dw,
                               int64_t n, int32_t k, int32_t ci, int32_t co, cudaStream_t stream);
 
-// ---- device error word (ptx.cuh declares the symbol)
+// ---- device error words.  ptx.cuh gives each translation unit its own
+// copy, so every unit whose kernels can set it reads back its own: the
+// forward / input-gradient conv (conv_tc.cu) and the weight gradient
+// (wgrad_tc.cu).  Each call waits for the stream and clears the unit's
+// bits after reading them: the conv's call stores them in *bits, the weight
+// gradient's ORs them in, so call the conv's first.
 spconv_status read_and_clear_device_error(cudaStream_t stream, unsigned int* bits);
+spconv_status read_and_clear_wgrad_device_error(cudaStream_t stream, unsigned int* bits);
 
 }  // namespace spconv

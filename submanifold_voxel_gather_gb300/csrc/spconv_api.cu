@@ -354,6 +354,8 @@ spconv_status spconv_device_status(void* stream) {
   unsigned int bits = 0;
   spconv_status st = spconv::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &bits);
   if (st != SPCONV_OK) return st;
+  st = spconv::read_and_clear_wgrad_device_error(static_cast<cudaStream_t>(stream), &bits);
+  if (st != SPCONV_OK) return st;
   if (bits != 0) return fail(SPCONV_ERR_DEVICE, "device error bits 0x" + std::to_string(bits));
   return spconv::ok();
 }

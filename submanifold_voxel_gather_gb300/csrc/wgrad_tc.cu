@@ -509,6 +509,21 @@ EncodeTiledFn encode_fn(spconv_status* st) {
 
 }  // namespace
 
+spconv_status read_and_clear_wgrad_device_error(cudaStream_t stream, unsigned int* bits) {
+  spconv_status st = SPCONV_OK;
+  if (!cuda_ok(cudaStreamSynchronize(stream), "cudaStreamSynchronize", &st)) return st;
+  unsigned int mine = 0;
+  const unsigned int zero = 0;
+  if (!cuda_ok(cudaMemcpyFromSymbol(&mine, g_device_error, sizeof(unsigned int)),
+               "cudaMemcpyFromSymbol", &st))
+    return st;
+  if (!cuda_ok(cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned int)),
+               "cudaMemcpyToSymbol", &st))
+    return st;
+  *bits |= mine;
+  return SPCONV_OK;
+}
+
 spconv_status launch_wgrad_tc(const void* feats, const void* dout, const int32_t* nmap, float* dw,
                               int64_t n, int32_t k, int32_t ci, int32_t co, cudaStream_t stream) {
   spconv_status st = SPCONV_OK;
