@@ -63,43 +63,50 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="approximate CPU work of the oracle baseline sample")
     ap.add_argument("--materialized", action="store_true",
-                    help="also time the materialising gather + GEMM path (torch ops) with peak memory")
+                    help="also time the materialising gather + GEMM path on the headline workload")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload lines (and the materialising comparison on medium)")
     return ap.parse_args()
 
 
-def materialized_baseline(torch, sv, feats, nmap, w, bias, out_fused, reps=3):
-    """The path the page replaces, on this GPU: the (K, N, Ci) gather is
-    materialised (torch index_select over feats with a zero pad row appended,
-    so the sentinel N selects zeros) and contracted with cuBLAS GEMMs (torch
-    matmul, bf16 in, fp32 accumulation across chunks).  Two variants: the
-    whole gather at once (one GEMM with K = 27 Ci) and chunks of two offsets,
-    as the page describes the stock layer.  Not part of the library: torch
-    ops only, for the time and peak-memory comparison.  Returns a dict of
-    ms, peak GB and the largest difference from the fused output relative
-    to its largest magnitude."""
+def materialized_forward(torch, feats, nmap, w, bias, chunk):
+    """The path the page replaces, on this GPU, with torch ops only: the
+    (K, N, Ci) gather is materialised ``chunk`` offsets at a time
+    (index_select over feats with a zero pad row appended, so the sentinel N
+    selects zeros), each chunk is contracted by one cuBLAS GEMM with bf16
+    inputs and an fp32 result, the chunk results are summed in fp32, the
+    bias is added and the sum is rounded once.  Not part of the library."""
     k, n = nmap.shape
     ci, co = w.shape[1], w.shape[2]
     dev = feats.device
+    padded = torch.cat([feats, torch.zeros((1, ci), dtype=feats.dtype, device=dev)])
+    idx = torch.where((nmap >= 0) & (nmap < n), nmap, torch.full_like(nmap, n)).long()
+    acc = torch.zeros((n, co), dtype=torch.float32, device=dev)
+    for k0 in range(0, k, chunk):
+        k1 = min(k, k0 + chunk)
+        # voxel-major index order: the gather lands as (N, chunk * Ci) directly
+        g = padded.index_select(0, idx[k0:k1].t().reshape(-1)).view(n, (k1 - k0) * ci)
+        acc += torch.mm(g, w[k0:k1].reshape((k1 - k0) * ci, co), out_dtype=torch.float32)
+        del g
+    if bias is not None:
+        acc += bias.float()
+    return acc.to(feats.dtype)
 
-    def run(chunk):
-        padded = torch.cat([feats, torch.zeros((1, ci), dtype=feats.dtype, device=dev)])
-        idx = torch.where((nmap >= 0) & (nmap < n), nmap, torch.full_like(nmap, n)).long()
-        acc = torch.zeros((n, co), dtype=torch.float32, device=dev)
-        for k0 in range(0, k, chunk):
-            k1 = min(k, k0 + chunk)
-            # voxel-major index order: the gather lands as (N, chunk * Ci) directly
-            g = padded.index_select(0, idx[k0:k1].t().reshape(-1)).view(n, (k1 - k0) * ci)
-            acc += (g @ w[k0:k1].reshape((k1 - k0) * ci, co)).float()
-            del g
-        return (acc + bias.float()).to(feats.dtype)
 
+def materialized_baseline(torch, sv, feats, nmap, w, bias, out_fused, reps=3):
+    """Time and peak device memory of the materialising path (chunks of two
+    offsets, as the page describes the stock layer, and the whole gather at
+    once) next to the fused call, on the same inputs.  Peak memory is what
+    each path allocates beyond its inputs and output."""
+    k = nmap.shape[0]
+    dev = feats.device
     res = {}
     for name, chunk in (("chunks_of_2_offsets", 2), ("whole_gather", k)):
         torch.cuda.synchronize(dev)
         torch.cuda.empty_cache()
         base = torch.cuda.memory_allocated(dev)
         torch.cuda.reset_peak_memory_stats(dev)
-        got = run(chunk)
+        got = materialized_forward(torch, feats, nmap, w, bias, chunk)
         torch.cuda.synchronize(dev)
         peak = torch.cuda.max_memory_allocated(dev) - base
         diff = float((got.float() - out_fused.float()).abs().max() / out_fused.float().abs().max())
@@ -107,7 +114,7 @@ def materialized_baseline(torch, sv, feats, nmap, w, bias, out_fused, reps=3):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(reps):
-            r = run(chunk)
+            r = materialized_forward(torch, feats, nmap, w, bias, chunk)
             del r
         e1.record()
         torch.cuda.synchronize(dev)
@@ -294,11 +301,12 @@ def host_pinned(torch, arr, dtype):
 _PER_ROW_S = None
 
 
-def oracle_step(wl, layer, seconds, threads, seed):
+def oracle_step(wl, layer, seconds, threads, seed, keep=False):
     """One bounded oracle pass over a seeded sample of output rows: the
     neighbour-map rows (sort of all N voxels + binary searches) and the fp64
     conv loop nest of those rows, sized for about ``seconds`` of work on
-    ``threads`` threads.  Returns (flops, timed seconds, rows)."""
+    ``threads`` threads.  Returns (flops, timed seconds, rows), plus
+    (rows, exact out, sum |terms|) when ``keep``."""
     global _PER_ROW_S
     import oracle
     import workloads as W
@@ -308,21 +316,130 @@ def oracle_step(wl, layer, seconds, threads, seed):
         full = np.full((wl.K, n), n, dtype=np.int32)   # untimed: sampled columns only
         full[:, rows] = sub
         t0 = time.perf_counter()
-        oracle.conv(layer.feats, full, layer.w, layer.bias, layer.dtype, rows=rows, threads=nthreads)
-        return time.perf_counter() - t0
+        res = oracle.conv(layer.feats, full, layer.w, layer.bias, layer.dtype, rows=rows, threads=nthreads)
+        return time.perf_counter() - t0, res
 
     if _PER_ROW_S is None:   # untimed calibration
         cal = np.unique((W.draws_u64(7, 1, 0, 64) % np.uint64(n)).astype(np.int64))
-        _PER_ROW_S = max(conv_rows(oracle.nmap_rows(wl.coords, wl.offsets, cal), cal, 1) / len(cal),
+        _PER_ROW_S = max(conv_rows(oracle.nmap_rows(wl.coords, wl.offsets, cal), cal, 1)[0] / len(cal),
                          1e-6)
     count = int(max(256, min(n, seconds * threads / _PER_ROW_S)))
     rows = np.unique((W.draws_u64(seed, 2, 0, count) % np.uint64(n)).astype(np.int64))
     t0 = time.perf_counter()
     sub = oracle.nmap_rows(wl.coords, wl.offsets, rows)
     t_map = time.perf_counter() - t0
-    t_conv = conv_rows(sub, rows, threads)
+    t_conv, (ref, sabs) = conv_rows(sub, rows, threads)
     pairs = int(((sub >= 0) & (sub < n)).sum())
-    return 2.0 * pairs * layer.Ci * layer.Co, t_map + t_conv, len(rows)
+    res = (2.0 * pairs * layer.Ci * layer.Co, t_map + t_conv, len(rows))
+    return res + ((rows, ref, sabs),) if keep else res
+
+
+def err_over_s(torch, out, rows, ref, sabs):
+    """max over the listed rows of |gpu - exact| / sum|terms| (the quantity
+    the acceptance tolerance bounds)."""
+    got = out[torch.from_numpy(rows).to(out.device)].float().cpu().numpy().astype(np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(sabs > 0, np.abs(got - ref) / sabs, np.where(got == ref, 0.0, np.inf))
+    return float(r.max()) if r.size else 0.0
+
+
+def sampled_rows(n, count, seed):
+    """First and last 160 rows plus ``count`` seeded rows, sorted, distinct."""
+    import workloads as W
+    rnd = (W.draws_u64(seed, 3, 0, count) % np.uint64(max(n, 1))).astype(np.int64)
+    return np.unique(np.concatenate([np.arange(min(n, 160)), np.arange(max(0, n - 160), n), rnd]))
+
+
+# Every workload of the benchmark suite other than the headline one: the
+# per-config lines of the bench record.
+PER_CONFIG = (("tiny", 0), ("small", 0), ("medium", 0), ("channel", 0), ("channel", 1))
+
+
+def fp32_alu_tflops(torch, dev, sm_mhz):
+    """CUDA-core fp32 peak: SMs x 128 fp32 lanes x 2 FLOP (FMA) x SM clock."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def per_config_lines(torch, sv, dev, bf16_peak, hbm_peak, sm_max_mhz, reps=10, check_rows=2048,
+                     materialized_on="medium"):
+    """Build + conv time, throughput, roofline fraction and parity (max
+    |gpu - exact| / sum|terms| on sampled rows against the oracle's own map
+    and loop nest) for each workload of PER_CONFIG.  L2 is flushed before
+    every timed launch (a 256 MB write), since the small workloads fit in
+    it.  Times are CUDA events on the launching stream, averaged over reps.
+    Returns (lines, the materialising comparison on ``materialized_on``)."""
+    import oracle
+    import workloads as W
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    alu_peak = fp32_alu_tflops(torch, dev, sm_max_mhz)
+    lines = {}
+    mat = None
+    wl = None
+    for name, li in PER_CONFIG:
+        if wl is None or wl.name != name:
+            wl = None
+            wl = W.make(name)
+        layer = wl.layers[li]
+        n, k, ci, co, dt = wl.N, wl.K, layer.Ci, layer.Co, layer.dtype
+        coords = torch.from_numpy(wl.coords).to(dev)
+        feats = to_device(torch, layer.feats, dt, dev)
+        w = to_device(torch, layer.w, dt, dev)
+        bias = to_device(torch, layer.bias, dt, dev)
+        nmap = torch.empty((k, n), dtype=torch.int32, device=dev)
+        out = torch.empty((n, co), dtype=feats.dtype, device=dev)
+        ws = torch.empty(sv.workspace_size(n), dtype=torch.uint8, device=dev)
+        tf = "tf32" if dt == "tf32" else None
+        for _ in range(3):
+            sv.build_nmap(coords, workspace=ws, out=nmap)
+            sv.submconv3d(feats, nmap, w, bias, out=out, dtype=tf)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+        for e in ev:
+            flush.zero_()
+            e[0].record(stream)
+            sv.build_nmap(coords, workspace=ws, out=nmap)
+            e[1].record(stream)
+            flush.zero_()
+            e[2].record(stream)
+            sv.submconv3d(feats, nmap, w, bias, out=out, dtype=tf)
+            e[3].record(stream)
+        torch.cuda.synchronize(dev)
+        sv.device_status()
+        build_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / reps
+        conv_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / reps
+        pairs = sv.count_valid_pairs(nmap)
+        flops = 2.0 * pairs * ci * co
+        tflops = flops / (conv_ms * 1e-3) / 1e12
+        elem = 2 if dt == "bf16" else 4
+        comp = n * ci * elem + n * co * elem + 4 * k * n + k * ci * co * elem + co * elem
+        if dt == "bf16":
+            bound, peak, peak_src = "tensor", bf16_peak, "measured bf16 dense (burst)"
+        else:
+            bound, peak, peak_src = "alu", alu_peak, "fp32 CUDA-core peak (SMs x 128 lanes x 2 x max SM clock)"
+        t_roof = max(flops / (peak * 1e12), comp / (hbm_peak * 1e9)) * 1e3
+        rows = sampled_rows(n, check_rows, 40 + li)
+        sub = oracle.nmap_rows(wl.coords, wl.offsets, rows)
+        full = np.full((k, n), n, dtype=np.int32)
+        full[:, rows] = sub
+        ref, sabs = oracle.conv(layer.feats, full, layer.w, layer.bias, dt, rows=rows,
+                                threads=oracle.host_threads())
+        key = name if len(wl.layers) == 1 else f"{name}_layer{'AB'[li]}"
+        lines[key] = {
+            "N": n, "K": k, "Ci": ci, "Co": co, "dtype": dt, "valid_pairs": pairs,
+            "conv_ms": conv_ms, "tflops": tflops, "voxels_per_s": n / (conv_ms * 1e-3),
+            "bound": bound, "peak": peak, "peak_source": peak_src, "frac": tflops / peak,
+            "t_roof_ms": t_roof, "frac_of_roofline": t_roof / conv_ms, "build_ms": build_ms,
+            "build_voxels_per_s": n / (build_ms * 1e-3),
+            "max_err_over_S": err_over_s(torch, out, rows, ref, sabs),
+            "tol": oracle.TOL[dt], "rows_checked": int(len(rows)),
+            "l2": "flushed before every timed launch"}
+        if name == materialized_on and dt == "bf16":
+            mat = materialized_baseline(torch, sv, feats, nmap, w, bias, out)
+            mat["workload"] = f"{name}: N={n}, {ci}->{co} {dt}"
+        del coords, feats, w, bias, nmap, out, ws
+    del flush
+    return lines, mat
 
 
 # --------------------------------------------------------------------- arms
@@ -367,6 +484,43 @@ def workload_config(wl, layer, pairs=None):
     if pairs is not None:
         cfg["valid_pairs"] = pairs
     return cfg
+
+
+def copy_bandwidths(torch, dev, d_in, h_in, d_out, h_out, streams, reps=3):
+    """Pinned host<->device copy rates (GB/s) measured with CUDA events:
+    host->device alone (h_in -> d_in), device->host alone (d_out -> h_out),
+    and both at once on two streams."""
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = d_out.numel() * d_out.element_size()
+    main = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        for st in streams:
+            st.wait_event(e0)
+        for _ in range(reps):
+            fn()
+        for st in streams:
+            main.wait_stream(st)
+        e1.record(main)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+
+    def up():
+        with torch.cuda.stream(streams[0]):
+            d_in.copy_(h_in, non_blocking=True)
+
+    def down():
+        with torch.cuda.stream(streams[1]):
+            h_out.copy_(d_out, non_blocking=True)
+
+    t_up = timed(up)
+    t_down = timed(down)
+    t_both = timed(lambda: (up(), down()))
+    return {"h2d_gbs": h2d / t_up / 1e6, "d2h_gbs": d2h / t_down / 1e6,
+            "both_gbs": (h2d + d2h) / t_both / 1e6}
 
 
 def run_ours(args):
@@ -433,6 +587,26 @@ def run_ours(args):
         pg.barrier()
     sv.device_status()
     ms_per_step = total_ms / args.steps
+
+    # ---- device memory the step uses beyond its inputs (coords, feats, w,
+    # bias) and outputs (nmap, out): the map build's workspace, which the
+    # caller allocates once, plus anything allocated during a step (the
+    # library allocates nothing; the conv needs no workspace)
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    sv.build_nmap(coords, workspace=ws, out=nmap)
+    torch.cuda.synchronize(dev)
+    during_build = torch.cuda.max_memory_allocated(dev) - base
+    torch.cuda.reset_peak_memory_stats(dev)
+    sv.submconv3d(feats, nmap, w, bias, out=out, dtype=tf)
+    torch.cuda.synchronize(dev)
+    during_conv = torch.cuda.max_memory_allocated(dev) - base
+    ws_bytes = ws.numel() * ws.element_size()
+    peak_extra = {"bytes": ws_bytes + max(during_build, during_conv), "build_workspace_bytes": ws_bytes,
+                  "allocated_during_build": during_build, "allocated_during_conv": during_conv,
+                  "gather_materialised_bytes": 0,
+                  "note": "nmap (4*K*N bytes) is the build's output and the conv's input, not counted"}
 
     # ---- end to end through the public API with pinned host buffers
     e2e = None
@@ -513,34 +687,19 @@ def run_ours(args):
         h2d = sum(t.numel() * t.element_size() for t in (h_coords, h_feats, h_w, h_bias))
         d2h = slots[0]["h_out"].numel() * slots[0]["h_out"].element_size()
 
-        # The same loop with the kernels left out (copies only), after the
-        # timed region: it tells the copies' own floor in this process from
-        # how well the loop overlaps them.
-        def copy_step(i):
-            sl, st = slots[i % nslots], streams[i % nslots]
-            with torch.cuda.stream(st):
-                sl["coords"].copy_(h_coords, non_blocking=True)
-                sl["feats"].copy_(h_feats, non_blocking=True)
-                sl["w"].copy_(h_w, non_blocking=True)
-                sl["bias"].copy_(h_bias, non_blocking=True)
-                sl["h_out"].copy_(sl["out"], non_blocking=True)
-
-        reps = max(nslots, min(args.steps, 6))
-        torch.cuda.synchronize(dev)
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        c0.record(main)
-        for st in streams:
-            st.wait_event(c0)
-        for i in range(reps):
-            copy_step(i)
-        for st in streams:
-            main.wait_stream(st)
-        c1.record(main)
-        torch.cuda.synchronize(dev)
+        # The copies' own floor on this machine: each direction alone and both at
+        # once, one large copy per stream, then the step's bytes at those
+        # rates.  No schedule of the loop above can move its bytes faster.
+        bw = copy_bandwidths(torch, dev, slots[0]["feats"], h_feats, slots[0]["out"], slots[0]["h_out"],
+                             streams[:2])
+        floor_ms = max(h2d / bw["h2d_gbs"], d2h / bw["d2h_gbs"], (h2d + d2h) / bw["both_gbs"]) / 1e6
         e2e = {"value": job_tflops(world, flops, e2e_ms / args.steps), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms / args.steps, "steps_in_flight": nslots, "host_node": host_node,
-               "copies_only_ms_per_step": c0.elapsed_time(c1) / reps}
+               "achieved_copy_gbs": (h2d + d2h) / (e2e_ms / args.steps) / 1e6,
+               "copy_floor": dict(bw, floor_ms_per_step=floor_ms)}
+        del e2e_step, slots, streams, h_coords, h_feats, h_w, h_bias
+        torch.cuda.empty_cache()
 
     if rank != 0:
         if pg is not None:
@@ -564,14 +723,28 @@ def run_ours(args):
                 "frac_of_roofline": t_roof_ms / conv_avg_ms}
 
     cpu = None
+    import oracle
+    threads = oracle.host_threads()
     if not args.no_cpu_baseline and world == 1:
-        import oracle
-        threads = oracle.host_threads()
-        f, s, r = oracle_step(wl, layer, args.cpu_seconds, threads, seed=99)
+        f, s, r, (rows, ref, sabs) = oracle_step(wl, layer, args.cpu_seconds, threads, seed=99, keep=True)
         cpu = {"value": f / s / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{r} seeded output rows of the same workload: neighbour map by sort + "
                          f"binary search over all N voxels, fp64 conv loop nest over the sample; "
                          f"{s:.1f} s"}
+    else:
+        _, _, _, (rows, ref, sabs) = oracle_step(wl, layer, 1.0, threads, seed=99, keep=True)
+    # parity of this run's output on the oracle's sampled rows (its own map rows)
+    parity = {"max_err_over_S": err_over_s(torch, out, rows, ref, sabs), "tol": oracle.TOL[dtype],
+              "rows_checked": int(len(rows))}
+
+    per_config, mat_medium = None, None
+    if not args.no_per_config:
+        del coords, feats, w, bias, nmap, ws
+        torch.cuda.empty_cache()
+        per_config, mat_medium = per_config_lines(torch, sv, dev, bf16_peak, hbm_peak,
+                                                  clocks.get("sm_max_mhz") or 2070.0)
+    if materialized is None:
+        materialized = mat_medium
 
     line = {
         "metric": METRIC, "value": job_tflops(world, flops, ms_per_step), "unit": UNIT,
@@ -583,6 +756,10 @@ def run_ours(args):
         "conv_tflops": achieved,
         "build_ms": ms_per_step - conv_avg_ms,
         "roofline": roofline,
+        "max_err_over_S": parity["max_err_over_S"],
+        "parity": parity,
+        "peak_extra_bytes": peak_extra["bytes"],
+        "peak_extra": peak_extra,
         "cpu_baseline": cpu,
         "e2e": e2e,
         # per step: the map build's six kernels (flag reset, range/order
@@ -591,6 +768,7 @@ def run_ours(args):
         "gpu_launches": (6 + (co + 255) // 256) * args.steps,
         "clocks": clocks,
         "generation_s": gen_s,
+        **({"per_config": per_config} if per_config is not None else {}),
         **({"materialized": materialized} if materialized is not None else {}),
     }
     print(json.dumps(line), flush=True)

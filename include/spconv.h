@@ -147,11 +147,11 @@ spconv_status spconv_build_nmap_async(const int32_t* coords_dev, int64_t N,
  * and nmap are still the caller's.  Limits and behaviour:
  *  - N must not exceed SPCONV_NOALLOC_MAX_VOXELS; larger N returns
  *    SPCONV_ERR_UNSUPPORTED before any device work.
- *  - The array (32 MiB + 256 B) is a static device variable: every GPU that
- *    loads this library holds it until the process exits.
- *  - The first call on a device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *  - The array is a static device variable of 32 MiB + 256 B: it takes that
+ *    much on each device where this library's module is loaded, until the
+ *    process exits.
+ *  - Each call looks up the array's device address on the current device
+ *    (the runtime's symbol lookup; nothing is cached between calls).
  *  - Every call on a device shares the one array and clears what it needs
  *    (table keys and flags) at its start; the previous call's contents are
  *    otherwise left in place.  Calls whose work overlaps on the GPU (other

@@ -95,6 +95,12 @@ def _load():
             lib.oracle_wgrad.restype = ctypes.c_int
             lib.oracle_count_valid_pairs.argtypes = [vp, i64, i32]
             lib.oracle_count_valid_pairs.restype = ctypes.c_int64
+            lib.oracle_table_new.argtypes = [vp, i64, ctypes.POINTER(ctypes.c_int)]
+            lib.oracle_table_new.restype = vp
+            lib.oracle_table_query.argtypes = [vp, vp, i64, vp, i32, i64, i64, vp]
+            lib.oracle_table_query.restype = ctypes.c_int
+            lib.oracle_table_free.argtypes = [vp]
+            lib.oracle_table_free.restype = None
             _lib = lib
     return _lib
 
@@ -103,16 +109,41 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-def build_nmap(coords: np.ndarray, offsets: np.ndarray) -> np.ndarray:
-    """(K, N) int32 neighbour map; entry N marks a missing neighbour."""
+def build_nmap(coords: np.ndarray, offsets: np.ndarray, threads: int = 1) -> np.ndarray:
+    """(K, N) int32 neighbour map; entry N marks a missing neighbour.
+
+    ``threads`` > 1 sorts the coordinates once and splits the voxels over
+    that many threads; every entry is the same binary search either way."""
     lib = _load()
     coords = np.ascontiguousarray(coords, dtype=np.int32).reshape(-1, 3)
     offsets = np.ascontiguousarray(offsets, dtype=np.int32).reshape(-1, 3)
     N, K = coords.shape[0], offsets.shape[0]
     nmap = np.empty((K, N), dtype=np.int32)
-    rc = lib.oracle_build_nmap(_ptr(coords), N, _ptr(offsets), K, _ptr(nmap))
-    if rc != OK:
-        raise OracleError(rc, "build_nmap")
+    threads = max(1, min(int(threads), N))
+    if threads == 1 or N == 0:
+        rc = lib.oracle_build_nmap(_ptr(coords), N, _ptr(offsets), K, _ptr(nmap))
+        if rc != OK:
+            raise OracleError(rc, "build_nmap")
+        return nmap
+    if K < 1:
+        raise OracleError(ERR_INVALID_ARG, "build_nmap")
+    status = ctypes.c_int(0)
+    table = lib.oracle_table_new(_ptr(coords), N, ctypes.byref(status))
+    if not table:
+        raise OracleError(status.value, "build_nmap")
+    try:
+        bounds = np.linspace(0, N, threads + 1).astype(np.int64)
+
+        def run(i):
+            rc = lib.oracle_table_query(table, _ptr(coords), N, _ptr(offsets), K,
+                                        int(bounds[i]), int(bounds[i + 1]), _ptr(nmap))
+            if rc != OK:
+                raise OracleError(rc, "build_nmap")
+
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(run, range(threads)))
+    finally:
+        lib.oracle_table_free(table)
     return nmap
 
 

@@ -168,6 +168,39 @@ int oracle_nmap_rows(const int32_t* coords, int64_t N, const int32_t* offsets, i
     return ORACLE_OK;
 }
 
+/*
+ * The same map in pieces, for large inputs split over host threads: the
+ * sorted table is built once (oracle_table_new) and each caller fills the
+ * columns n0 <= n < n1 of the full (K, N) map with the same binary search
+ * (oracle_table_query); oracle_table_free releases the table.
+ */
+void* oracle_table_new(const int32_t* coords, int64_t N, int* status)
+{
+    if (status == NULL) return NULL;
+    if (N < 1 || coords == NULL || N >= INT32_MAX) {
+        *status = ORACLE_ERR_INVALID_ARG;
+        return NULL;
+    }
+    *status = oracle_check_coords(coords, N);
+    if (*status != ORACLE_OK) return NULL;
+    return oracle_sorted_table(coords, N, status);
+}
+
+int oracle_table_query(const void* table, const int32_t* coords, int64_t N, const int32_t* offsets,
+                       int32_t K, int64_t n0, int64_t n1, int32_t* nmap)
+{
+    if (table == NULL || coords == NULL || offsets == NULL || nmap == NULL || K < 1 || n0 < 0 ||
+        n1 > N || n0 > n1)
+        return ORACLE_ERR_INVALID_ARG;
+    for (int64_t n = n0; n < n1; ++n)
+        for (int32_t k = 0; k < K; ++k)
+            nmap[(size_t)k * (size_t)N + (size_t)n] =
+                oracle_neighbour((const oracle_entry*)table, coords, N, offsets, n, k);
+    return ORACLE_OK;
+}
+
+void oracle_table_free(void* table) { free(table); }
+
 /* Exact widening of one stored value to double. */
 static double oracle_widen(const void* base, int32_t dtype, size_t i)
 {

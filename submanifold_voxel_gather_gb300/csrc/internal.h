@@ -33,7 +33,7 @@ spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOff
                                 int32_t k, int32_t* nmap, void* workspace, cudaStream_t stream,
                                 int32_t* status_dev = nullptr);
 // Device address of the allocation-free variant's static scratch on the
-// current device (looked up once per device).
+// current device (looked up on every call).
 spconv_status noalloc_scratch(void** scratch);
 spconv_status launch_count_valid_pairs(const int32_t* nmap, int64_t n, int32_t k, int64_t* count,
                                        cudaStream_t stream);

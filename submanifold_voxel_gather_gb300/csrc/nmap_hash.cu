@@ -44,7 +44,6 @@
 
 #include <climits>
 
-#include <mutex>
 #include <string>
 
 #include "internal.h"
@@ -663,8 +662,8 @@ spconv_status launch_count_valid_pairs(const int32_t* nmap, int64_t n, int32_t k
 // a host framework that owns every device allocation, or a fixed-budget
 // deployment that forbids allocations after start-up).  For them the hash
 // table lives in one file-scope device array of fixed size instead of a
-// caller-provided workspace.  Every GPU that loads this library holds the
-// array (32 MiB + 256 B) until the process exits.
+// caller-provided workspace.  The array takes 32 MiB + 256 B on each device
+// where this library's module is loaded, until the process exits.
 namespace {
 
 constexpr size_t kNoAllocBytes = kFlagBytes + 2 * static_cast<size_t>(SPCONV_NOALLOC_MAX_VOXELS) * 16;
@@ -674,24 +673,16 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 }  // namespace
 
 spconv_status noalloc_scratch(void** scratch) {
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static void* addr[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(SPCONV_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return fail(SPCONV_ERR_UNSUPPORTED, "device ordinal out of range");
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    // Host code only has a stand-in for the array's name; its device address
-    // comes from the runtime, once per device, with that device current.
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess)
-      return fail(SPCONV_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
-    addr[dev] = p;
-  }
-  *scratch = addr[dev];
+  // Host code only has a stand-in for the array's name; its device address
+  // comes from the runtime, for the current device.  It is looked up on
+  // every call (cheap next to the build, which waits for its stream): a
+  // cached address would go stale if the device's context were reset and
+  // the module loaded again elsewhere.
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess)
+    return fail(SPCONV_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+  *scratch = p;
   return SPCONV_OK;
 }
 

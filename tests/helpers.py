@@ -45,3 +45,18 @@ def sample_rows(n, count, seed):
     tail = np.arange(max(0, n - 160), n)
     rnd = (W.draws_u64(seed, W.SID_TEST + 7, 0, count) % np.uint64(max(n, 1))).astype(np.int64)
     return np.unique(np.concatenate([head, tail, rnd])).astype(np.int64)
+
+
+_ORACLE_MAPS = {}
+
+
+def oracle_full_map(name):
+    """(coords, the oracle's whole (K, N) map) of a named workload, computed
+    once per test session (threaded: one sort, voxels split over the host's
+    threads)."""
+    import oracle
+    if name not in _ORACLE_MAPS:
+        coords = W.coords_only(name)
+        _ORACLE_MAPS[name] = (coords, oracle.build_nmap(coords, W.offsets_3x3x3(),
+                                                        threads=oracle.host_threads()))
+    return _ORACLE_MAPS[name]

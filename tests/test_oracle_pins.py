@@ -343,6 +343,29 @@ def test_planted_mistakes_fail_a_pin(oracle_mod):
     assert not np.array_equal(out, np.asarray(ex["out"], np.float64))
 
 
+@pytest.mark.parametrize("threads", [2, 3, 7])
+def test_threaded_nmap_equals_brute_force(oracle_mod, threads):
+    """The threaded build (one sort, voxels split over threads) gives the
+    brute-force map, shuffled input and 125 offsets included, and raises the
+    same errors."""
+    coords = W.random_occupancy(9, 0.45, 13)
+    coords = coords[W.permutation(len(coords), 13)]
+    for offs in (W.offsets_3x3x3(), W.offsets_cube(2)):
+        np.testing.assert_array_equal(oracle_mod.build_nmap(coords, offs, threads=threads),
+                                      brute_force_nmap(coords, offs))
+    tiny = coords[:threads - 1]  # fewer voxels than threads
+    np.testing.assert_array_equal(oracle_mod.build_nmap(tiny, W.offsets_3x3x3(), threads=threads),
+                                  brute_force_nmap(tiny, W.offsets_3x3x3()))
+    with pytest.raises(oracle_mod.OracleError) as e:
+        oracle_mod.build_nmap(np.array([[1, 2, 3], [4, 5, 6], [1, 2, 3]], np.int32), W.offsets_3x3x3(),
+                              threads=threads)
+    assert e.value.code == oracle_mod.ERR_DUPLICATE_COORD
+    with pytest.raises(oracle_mod.OracleError) as e:
+        oracle_mod.build_nmap(np.array([[1, 2, 3], [1, 1 << 20, 3]], np.int32), W.offsets_3x3x3(),
+                              threads=threads)
+    assert e.value.code == oracle_mod.ERR_INVALID_ARG
+
+
 def test_nmap_rows_equals_full_map_columns(oracle_mod):
     coords = W.random_occupancy(9, 0.5, 71)
     offs = W.offsets_3x3x3()

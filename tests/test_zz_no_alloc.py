@@ -5,7 +5,9 @@ table in a fixed device array of the library instead of a caller workspace.
 
 Called through the C ABI and compared, bit for bit, with the map that the
 workspace entry point spconv_build_nmap builds for the same input, on two
-calls in a row (the second call reuses the array the first one filled).
+calls in a row (the second call reuses the array the first one filled), and
+at exactly SPCONV_NOALLOC_MAX_VOXELS voxels (the one size whose table fills
+the whole array) also with the oracle's map.
 This file is collected last so that a run stopping at the first failure has
 already run every other test.
 """
@@ -63,6 +65,25 @@ def test_noalloc_equals_workspace_build_on_two_calls_in_a_row(env):
     out_b, ref_b = _noalloc_map(env, b, W.offsets_cube(2))
     assert torch.equal(out_b, ref_b)
     assert int((out_b == len(b)).sum()) > 0 and int((out_b < len(b)).sum()) > 0
+
+
+def test_noalloc_at_its_maximum_size(env, oracle_mod):
+    """N = SPCONV_NOALLOC_MAX_VOXELS (a 128 x 128 x 64 block, shuffled so the
+    voxel hash is used): its 2^21 slots fill the whole array.  Equal to the
+    workspace build and to the oracle's map; then a small call right after
+    still gives the right map."""
+    torch = env[0]
+    g = np.stack(np.meshgrid(np.arange(128), np.arange(128), np.arange(64), indexing="ij"), -1)
+    coords = (g.reshape(-1, 3) + np.array([7, 900, 3])).astype(np.int32)
+    assert len(coords) == MAX_VOXELS
+    coords = coords[W.permutation(len(coords), 21)]
+    offs = W.offsets_3x3x3()
+    out, ref = _noalloc_map(env, coords, offs)
+    assert torch.equal(out, ref)
+    np.testing.assert_array_equal(out.cpu().numpy(),
+                                  oracle_mod.build_nmap(coords, offs, threads=oracle_mod.host_threads()))
+    out_s, ref_s = _noalloc_map(env, W.coords_only("tiny"), offs)
+    assert torch.equal(out_s, ref_s)
 
 
 def test_noalloc_rejects_sizes_above_its_maximum(env):
