@@ -59,8 +59,9 @@ typedef enum spconv_status {
 
 typedef enum spconv_dtype {
     SPCONV_F32 = 0,   /* fp32 storage, fp32 products and fp32 accumulation (CUDA cores) */
-    SPCONV_TF32 = 1,  /* fp32 storage, results within the tf32 tolerance (4e-3 * sum|terms|);
-                         currently computed with fp32 products on CUDA cores */
+    SPCONV_TF32 = 1,  /* fp32 storage, tf32 tensor-core products (the MMA reads each fp32
+                         operand's sign, exponent and top 10 mantissa bits), fp32
+                         accumulation, fp32 output; within 4e-3 * sum|terms| */
     SPCONV_BF16 = 2   /* bf16 storage, bf16 tensor-core products, fp32 accumulation, bf16 output */
 } spconv_dtype;
 
@@ -253,8 +254,8 @@ spconv_status spconv_submconv3d_ex(const void* feats_dev, const int32_t* nmap_de
  *  w_dev       (K, Ci, Co) storage type: the forward weights.
  *  dfeats_dev  (N, Ci) storage type, written (must not overlap the inputs).
  *  N, K, Ci, Co, dtype, stream   the forward layer's sizes; requirements,
- *              tolerance and asynchrony as for spconv_submconv3d (bf16 on
- *              the tensor cores, f32 / tf32 exact fp32).
+ *              tolerance and asynchrony as for spconv_submconv3d (bf16 and
+ *              tf32 on the tensor cores, f32 exact fp32 on CUDA cores).
  */
 spconv_status spconv_submconv3d_dgrad(const void* dout_dev, const int32_t* nmap_dev,
                                       const void* w_dev, void* dfeats_dev, int64_t N, int32_t K,
@@ -332,8 +333,8 @@ spconv_status spconv_tile_order(const int32_t* nmap_dev, int64_t N, int32_t K, i
  *             once.
  *
  * Other arguments, layouts and errors as spconv_submconv3d.  For SPCONV_F32
- * and SPCONV_TF32 the order does not change how the exact fp32 kernel
- * works, and it is ignored.
+ * the order does not change how the exact fp32 kernel works, and it is
+ * ignored.
  */
 spconv_status spconv_submconv3d_ordered(const void* feats_dev, const int32_t* nmap_dev,
                                         const int32_t* order_dev, const void* w_dev,

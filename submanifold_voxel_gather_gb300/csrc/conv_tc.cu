@@ -83,11 +83,11 @@ constexpr int kMaxSmem = 232448;       // 227 KB opt-in limit per block
 enum : uint32_t { kMetaFirst = 1u, kMetaEnd = 2u };
 
 struct TcParams {
-  const __nv_bfloat16* feats;
+  const void* feats;     // bf16, or fp32 for the tf32 instantiation (as are bias, residual, out)
   const int32_t* nmap;
-  const __nv_bfloat16* bias;
-  const __nv_bfloat16* residual;  // (N, co) or null; may alias out
-  __nv_bfloat16* out;
+  const void* bias;
+  const void* residual;  // (N, co) or null; may alias out
+  void* out;
   const int32_t* order;  // tile slot -> voxel (a permutation of 0..N-1), or null for identity
   int64_t n;
   int64_t num_tiles;
@@ -110,6 +110,8 @@ struct TcParams {
   uint32_t off_bias;
   uint32_t off_meta;
   uint32_t off_bars;
+  uint32_t off_raw;   // tf32 forward: ring of two channel-major weight chunks (TMA), transposed by warp 3
+  uint32_t raw_bytes; // bytes of one raw slot (M blocks x 16 KB)
 };
 
 // Named barrier for the four epilogue warps only.
@@ -149,19 +151,77 @@ __device__ __forceinline__ bool issue_row(uint32_t flag, int kk, int k_count, bo
   return flag != 0u || (kk == k_count - 1 && !issued);
 }
 
+// One MMA of the stage's kind: bf16 products (kind::f16, K = 16) or tf32
+// products of fp32 storage (kind::tf32, K = 8); 32 bytes of K either way.
+template <bool kTf32>
+__device__ __forceinline__ void umma_kind(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  if constexpr (kTf32)
+    umma_tf32(d_tmem, a_desc, b_desc, idesc, accumulate);
+  else
+    umma_f16(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
+
+// tf32 forward: the weight chunk of one stage arrives channel-major (TMA,
+// 128-byte swizzle: per 32-channel box, row ci of 128 bytes holds output
+// channels co, 16-byte piece j at j ^ (ci & 7)), but kind::tf32 reads its A
+// operand K-major only (row co of 128 bytes holding 32 input channels,
+// 16-byte piece q = ci / 4 at q ^ (co & 7)).  One warp transposes it in 4 x 4
+// blocks: four 16-byte loads (ci rows 4a..4a+3, channels 4b..4b+3) and four
+// 16-byte stores (co rows 4b..4b+3, channels 4a..4a+3).  Lane i of lane group
+// g takes block a = i, j = (i + d) mod 8 of box beta, with (beta, d) from the
+// group and the iteration: the eight lanes of each 16-byte phase then touch
+// eight distinct bank groups on both sides.
+template <int MBLK>
+__device__ __forceinline__ void transpose_weight_chunk(const uint8_t* raw, uint8_t* a_tile, uint32_t lane) {
+  const uint32_t i = lane & 7u, g = lane >> 3;
+#pragma unroll
+  for (uint32_t t = 0; t < 8u * MBLK; ++t) {
+    const uint32_t c = t * 4u + g;             // (box, shift) pair, 0 .. 32 MBLK - 1
+    const uint32_t beta = c >> 3, d = c & 7u;  // box of 32 output channels, shift
+    const uint32_t a = i, j = (i + d) & 7u;
+    const uint32_t b = beta * 8u + j;          // 4-channel group of the output channel
+    float4 v[4];
+#pragma unroll
+    for (uint32_t r = 0; r < 4; ++r) {
+      const uint32_t ci = 4u * a + r;
+      v[r] = *reinterpret_cast<const float4*>(raw + beta * 4096u + ci * 128u + ((j ^ (ci & 7u)) << 4));
+    }
+    const float x[4][4] = {{v[0].x, v[1].x, v[2].x, v[3].x},
+                           {v[0].y, v[1].y, v[2].y, v[3].y},
+                           {v[0].z, v[1].z, v[2].z, v[3].z},
+                           {v[0].w, v[1].w, v[2].w, v[3].w}};
+#pragma unroll
+    for (uint32_t cc = 0; cc < 4; ++cc) {
+      const uint32_t co = 4u * b + cc;         // row of the K-major tile (M blocks stacked)
+      *reinterpret_cast<float4*>(a_tile + co * 128u + ((a ^ (co & 7u)) << 4)) =
+          make_float4(x[cc][0], x[cc][1], x[cc][2], x[cc][3]);
+    }
+  }
+}
+
 // kHoist: the per-row source index and byte count are computed once per
 // offset instead of once per chunk (used when an offset has two or more
 // 128-byte chunks; with one chunk the in-loop form is measured faster).
 // kDgrad: input gradient; the weights of offset k are w[K-1-k] transposed,
 // read from the forward layout as a K-major operand.
 // kSplit: two-chunk stages with one full / empty barrier pair per chunk.
-template <int TILE_N, int MBLK, bool kHoist, bool kDgrad, bool kSplit>
+// kTf32: fp32 storage, tf32 products (kind::tf32), fp32 output; a 128-byte
+// chunk is 32 channels, one chunk per stage; the forward's weights are
+// transposed in shared memory by warp 3 (kind::tf32 reads K-major A only).
+template <int TILE_N, int MBLK, bool kHoist, bool kDgrad, bool kSplit, bool kTf32>
 __global__ void __launch_bounds__(kThreads, 1)
     submconv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const TcParams p) {
   constexpr int kRowsPerWarp = TILE_N / 4;       // gathered rows per producer warp
   constexpr int kIdxPerLane = kRowsPerWarp / 4;  // 4 rows per warp instruction
   static_assert(kRowsPerWarp == 64, "ring layout: 64 rows per gather producer warp");
   static_assert(!kSplit || (MBLK == 1 && kHoist), "per-chunk barriers need two-chunk stages");
+  static_assert(!(kSplit && kTf32), "tf32 stages hold one chunk");
+  constexpr int kChunkE = kTf32 ? 32 : kChunk;           // elements per 128-byte row
+  constexpr int kKPerMmaE = kTf32 ? 8 : kKPerMma;        // K per MMA instruction
+  constexpr uint32_t kEsz = kTf32 ? 4u : 2u;             // element bytes
+  constexpr bool kTranspose = kTf32 && !kDgrad;          // weights transposed by warp 3
+  constexpr bool kKMajorA = kDgrad || kTf32;             // A operand K-major
   constexpr int kLoaderPerLane = TILE_N / 32;
   constexpr int kOutStride = MBLK * 128;         // staged output row, elements
   // Two accumulator buffers (the epilogue of one tile overlaps the next) when
@@ -192,9 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tmem_full = ring_empty + kRing;
   uint64_t* tmem_empty = tmem_full + 2;
   uint64_t* drain = tmem_empty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* raw_full = drain + 1;    // tf32 forward: raw weight slots (two)
+  uint64_t* raw_empty = raw_full + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(raw_empty + 2);
   uint32_t* consumed_holder = tmem_holder + 1;
   uint32_t* fills_holder = tmem_holder + 2;
+  uint32_t* raw_consumed_holder = tmem_holder + 3;
+  uint32_t* raw_meta = tmem_holder + 4;  // two words: the stage metadata of each raw slot
 
   if (warp == 0 && lane == 0) {
     for (uint32_t s = 0; s < S * parts; ++s) {
@@ -210,8 +274,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&tmem_empty[i]), 4);
     }
     mbar_init(smem_addr(drain), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&raw_full[i]), 1);
+      mbar_init(smem_addr(&raw_empty[i]), 1);
+    }
     *consumed_holder = 0;
     *fills_holder = 0;
+    *raw_consumed_holder = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_w);
   }
@@ -220,8 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == 3) {
-    for (int j = lane; j < MBLK * 128; j += 32)
-      bias_s[j] = (p.bias != nullptr && j < p.co_count) ? __bfloat162float(p.bias[p.co_base + j]) : 0.0f;
+    for (int j = lane; j < MBLK * 128; j += 32) {
+      float b = 0.0f;
+      if (p.bias != nullptr && j < p.co_count) {
+        if constexpr (kTf32)
+          b = static_cast<const float*>(p.bias)[p.co_base + j];
+        else
+          b = __bfloat162float(static_cast<const __nv_bfloat16*>(p.bias)[p.co_base + j]);
+      }
+      bias_s[j] = b;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -284,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sub_row = static_cast<int>(lane >> 3);
     const int chunk16 = static_cast<int>(lane & 7);
     const char* feats = reinterpret_cast<const char*>(p.feats);
-    const uint32_t row_bytes = static_cast<uint32_t>(p.ci) * 2u;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.ci) * kEsz;
     // Row-independent part of the destination: this lane's row group and its
     // swizzled 16-byte slot (rows 4 j + sub_row alternate between two
     // swizzle phases).  The producer loop is issue-bound, so its per-row
@@ -384,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 0) {
     // ------------------------------------------------------ weight producer
     uint32_t stage = 0, st_phase = 0, e = 0, ephase = 0, fills = 0;
+    uint32_t rslot = 0, rphase = 0;  // tf32 forward: raw weight slot ring
     bool ok = true;
     for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
       bool issued = false;
@@ -400,6 +478,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           ephase ^= 1;
         }
         if (!go) continue;
+        if constexpr (kTranspose) {
+          // tf32 forward: each chunk's weights go to a raw slot, channel-major
+          // (four 32 x 32 boxes per M block), with the stage metadata; warp 3
+          // transposes them into the stage.
+          for (int c = 0; c < p.num_chunks && ok; ++c) {
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&raw_empty[rslot]), rphase ^ 1))) {
+              ok = false;
+              break;
+            }
+            const uint32_t rfull = smem_addr(&raw_full[rslot]);
+            if (lane == 0) {
+              const int steps = min(kChunkE, p.ci - c * kChunkE) / kKPerMmaE;
+              raw_meta[rslot] = (static_cast<uint32_t>(steps) << 8) | (issued ? 0u : kMetaFirst);
+              mbar_arrive_expect_tx(rfull, p.raw_bytes);
+            }
+            ++fills;
+            __syncwarp();
+            if (static_cast<int>(lane) < 4 * MBLK) {
+              const int mb = static_cast<int>(lane) >> 2, q = static_cast<int>(lane) & 3;
+              tma_load_3d(smem_addr(smem + p.off_raw) + rslot * p.raw_bytes + mb * kWBlockBytes + q * 4096u,
+                          &tm_w, p.co_base + mb * 128 + q * 32, c * kChunkE, kk, rfull);
+            }
+            issued = true;
+            rslot ^= 1u;
+            if (rslot == 0) rphase ^= 1u;
+          }
+          continue;
+        }
         for (int c = 0; c < p.num_chunks && ok; c += p.cps) {
           for (int sub = 0; sub < p.cps; ++sub) {  // the stage's chunks, one weight block each
             const uint32_t part = kSplit ? stage * 2u + static_cast<uint32_t>(sub) : stage;
@@ -412,7 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (lane == 0) {
                 if (sub == 0) {
                   // MMAs per part
-                  const int steps = (p.cps / static_cast<int>(parts)) * (min(kChunk, p.ci - c * kChunk) / kKPerMma);
+                  const int steps =
+                      (p.cps / static_cast<int>(parts)) * (min(kChunkE, p.ci - c * kChunkE) / kKPerMmaE);
                   meta[stage] = (static_cast<uint32_t>(steps) << 8) | (issued ? 0u : kMetaFirst);
                 }
                 mbar_arrive_expect_tx(fullb, p.w_bytes / parts);
@@ -422,7 +529,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             // With two parts MBLK is 1, so the part's block is `sub`; with one
             // part, the M blocks are side by side.
-            if constexpr (!kDgrad) {
+            if constexpr (kTf32) {
+              // tf32 input gradient: rows of w[K-1-k] (output channel =
+              // forward ci) with 32 of their forward-co entries each, K-major
+              if (static_cast<int>(lane) < MBLK) {
+                const int mb = static_cast<int>(lane);
+                tma_load_3d(smem_addr(smem + stage * p.stage_bytes) + mb * kWBlockBytes, &tm_w,
+                            c * kChunkE, p.co_base + mb * 128, k_count - 1 - kk, fullb);
+              }
+            } else if constexpr (!kDgrad) {
               // forward: w[k] channel-major, two 64-channel boxes per M block
               if (static_cast<int>(lane) < 2 * MBLK) {
                 const int mb = static_cast<int>(lane) >> 1, half = static_cast<int>(lane) & 1;
@@ -445,7 +560,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (ok && __all_sync(0xffffffffu, mbar_wait(smem_addr(&empty[stage * parts]), st_phase ^ 1))) {
+    if constexpr (kTranspose) {
+      // end-of-work marker through the raw ring (no bytes)
+      if (ok && __all_sync(0xffffffffu, mbar_wait(smem_addr(&raw_empty[rslot]), rphase ^ 1))) {
+        if (lane == 0) {
+          raw_meta[rslot] = kMetaEnd;
+          mbar_arrive(smem_addr(&raw_full[rslot]));
+        }
+        ++fills;
+      }
+    } else if (ok && __all_sync(0xffffffffu, mbar_wait(smem_addr(&empty[stage * parts]), st_phase ^ 1))) {
       if (lane == 0) {
         meta[stage] = kMetaEnd;
         mbar_arrive(smem_addr(&full[stage * parts]));
@@ -453,14 +577,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++fills;
     }
     if (lane == 0) *fills_holder = fills;
+  } else if (warp == 3 && kTranspose) {
+    // ------------------------------------------------------ weight transposer (tf32 forward)
+    uint32_t stage = 0, st_phase = 0, rslot = 0, rphase = 0, consumed = 0;
+    const uint8_t* raw_base = smem + p.off_raw;
+    while (true) {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&raw_full[rslot]), rphase))) break;
+      const uint32_t m = raw_meta[rslot];
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&empty[stage]), st_phase ^ 1))) break;
+      if ((m & kMetaEnd) == 0u) {
+        transpose_weight_chunk<MBLK>(raw_base + rslot * p.raw_bytes, smem + stage * p.stage_bytes, lane);
+        // the MMA reads the tile through the async proxy
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      ++consumed;
+      if (lane == 0) {
+        meta[stage] = m;
+        mbar_arrive(smem_addr(&raw_empty[rslot]));
+        mbar_arrive(smem_addr(&full[stage]));
+      }
+      if ((m & kMetaEnd) != 0u) break;
+      rslot ^= 1u;
+      if (rslot == 0) rphase ^= 1u;
+      if (++stage == S) {
+        stage = 0;
+        st_phase ^= 1;
+      }
+    }
+    if (lane == 0) *raw_consumed_holder = consumed;
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
       // Descriptors of stage 0; a stage or K step only moves the start
       // address (the low 14 bits, in 16-byte units), so advancing is one add.
-      // Weights channel-major (forward) or K-major (input gradient).
-      const uint64_t adesc0 = sw128_desc(smem_addr(smem), kDgrad ? 16u : 8192u, 1024u);
-      constexpr uint64_t a_step = kDgrad ? kBStepUnits : kAStepUnits;
+      // Weights channel-major (bf16 forward) or K-major (input gradient, and
+      // the tf32 forward after the transposer).
+      const uint64_t adesc0 = sw128_desc(smem_addr(smem), kKMajorA ? 16u : 8192u, 1024u);
+      constexpr uint64_t a_step = kKMajorA ? kBStepUnits : kAStepUnits;
       const uint64_t bdesc0 = sw128_desc(smem_addr(smem) + p.w_bytes, 16u, 1024u);
       const uint64_t stage_units = p.stage_bytes >> 4;
       const uint32_t idesc = p.idesc;
@@ -498,41 +652,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           // two chunks (MBLK == 1), each its own part: chunk 1's weight
           // block and row block follow those of chunk 0
 #pragma unroll
-          for (int s = 0; s < kChunk / kKPerMma; ++s)
-            umma_f16(d_tmem, ad + s * a_step, bd + s * kBStepUnits, idesc, s > 0 ? 1u : acc0);
+          for (int s = 0; s < kChunkE / kKPerMmaE; ++s)
+            umma_kind<kTf32>(d_tmem, ad + s * a_step, bd + s * kBStepUnits, idesc, s > 0 ? 1u : acc0);
           umma_commit(smem_addr(&empty[stage * 2u]));
           ++consumed;
           if (!mbar_wait(smem_addr(&full[stage * 2u + 1u]), st_phase)) break;
           fence_proxy_async_smem();
           tc_fence_after();
 #pragma unroll
-          for (int s = 0; s < kChunk / kKPerMma; ++s)
-            umma_f16(d_tmem, ad + kWBlockUnits + s * a_step, bd + ((TILE_N * 128u) >> 4) + s * kBStepUnits, idesc,
+          for (int s = 0; s < kChunkE / kKPerMmaE; ++s)
+            umma_kind<kTf32>(d_tmem, ad + kWBlockUnits + s * a_step, bd + ((TILE_N * 128u) >> 4) + s * kBStepUnits, idesc,
                      1u);
           umma_commit(smem_addr(&empty[stage * 2u + 1u]));
           ++consumed;
         } else {
-          if (steps == 2 * kChunk / kKPerMma) {
+          if (steps == 2 * kChunkE / kKPerMmaE) {
             // two chunks in one part (MBLK == 1): chunk 1's weight block and
             // row block follow those of chunk 0
 #pragma unroll
-            for (int s = 0; s < 2 * kChunk / kKPerMma; ++s) {
+            for (int s = 0; s < 2 * kChunkE / kKPerMmaE; ++s) {
               const int sub = s >> 2, ss = s & 3;
-              umma_f16(d_tmem, ad + sub * kWBlockUnits + ss * a_step,
+              umma_kind<kTf32>(d_tmem, ad + sub * kWBlockUnits + ss * a_step,
                        bd + sub * ((TILE_N * 128u) >> 4) + ss * kBStepUnits, idesc, s > 0 ? 1u : acc0);
             }
-          } else if (steps == kChunk / kKPerMma) {
+          } else if (steps == kChunkE / kKPerMmaE) {
 #pragma unroll
-            for (int s = 0; s < kChunk / kKPerMma; ++s)
+            for (int s = 0; s < kChunkE / kKPerMmaE; ++s)
 #pragma unroll
               for (int mb = 0; mb < MBLK; ++mb)
-                umma_f16(d_tmem + mb * TILE_N, ad + mb * kWBlockUnits + s * a_step,
+                umma_kind<kTf32>(d_tmem + mb * TILE_N, ad + mb * kWBlockUnits + s * a_step,
                          bd + s * kBStepUnits, idesc, s > 0 ? 1u : acc0);
           } else {
             for (int s = 0; s < steps; ++s)
 #pragma unroll
               for (int mb = 0; mb < MBLK; ++mb)
-                umma_f16(d_tmem + mb * TILE_N, ad + mb * kWBlockUnits + s * a_step,
+                umma_kind<kTf32>(d_tmem + mb * TILE_N, ad + mb * kWBlockUnits + s * a_step,
                          bd + s * kBStepUnits, idesc, s > 0 ? 1u : acc0);
           }
           umma_commit(smem_addr(&empty[stage]));
@@ -562,6 +716,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (row, piece) pairs, residual first, so the residual may be the output.
     // The next chunk's pieces are loaded as soon as the current ones are used.
     float* stage_f = reinterpret_cast<float*>(stage_out);
+    const __nv_bfloat16* residual_bf = static_cast<const __nv_bfloat16*>(p.residual);
+    __nv_bfloat16* out_bf = static_cast<__nv_bfloat16*>(p.out);
     uint4 res[MBLK][4];
     auto load_residual = [&](int mb, int64_t nb) {
       const int ppr = min(128, p.co_count - mb * 128) / 8;
@@ -574,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c8 = q - r * ppr;
           const int64_t row = slot_voxel(p.order, nb + r, n_rows);
           if (row >= 0)
-            res[mb][j] = __ldg(reinterpret_cast<const uint4*>(p.residual + row * p.co + p.co_base +
+            res[mb][j] = __ldg(reinterpret_cast<const uint4*>(residual_bf + row * p.co + p.co_base +
                                                               mb * 128 + c8 * 8));
         }
       }
@@ -587,7 +743,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int64_t n0 = t * TILE_N;
       const uint32_t tcol = tmem_base + ((sub * 32u) << 16) + buf * static_cast<uint32_t>(MBLK * TILE_N);
-      if (!fused) {
+      if constexpr (kTf32) {
+        // fp32 output: one 128-channel block at a time staged in fp32 (32
+        // rows x 128), then stored as 16-byte pieces (4 channels) of the
+        // rows; the fused epilogue adds the residual piece and applies the
+        // activation before the store.  Each thread reads and writes the same
+        // (row, piece) pairs, so the residual may be the output.
+        const float* residual_f = static_cast<const float*>(p.residual);
+        float* out_f = static_cast<float*>(p.out);
+        for (int vc = 0; vc < TILE_N / 32; ++vc) {
+#pragma unroll
+          for (int mb = 0; mb < MBLK; ++mb) {
+            const int ppr = min(128, p.co_count - mb * 128) / 4;
+            const int co_s = static_cast<int>(sub) * 32 + static_cast<int>(lane);
+            epilogue_bar();  // the staging buffer is free
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tcol + mb * TILE_N + vc * 32, v);
+            tmem_ld_wait();
+            const float b = bias_s[mb * 128 + co_s];  // zero beyond co_count
+#pragma unroll
+            for (int i = 0; i < 32; ++i) stage_f[i * 128 + co_s] = __uint_as_float(v[i]) + b;
+            epilogue_bar();
+            for (int q = et; q < 32 * ppr; q += 128) {
+              const int r = q / ppr;
+              const int c4 = q - r * ppr;
+              const int64_t row = slot_voxel(p.order, n0 + vc * 32 + r, n_rows);
+              if (row < 0) continue;
+              float4 a = *reinterpret_cast<const float4*>(stage_f + r * 128 + c4 * 4);
+              const int64_t o = row * p.co + p.co_base + mb * 128 + c4 * 4;
+              if (fused) {
+                if (residual_f != nullptr) {
+                  const float4 rr = __ldg(reinterpret_cast<const float4*>(residual_f + o));
+                  a.x += rr.x;
+                  a.y += rr.y;
+                  a.z += rr.z;
+                  a.w += rr.w;
+                }
+                a.x = apply_activation(a.x, p.act);
+                a.y = apply_activation(a.y, p.act);
+                a.z = apply_activation(a.z, p.act);
+                a.w = apply_activation(a.w, p.act);
+              }
+              *reinterpret_cast<float4*>(out_f + o) = a;
+            }
+          }
+        }
+      } else if (!fused) {
         for (int vc = 0; vc < TILE_N / 32; ++vc) {
           epilogue_bar();  // the previous chunk's staged rows have been stored
 #pragma unroll
@@ -609,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c8 = q - r * chunks_per_row;
             const int64_t n = slot_voxel(p.order, n0 + vc * 32 + r, n_rows);
             if (n >= 0)
-              *reinterpret_cast<uint4*>(p.out + n * p.co + p.co_base + c8 * 8) =
+              *reinterpret_cast<uint4*>(out_bf + n * p.co + p.co_base + c8 * 8) =
                   *reinterpret_cast<const uint4*>(stage_out + r * kOutStride + c8 * 8);
           }
         }
@@ -651,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
                 o[h] = *reinterpret_cast<const uint32_t*>(&pr);
               }
-              *reinterpret_cast<uint4*>(p.out + row * p.co + p.co_base + mb * 128 + c8 * 8) =
+              *reinterpret_cast<uint4*>(out_bf + row * p.co + p.co_base + mb * 128 + c8 * 8) =
                   make_uint4(o[0], o[1], o[2], o[3]);
             }
             if (vc + 1 < TILE_N / 32) load_residual(mb, nb + 32);
@@ -671,9 +872,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Weight loads issued but never consumed exist only after a timed-out
     // wait: wait (bounded) for them to land before the CTA's memory goes away.
     const uint32_t fills = *fills_holder;
-    const uint32_t np = S * (kSplit ? 2u : 1u);
-    for (uint32_t i = *consumed_holder; i < fills; ++i)
-      mbar_wait(smem_addr(&full[i % np]), (i / np) & 1u);
+    if constexpr (kTranspose) {
+      for (uint32_t i = *raw_consumed_holder; i < fills; ++i)
+        mbar_wait(smem_addr(&raw_full[i & 1u]), (i >> 1) & 1u);
+    } else {
+      const uint32_t np = S * (kSplit ? 2u : 1u);
+      for (uint32_t i = *consumed_holder; i < fills; ++i)
+        mbar_wait(smem_addr(&full[i % np]), (i / np) & 1u);
+    }
   }
   __syncthreads();
   if (warp == 1) {
@@ -702,7 +908,7 @@ EncodeTiledFn encode_fn(spconv_status* st) {
   return fn;
 }
 
-template <int TILE_N, int MBLK, bool kHoist, bool kDgrad, bool kSplit>
+template <int TILE_N, int MBLK, bool kHoist, bool kDgrad, bool kSplit, bool kTf32>
 spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t stream) {
   const int sms = sm_count();
   if (sms <= 0) return fail(SPCONV_ERR_CUDA, "could not query the SM count");
@@ -711,25 +917,31 @@ spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t str
   p.w_bytes = p.cps * MBLK * kWBlockBytes;
   p.stage_bytes = p.w_bytes + p.cps * TILE_N * 128u;
   p.tmem_cols = 512u;  // kAccBufs accumulator buffers of MBLK x TILE_N columns
-  // D f32, A and B bf16, B (gathered rows) K-major; A (weights) channel-major
-  // for the forward pass, K-major for the input gradient.
-  const uint32_t a_mn_major = kDgrad ? 0u : 1u;
-  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major << 15) |
+  // D f32; A and B bf16 (format 1) or tf32 (format 2); B (gathered rows)
+  // K-major; A (weights) channel-major for the bf16 forward pass, K-major for
+  // the input gradient and for the tf32 forward (transposed in the kernel).
+  constexpr bool kTranspose = kTf32 && !kDgrad;
+  const uint32_t a_mn_major = (kDgrad || kTf32) ? 0u : 1u;
+  const uint32_t fmt = kTf32 ? 2u : 1u;
+  p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (a_mn_major << 15) |
             ((static_cast<uint32_t>(TILE_N) >> 3) << 17) | ((128u >> 4) << 24);
+  p.raw_bytes = kTranspose ? MBLK * kWBlockBytes : 0u;
 
   const uint32_t ring_bytes = kRing * TILE_N * 4u;
   // 32 staged output rows: bf16 for all channels, or fp32 for one 128-channel
   // block (fused epilogue); the larger of the two.
   const uint32_t stage_out_bytes = (32u * MBLK * 128u * 2u > 32u * 128u * 4u) ? 32u * MBLK * 128u * 2u
                                                                               : 32u * 128u * 4u;
-  const uint32_t fixed = ring_bytes + stage_out_bytes + 256u * 4u + (kMaxStages + kRing) * 4u +
-                         (2u * kMaxStages + 2u * kRing + 5u) * 8u + 16u + 1024u;
+  const uint32_t fixed = 2u * p.raw_bytes + ring_bytes + stage_out_bytes + 256u * 4u +
+                         (kMaxStages + kRing) * 4u + (2u * kMaxStages + 2u * kRing + 9u) * 8u + 32u + 1024u;
   uint32_t stages = (kMaxSmem - fixed) / p.stage_bytes;
   constexpr uint32_t parts = kSplit ? 2u : 1u;
   if (stages * parts > kMaxStages) stages = kMaxStages / parts;
   if (stages < 2) return fail(SPCONV_ERR_UNSUPPORTED, "shared memory too small for the tile shape");
   p.stages = stages;
   uint32_t off = stages * p.stage_bytes;
+  p.off_raw = off;  // 1024-aligned (stage sizes are multiples of 1 KB)
+  off += 2u * p.raw_bytes;
   p.off_ring = off;
   off += ring_bytes;
   p.off_stage_out = off;
@@ -740,10 +952,10 @@ spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t str
   off += (stages + kRing) * 4u;
   off = (off + 7u) & ~7u;
   p.off_bars = off;
-  off += (2u * stages * parts + 2u * kRing + 5u) * 8u + 16u;
+  off += (2u * stages * parts + 2u * kRing + 9u) * 8u + 32u;
   const uint32_t smem_bytes = off + 1024u;  // slack for the 1024-byte alignment
 
-  auto kern = submconv_tc_kernel<TILE_N, MBLK, kHoist, kDgrad, kSplit>;
+  auto kern = submconv_tc_kernel<TILE_N, MBLK, kHoist, kDgrad, kSplit, kTf32>;
   spconv_status st = SPCONV_OK;
   if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem_bytes)),
@@ -754,10 +966,10 @@ spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t str
   return SPCONV_OK;
 }
 
-template <int MBLK, bool kHoist, bool kSplit>
+template <int MBLK, bool kHoist, bool kSplit, bool kTf32 = false>
 spconv_status launch_dir(const CUtensorMap& tm_w, const TcParams& p, cudaStream_t stream) {
-  return p.dgrad != 0 ? launch_shape<256, MBLK, kHoist, true, kSplit>(tm_w, p, stream)
-                      : launch_shape<256, MBLK, kHoist, false, kSplit>(tm_w, p, stream);
+  return p.dgrad != 0 ? launch_shape<256, MBLK, kHoist, true, kSplit, kTf32>(tm_w, p, stream)
+                      : launch_shape<256, MBLK, kHoist, false, kSplit, kTf32>(tm_w, p, stream);
 }
 
 }  // namespace
@@ -779,38 +991,45 @@ spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_
                              const void* w, const void* bias, const void* residual, void* out,
                              int64_t n, int32_t k, int32_t ci, int32_t co, spconv_activation act,
                              bool dgrad, cudaStream_t stream, const int32_t* order) {
-  if (dtype != SPCONV_BF16) return fail(SPCONV_ERR_UNSUPPORTED, "tensor-core path supports bf16 only");
+  if (dtype != SPCONV_BF16 && dtype != SPCONV_TF32)
+    return fail(SPCONV_ERR_UNSUPPORTED, "tensor-core path supports bf16 and tf32 only");
+  const bool tf32 = dtype == SPCONV_TF32;
+  const uint32_t esz = tf32 ? 4u : 2u;
+  const int chunk = tf32 ? 32 : kChunk;  // channels per 128-byte row
   spconv_status st = SPCONV_OK;
   EncodeTiledFn encode = encode_fn(&st);
   if (encode == nullptr) return st;
 
-  // w viewed as its (K, Ci_fwd, Co_fwd) layout, innermost Co_fwd.  Forward:
-  // box = 64 output channels x 64 input channels of one offset (the
-  // channel-major UMMA operand).  Input gradient (ci = Co_fwd, co = Ci_fwd):
-  // box = 64 forward-co x 128 forward-ci, i.e. 128 output rows with 64 input
-  // channels each (the K-major operand).  128-byte swizzle in both.
+  // w viewed as its (K, Ci_fwd, Co_fwd) layout, innermost Co_fwd; boxes are
+  // 128 bytes wide (64 bf16 or 32 fp32 elements), 128-byte swizzle.  bf16
+  // forward: box = 64 output channels x 64 input channels of one offset (the
+  // channel-major UMMA operand).  tf32 forward: 32 x 32 boxes, transposed in
+  // the kernel.  Input gradient (ci = Co_fwd, co = Ci_fwd): box = one row
+  // width of forward-co x 128 forward-ci, i.e. 128 output rows with 64 (32)
+  // input channels each (the K-major operand).
   const cuuint64_t wi = static_cast<cuuint64_t>(dgrad ? co : ci);  // forward Ci
   const cuuint64_t wo = static_cast<cuuint64_t>(dgrad ? ci : co);  // forward Co
   CUtensorMap tm_w;
   cuuint64_t dims[3] = {wo, wi, static_cast<cuuint64_t>(k)};
-  cuuint64_t strides[2] = {wo * 2, wi * wo * 2};
-  cuuint32_t box[3] = {64, dgrad ? 128u : 64u, 1};
+  cuuint64_t strides[2] = {wo * esz, wi * wo * esz};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(chunk), dgrad ? 128u : static_cast<cuuint32_t>(chunk), 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides,
-                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = encode(&tm_w, tf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                      const_cast<void*>(w), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(SPCONV_ERR_CUDA, "cuTensorMapEncodeTiled(w) failed: " + std::to_string(r));
 
   for (int32_t co_base = 0; co_base < co; co_base += 256) {
     TcParams p{};
-    p.feats = static_cast<const __nv_bfloat16*>(feats);
+    p.feats = feats;
     p.nmap = nmap;
-    p.bias = static_cast<const __nv_bfloat16*>(bias);
-    p.residual = static_cast<const __nv_bfloat16*>(residual);
+    p.bias = bias;
+    p.residual = residual;
     p.act = static_cast<int32_t>(act);
     p.dgrad = dgrad ? 1 : 0;
-    p.out = static_cast<__nv_bfloat16*>(out);
+    p.out = out;
     p.order = order;
     p.n = n;
     p.k = k;
@@ -818,7 +1037,7 @@ spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_
     p.co = co;
     p.co_base = co_base;
     p.co_count = (co - co_base) < 256 ? (co - co_base) : 256;
-    p.num_chunks = (ci + kChunk - 1) / kChunk;
+    p.num_chunks = (ci + chunk - 1) / chunk;
     // Two 64-channel chunks per stage where they fit (two 96 KB stages):
     // a stage's cost is mostly fixed, so fewer, larger stages are faster
     // (measured: decoder 8.3 -> 7.7 ms, medium 0.72 -> 0.64 ms).
@@ -827,7 +1046,16 @@ spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_
     // Ci = 256, Co = 128 2.27 -> 2.05 ms; with Ci = 128 they cost 1-4%).
     const bool split = p.cps == 2 && p.num_chunks > 2;
     const bool hoist = p.num_chunks >= 2;
-    if (split)
+    if (tf32) {
+      // one 32-channel chunk per stage (48 KB, or 64 KB with two M blocks)
+      p.cps = 1;
+      if (p.co_count <= 128)
+        st = hoist ? launch_dir<1, true, false, true>(tm_w, p, stream)
+                   : launch_dir<1, false, false, true>(tm_w, p, stream);
+      else
+        st = hoist ? launch_dir<2, true, false, true>(tm_w, p, stream)
+                   : launch_dir<2, false, false, true>(tm_w, p, stream);
+    } else if (split)
       st = launch_dir<1, true, true>(tm_w, p, stream);
     else if (p.co_count <= 128)
       st = hoist ? launch_dir<1, true, false>(tm_w, p, stream) : launch_dir<1, false, false>(tm_w, p, stream);

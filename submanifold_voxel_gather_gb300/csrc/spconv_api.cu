@@ -228,9 +228,9 @@ spconv_status submconv3d_impl(const void* feats_dev, const int32_t* nmap_dev, co
   spconv_status st = check_device();
   if (st != SPCONV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // SPCONV_TF32 runs the exact fp32 kernel for now (its results are within
-  // the tf32 tolerance); the tensor-core tf32 variant is not enabled.
-  if (dtype == SPCONV_F32 || dtype == SPCONV_TF32)
+  // SPCONV_F32: exact fp32 products on CUDA cores; SPCONV_TF32 and
+  // SPCONV_BF16: the tensor-core kernel (kind::tf32 / kind::f16 MMAs).
+  if (dtype == SPCONV_F32)
     st = launch_conv_simt_f32(static_cast<const float*>(feats_dev), nmap_dev,
                               static_cast<const float*>(w_dev), static_cast<const float*>(bias_dev),
                               static_cast<const float*>(residual_dev), static_cast<float*>(out_dev), N,

@@ -132,6 +132,41 @@ def test_other_offset_counts(sv, oracle_mod, k, dtype):
     assert_within(run_gpu(sv, feats, nmap, w, b, dtype), ref, sabs, dtype)
 
 
+@pytest.mark.parametrize("ci,co", [(32, 32), (64, 128), (128, 128), (96, 208)])
+def test_tf32_runs_tensor_core_products(sv, oracle_mod, ci, co):
+    """SPCONV_TF32 takes the tensor-core kernel (kind::tf32): its products use
+    operands with 10 mantissa bits, so on inputs whose low mantissa bits are
+    set its output differs from the exact-fp32 kernel's (SPCONV_F32) by at
+    most what that operand rounding allows (2 * 2^-10 relative per product,
+    plus fp32 accumulation), while staying within the tf32 tolerance of the
+    oracle.  It also matches the oracle evaluated on the inputs rounded to 10
+    mantissa bits (toward zero or to nearest) within the fp32 bound."""
+    import torch
+    coords = W.random_occupancy(16, 0.3, ci + 3 * co)
+    nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    feats, w, b = layer_values(ci + co, len(coords), 27, ci, co, "f32")
+    ref, sabs = oracle_mod.conv(feats, nmap, w, b, "f32", threads=oracle_mod.host_threads())
+    got_tf32 = run_gpu(sv, feats, nmap, w, b, "tf32")
+    got_f32 = run_gpu(sv, feats, nmap, w, b, "f32")
+    assert_within(got_tf32, ref, sabs, "tf32")
+    assert_within(got_f32, ref, sabs, "f32")
+    assert not np.array_equal(got_tf32, got_f32)
+    assert (np.abs(got_tf32 - got_f32) <= (2 * 2.0 ** -10 + 1e-5) * sabs).all()
+
+    def to_tf32(a, nearest):
+        bits = np.ascontiguousarray(a, np.float32).view(np.uint32).astype(np.uint64)
+        if nearest:
+            bits = bits + 0x1000 + ((bits >> 13) & 1) - 1   # round half to even at bit 13
+        return (bits & np.uint64(0xFFFFE000)).astype(np.uint32).view(np.float32)
+
+    fits = []
+    for nearest in (False, True):
+        ref_t, sabs_t = oracle_mod.conv(to_tf32(feats, nearest), nmap, to_tf32(w, nearest), b, "f32",
+                                        threads=oracle_mod.host_threads())
+        fits.append(bool((np.abs(got_tf32 - ref_t) <= 1e-5 * sabs_t).all()))
+    assert any(fits), "tf32 output matches neither truncated nor rounded tf32 operands"
+
+
 def test_isolated_voxels_reduce_to_centre_gemm(sv, oracle_mod):
     """Voxels with no neighbour: out = feats @ w[13] + bias."""
     g = np.arange(0, 40, 3)

@@ -40,14 +40,15 @@ def run_ex(sv, nmap, feats, w, b, res, dtype, act, in_place=False):
     f, ww, bb = torch_storage(feats, dtype), torch_storage(w, dtype), torch_storage(b, dtype)
     r = None if res is None else torch_storage(res, dtype)
     out = r if in_place else None
-    got = sv.submconv3d(f, nm, ww, bb, out=out, residual=r, activation=act)
+    got = sv.submconv3d(f, nm, ww, bb, out=out, residual=r, activation=act,
+                        dtype=("tf32" if dtype == "tf32" else None))
     sv.device_status()
     if in_place:
         assert got.data_ptr() == r.data_ptr()
     return to_f64(got)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "tf32"])
 @pytest.mark.parametrize("act", ["relu", "silu", None])
 @pytest.mark.parametrize("with_res", [True, False])
 def test_epilogue_matches_oracle(sv, oracle_mod, dtype, act, with_res):
@@ -59,18 +60,19 @@ def test_epilogue_matches_oracle(sv, oracle_mod, dtype, act, with_res):
     assert_within(got, ref, scale, dtype)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "tf32"])
 @pytest.mark.parametrize("ci,co", [(128, 128), (64, 256), (32, 272)])
-def test_epilogue_channel_shapes_bf16(sv, oracle_mod, ci, co):
+def test_epilogue_channel_shapes(sv, oracle_mod, ci, co, dtype):
     """One and two M blocks, and Co > 256 (two launches, the second with a
     16-channel remainder): each launch adds its own channel range of the
     residual."""
-    nmap, feats, w, b, res = case(oracle_mod, 14, 0.3, ci + co, ci, co, "bf16")
-    ref, scale = oracle_mod.conv_fused(feats, nmap, w, b, "bf16", residual=res, act="silu",
+    nmap, feats, w, b, res = case(oracle_mod, 14, 0.3, ci + co, ci, co, dtype)
+    ref, scale = oracle_mod.conv_fused(feats, nmap, w, b, dtype, residual=res, act="silu",
                                        threads=oracle_mod.host_threads())
-    assert_within(run_ex(sv, nmap, feats, w, b, res, "bf16", "silu"), ref, scale, "bf16")
+    assert_within(run_ex(sv, nmap, feats, w, b, res, dtype, "silu"), ref, scale, dtype)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "tf32"])
 def test_epilogue_in_place_residual(sv, oracle_mod, dtype):
     """out is the residual buffer itself (x <- act(conv(x') + b + x))."""
     nmap, feats, w, b, res = case(oracle_mod, 15, 0.3, 71, 64, 128, dtype)
