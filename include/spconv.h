@@ -384,7 +384,12 @@ spconv_status spconv_xrun_layout(const int32_t* coords_dev, const int32_t* nmap_
  * tolerance (products in bf16, fp32 accumulation, one rounding to bf16 after
  * the bias); the order of the fp32 additions differs.
  *
- *  slots_dev, slot_count_dev  from spconv_xrun_layout on the same map.
+ *  slots_dev, slot_count_dev  from spconv_xrun_layout on the same map; the
+ *                             kernel reads S from slot_count_dev and clamps
+ *                             it to slots_capacity (the entries of
+ *                             slots_dev), so no read leaves the buffer.
+ *                             Slot codes naming no voxel of [0, N) are
+ *                             treated as empty.
  *  dtype                      SPCONV_BF16 only; K = 27, Ci = 128, Co a
  *                             multiple of 16 in [16, 128].
  *
@@ -392,9 +397,9 @@ spconv_status spconv_xrun_layout(const int32_t* coords_dev, const int32_t* nmap_
  * return SPCONV_ERR_UNSUPPORTED.
  */
 spconv_status spconv_submconv3d_xrun(const void* feats_dev, const int32_t* nmap_dev, const int32_t* slots_dev,
-                                     const int64_t* slot_count_dev, const void* w_dev, const void* bias_dev,
-                                     void* out_dev, int64_t N, int32_t K, int32_t Ci, int32_t Co,
-                                     spconv_dtype dtype, void* stream);
+                                     int64_t slots_capacity, const int64_t* slot_count_dev, const void* w_dev,
+                                     const void* bias_dev, void* out_dev, int64_t N, int32_t K, int32_t Ci,
+                                     int32_t Co, spconv_dtype dtype, void* stream);
 
 /*
  * Wait for `stream`, then read and clear the current device's sticky kernel

@@ -101,8 +101,8 @@ def load_library() -> ctypes.CDLL:
         lib.spconv_xrun_slot_capacity.restype = i64
         lib.spconv_xrun_layout.argtypes = [vp, vp, i64, i32, vp, i64, vp, vp, ctypes.c_size_t, vp]
         lib.spconv_xrun_layout.restype = ctypes.c_int
-        lib.spconv_submconv3d_xrun.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, ctypes.c_int,
-                                               vp]
+        lib.spconv_submconv3d_xrun.argtypes = [vp, vp, vp, i64, vp, vp, vp, vp, i64, i32, i32, i32,
+                                               ctypes.c_int, vp]
         lib.spconv_submconv3d_xrun.restype = ctypes.c_int
         lib.spconv_count_valid_pairs.argtypes = [vp, i64, i32, vp, vp]
         lib.spconv_count_valid_pairs.restype = ctypes.c_int
@@ -401,8 +401,9 @@ def submconv3d_xrun(feats, nmap, slots, slot_count, w, bias=None, out=None, stre
         _require_cuda(out, "out", feats.dtype)
         if tuple(out.shape) != (n, co):
             raise ValueError("out must have shape (N, Co)")
-    _check(load_library().spconv_submconv3d_xrun(_ptr(feats), _ptr(nmap), _ptr(slots), _ptr(slot_count), _ptr(w),
-                                                 _ptr(bias), _ptr(out), n, k, ci, co, BF16, _stream_handle(stream)))
+    _check(load_library().spconv_submconv3d_xrun(_ptr(feats), _ptr(nmap), _ptr(slots), slots.numel(),
+                                                 _ptr(slot_count), _ptr(w), _ptr(bias), _ptr(out), n, k, ci, co,
+                                                 BF16, _stream_handle(stream)))
     return out
 
 

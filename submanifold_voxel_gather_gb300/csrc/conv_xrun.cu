@@ -74,6 +74,7 @@ struct XrParams {
   const int32_t* nmap;
   const int32_t* slots;
   const int64_t* slot_count;
+  int64_t slots_capacity;  // entries of slots: S is clamped to it
   const __nv_bfloat16* bias;
   __nv_bfloat16* out;
   int64_t n;
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int64_t n_rows = p.n;
-  const int64_t S = __ldg(p.slot_count);
+  const int64_t S = max(int64_t{0}, min(__ldg(p.slot_count), p.slots_capacity));
   const int64_t num_tiles = (S + kTileN - 1) / kTileN;
 
   if (warp == 2) {
@@ -547,8 +548,8 @@ spconv_status read_and_clear_xrun_device_error(cudaStream_t stream, unsigned int
 }
 
 spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int32_t* slots,
-                               const int64_t* slot_count, const void* w, const void* bias, void* out,
-                               int64_t n, int32_t co, cudaStream_t stream) {
+                               int64_t slots_capacity, const int64_t* slot_count, const void* w,
+                               const void* bias, void* out, int64_t n, int32_t co, cudaStream_t stream) {
   spconv_status st = SPCONV_OK;
   EncodeTiledFn encode = xrun_encode_fn(&st);
   if (encode == nullptr) return st;
@@ -568,6 +569,7 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
   p.nmap = nmap;
   p.slots = slots;
   p.slot_count = slot_count;
+  p.slots_capacity = slots_capacity;
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.n = n;

@@ -90,7 +90,7 @@ spconv_status launch_xrun_layout(const int32_t* coords, const int32_t* nmap, int
                                  int64_t cap, int64_t* slot_count, void* workspace, cudaStream_t stream);
 // bf16, lexicographic 3x3x3 offsets, Ci = 128, Co <= 128
 spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int32_t* slots,
-                               const int64_t* slot_count, const void* w, const void* bias, void* out,
-                               int64_t n, int32_t co, cudaStream_t stream);
+                               int64_t slots_capacity, const int64_t* slot_count, const void* w,
+                               const void* bias, void* out, int64_t n, int32_t co, cudaStream_t stream);
 
 }  // namespace spconv

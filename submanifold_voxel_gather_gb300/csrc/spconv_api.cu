@@ -302,9 +302,9 @@ spconv_status spconv_xrun_layout(const int32_t* coords_dev, const int32_t* nmap_
 }
 
 spconv_status spconv_submconv3d_xrun(const void* feats_dev, const int32_t* nmap_dev, const int32_t* slots_dev,
-                                     const int64_t* slot_count_dev, const void* w_dev, const void* bias_dev,
-                                     void* out_dev, int64_t N, int32_t K, int32_t Ci, int32_t Co,
-                                     spconv_dtype dtype, void* stream) {
+                                     int64_t slots_capacity, const int64_t* slot_count_dev, const void* w_dev,
+                                     const void* bias_dev, void* out_dev, int64_t N, int32_t K, int32_t Ci,
+                                     int32_t Co, spconv_dtype dtype, void* stream) {
   if (N < 1 || N >= (int64_t{1} << 30)) return fail(SPCONV_ERR_INVALID_ARG, "N must be in [1, 2^30)");
   if (dtype != SPCONV_BF16 || K != 27 || Ci != 128 || Co < 16 || Co > 128 || Co % 16 != 0)
     return fail(SPCONV_ERR_UNSUPPORTED, "the x-run conv takes bf16, K = 27, Ci = 128 and Co in [16, 128], a multiple of 16");
@@ -315,10 +315,11 @@ spconv_status spconv_submconv3d_xrun(const void* feats_dev, const int32_t* nmap_
       !spconv::aligned(nmap_dev, 4) || !spconv::aligned(slots_dev, 4) || !spconv::aligned(slot_count_dev, 8) ||
       (bias_dev != nullptr && !spconv::aligned(bias_dev, 2)))
     return fail(SPCONV_ERR_INVALID_ARG, "misaligned pointer");
+  if (slots_capacity < 1) return fail(SPCONV_ERR_INVALID_ARG, "slots_capacity must be >= 1");
   spconv_status st = spconv::check_device();
   if (st != SPCONV_OK) return st;
-  st = spconv::launch_conv_xrun(feats_dev, nmap_dev, slots_dev, slot_count_dev, w_dev, bias_dev, out_dev, N, Co,
-                                static_cast<cudaStream_t>(stream));
+  st = spconv::launch_conv_xrun(feats_dev, nmap_dev, slots_dev, slots_capacity, slot_count_dev, w_dev, bias_dev,
+                                out_dev, N, Co, static_cast<cudaStream_t>(stream));
   return st == SPCONV_OK ? spconv::ok() : st;
 }
 

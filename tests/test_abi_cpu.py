@@ -147,15 +147,16 @@ def test_xrun_entry_points_validate_without_gpu(lib):
     assert _status(xl(fake, fake, n, 27, fake, cap, ctypes.c_void_p(0x100004), fake, ws, None))[0] == -1
     assert _status(xl(fake, fake, n, 27, fake, cap, fake, fake, ws - 1, None))[0] == -3
     xc = lib.spconv_submconv3d_xrun
-    assert _status(xc(fake, fake, fake, fake, fake, None, fake, n, 27, 128, 128, 0, None))[0] == -2
-    assert _status(xc(fake, fake, fake, fake, fake, None, fake, n, 27, 64, 128, 2, None))[0] == -2
-    assert _status(xc(fake, fake, fake, fake, fake, None, fake, n, 27, 128, 256, 2, None))[0] == -2
-    assert _status(xc(fake, fake, fake, fake, fake, None, fake, n, 27, 128, 24, 2, None))[0] == -2
-    assert _status(xc(fake, fake, fake, fake, fake, None, fake, n, 125, 128, 128, 2, None))[0] == -2
-    assert _status(xc(fake, fake, None, fake, fake, None, fake, n, 27, 128, 128, 2, None))[0] == -1
-    assert _status(xc(fake, fake, fake, fake, ctypes.c_void_p(0x100008), None, fake, n, 27, 128, 128, 2,
+    assert _status(xc(fake, fake, fake, 31, fake, fake, None, fake, n, 27, 128, 128, 0, None))[0] == -2
+    assert _status(xc(fake, fake, fake, 31, fake, fake, None, fake, n, 27, 64, 128, 2, None))[0] == -2
+    assert _status(xc(fake, fake, fake, 31, fake, fake, None, fake, n, 27, 128, 256, 2, None))[0] == -2
+    assert _status(xc(fake, fake, fake, 31, fake, fake, None, fake, n, 27, 128, 24, 2, None))[0] == -2
+    assert _status(xc(fake, fake, fake, 31, fake, fake, None, fake, n, 125, 128, 128, 2, None))[0] == -2
+    assert _status(xc(fake, fake, None, 31, fake, fake, None, fake, n, 27, 128, 128, 2, None))[0] == -1
+    assert _status(xc(fake, fake, fake, 31, fake, ctypes.c_void_p(0x100008), None, fake, n, 27, 128, 128, 2,
                       None))[0] == -1
-    assert _status(xc(fake, fake, fake, fake, fake, None, fake, 0, 27, 128, 128, 2, None))[0] == -1
+    assert _status(xc(fake, fake, fake, 31, fake, fake, None, fake, 0, 27, 128, 128, 2, None))[0] == -1
+    assert _status(xc(fake, fake, fake, 0, fake, fake, None, fake, n, 27, 128, 128, 2, None))[0] == -1
 
 
 def test_python_binding_rejects_cpu_tensors(lib):
