@@ -79,3 +79,43 @@ def test_separator_counts(oracle_mod):
     nm = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
     slots = layout_reference(coords, nmap=nm)
     assert len(slots) == 64 + 63
+
+
+def test_tiled_shifted_sum_equals_oracle(oracle_mod):
+    """The row-shifted convolution's data flow in numpy: 256-slot tiles, one
+    258-row operand per (dz, dy) group gathered from the slots one before the
+    tile to one after it, the three dx offsets read 0, 1 and 2 rows in.  Its
+    voxel rows equal the oracle's sum."""
+    coords = W.random_occupancy(14, 0.3, 60)
+    n = len(coords)
+    nm = oracle_mod.build_nmap(coords, W.offsets_3x3x3()).astype(np.int64)
+    nm[(nm < 0) | (nm >= n)] = n
+    rng = np.random.default_rng(1)
+    ci, co = 8, 5
+    feats = rng.standard_normal((n, ci))
+    w = rng.standard_normal((27, ci, co))
+    b = rng.standard_normal(co)
+    slots = layout_reference(coords, nmap=nm)
+    S = len(slots)
+    fpad = np.vstack([feats, np.zeros((1, ci))])  # row n: a missing neighbour
+    out = np.full((n, co), np.nan)
+    tile = 256
+    for s0 in range(0, S, tile):
+        acc = np.zeros((tile, co))
+        for g in range(9):
+            rows = []
+            for r in range(tile + 2):
+                s = s0 - 1 + r
+                code = slots[s] if 0 <= s < S else -1
+                rows.append(group_row(nm, n, code, g))
+            G = fpad[np.array(rows)]
+            for dxi in range(3):
+                acc += G[dxi:dxi + tile] @ w[3 * g + dxi]
+        for j in range(tile):
+            s = s0 + j
+            if s < S and slots[s] >= 0:
+                out[slots[s]] = acc[j] + b
+    ref, _ = oracle_mod.conv(feats.astype(np.float32), nm.astype(np.int32), w.astype(np.float32),
+                             b.astype(np.float32), "f32")
+    assert not np.isnan(out).any()
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-9 * np.abs(ref).max() + 1e-5)
