@@ -62,10 +62,12 @@ constexpr int kProducerThreads = 128;
 constexpr int kEpilogueWarp0 = 4;
 constexpr uint64_t kAStepUnits = (16 * 128) >> 4;   // one K step of channel-major weights
 constexpr uint64_t kBStepUnits = (16 * 2) >> 4;     // one K step of K-major rows
-// The B descriptor of a row-shifted operand: start address dxi * 128 bytes
-// into the 1024-byte-aligned chunk.  With kShiftBaseOffset the descriptor's
-// base-offset field carries (start >> 7) & 7.
-constexpr bool kShiftBaseOffset = true;
+// The B descriptor of an operand shifted by dxi rows in its 1024-byte-aligned
+// chunk (128-byte swizzle, so the swizzle pattern repeats every 8 rows):
+//   0: start address + dxi * 128, base-offset field 0;
+//   1: start address + dxi * 128, base-offset field (start >> 7) & 7;
+//   2: start address on the chunk's row 0, base-offset field dxi.
+constexpr int kShiftMode = 1;
 
 enum : uint32_t { kMetaFirst = 1u, kMetaEnd = 2u };
 
@@ -425,9 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
             }
             const uint64_t ad = adesc0 + ws * (kWSlotBytes >> 4);
-            const uint32_t baddr = gaddr + c * kGChunkBytes + static_cast<uint32_t>(dxi) * 128u;
+            const uint32_t baddr = gaddr + c * kGChunkBytes + (kShiftMode == 2 ? 0u : static_cast<uint32_t>(dxi) * 128u);
             uint64_t bd = sw128_desc(baddr, 16u, 1024u);
-            if (kShiftBaseOffset) bd |= static_cast<uint64_t>((baddr >> 7) & 7u) << 49;
+            if (kShiftMode == 1) bd |= static_cast<uint64_t>((baddr >> 7) & 7u) << 49;
+            if (kShiftMode == 2) bd |= static_cast<uint64_t>(dxi) << 49;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               umma_f16(d_tmem, ad + ks * kAStepUnits, bd + ks * kBStepUnits, idesc, acc);
