@@ -402,6 +402,22 @@ spconv_status spconv_submconv3d_xrun(const void* feats_dev, const int32_t* nmap_
                                      int32_t Co, spconv_dtype dtype, void* stream);
 
 /*
+ * spconv_submconv3d_dgrad over an x-run slot layout: dfeats (N, Ci) from
+ * dout (N, Co), dfeats[n] = sum_k dout[nmap[k, n]] . w[K-1-k]^T (the map of
+ * the 3x3x3 offsets is symmetric), with the row-shifted operands of
+ * spconv_submconv3d_xrun gathered from dout.
+ *
+ *  dtype  SPCONV_BF16 only; K = 27, Co = 128 (the reduced channels), Ci a
+ *         multiple of 16 in [16, 128] (the output channels).
+ *
+ * Other arguments as spconv_submconv3d_xrun and spconv_submconv3d_dgrad.
+ */
+spconv_status spconv_submconv3d_dgrad_xrun(const void* dout_dev, const int32_t* nmap_dev, const int32_t* slots_dev,
+                                           int64_t slots_capacity, const int64_t* slot_count_dev,
+                                           const void* w_dev, void* dfeats_dev, int64_t N, int32_t K, int32_t Ci,
+                                           int32_t Co, spconv_dtype dtype, void* stream);
+
+/*
  * Wait for `stream`, then read and clear the current device's sticky kernel
  * error word.  Returns SPCONV_OK if no kernel of this library has reported
  * an internal error since the last call, else SPCONV_ERR_DEVICE with the

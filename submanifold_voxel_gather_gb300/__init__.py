@@ -24,7 +24,7 @@ import numpy as np
 __all__ = [
     "SpconvError", "load_library", "library_path", "version", "workspace_size", "build_nmap",
     "submconv3d", "submconv3d_dgrad", "submconv3d_wgrad", "tile_order", "count_valid_pairs",
-    "xrun_layout", "submconv3d_xrun",
+    "xrun_layout", "submconv3d_xrun", "submconv3d_dgrad_xrun",
     "device_status",
     "default_offsets", "ACTIVATIONS",
     "F32", "TF32", "BF16",
@@ -104,6 +104,9 @@ def load_library() -> ctypes.CDLL:
         lib.spconv_submconv3d_xrun.argtypes = [vp, vp, vp, i64, vp, vp, vp, vp, i64, i32, i32, i32,
                                                ctypes.c_int, vp]
         lib.spconv_submconv3d_xrun.restype = ctypes.c_int
+        lib.spconv_submconv3d_dgrad_xrun.argtypes = [vp, vp, vp, i64, vp, vp, vp, i64, i32, i32, i32,
+                                                     ctypes.c_int, vp]
+        lib.spconv_submconv3d_dgrad_xrun.restype = ctypes.c_int
         lib.spconv_count_valid_pairs.argtypes = [vp, i64, i32, vp, vp]
         lib.spconv_count_valid_pairs.restype = ctypes.c_int
         lib.spconv_device_status.argtypes = [vp]
@@ -404,6 +407,34 @@ def submconv3d_xrun(feats, nmap, slots, slot_count, w, bias=None, out=None, stre
     _check(load_library().spconv_submconv3d_xrun(_ptr(feats), _ptr(nmap), _ptr(slots), slots.numel(),
                                                  _ptr(slot_count), _ptr(w), _ptr(bias), _ptr(out), n, k, ci, co,
                                                  BF16, _stream_handle(stream)))
+    return out
+
+
+def submconv3d_dgrad_xrun(dout, nmap, slots, slot_count, w, out=None, stream=None):
+    """``submconv3d_dgrad`` over an x-run slot layout from ``xrun_layout``
+    (spconv_submconv3d_dgrad_xrun): bf16, K = 27, Co = 128, Ci <= 128.
+    Returns dfeats (N, Ci)."""
+    torch = _torch()
+    _require_cuda(dout, "dout", torch.bfloat16)
+    _require_cuda(nmap, "nmap", torch.int32)
+    _require_cuda(slots, "slots", torch.int32)
+    _require_cuda(slot_count, "slot_count", torch.int64)
+    _require_cuda(w, "w", torch.bfloat16)
+    if dout.dim() != 2 or w.dim() != 3 or nmap.dim() != 2:
+        raise ValueError("expected dout (N, Co), nmap (K, N), w (K, Ci, Co)")
+    n, co = dout.shape
+    k, ci = w.shape[0], w.shape[1]
+    if tuple(nmap.shape) != (k, n) or w.shape[2] != co:
+        raise ValueError("shapes of dout, nmap and w do not agree")
+    if out is None:
+        out = torch.empty((n, ci), dtype=dout.dtype, device=dout.device)
+    else:
+        _require_cuda(out, "out", dout.dtype)
+        if tuple(out.shape) != (n, ci):
+            raise ValueError("out must have shape (N, Ci)")
+    _check(load_library().spconv_submconv3d_dgrad_xrun(_ptr(dout), _ptr(nmap), _ptr(slots), slots.numel(),
+                                                       _ptr(slot_count), _ptr(w), _ptr(out), n, k, ci, co, BF16,
+                                                       _stream_handle(stream)))
     return out
 
 

@@ -145,6 +145,11 @@ __device__ __forceinline__ bool issue_group(uint32_t flag, int g, bool issued) {
   return flag != 0u || (g == kGroups - 1 && !issued);
 }
 
+// kDgrad: input gradient, dfeats[n] = sum_k dout[nmap[k, n]] . w[26 - k]^T
+// (the map is symmetric); the gathered rows are dout's (Co = 128 reduced
+// channels) and the weights of offset k are w[26 - k] read from the forward
+// layout as a K-major operand, as in conv_tc.cu.
+template <bool kDgrad>
 __global__ void __launch_bounds__(kThreads, 1)
     submconv_xrun_kernel(const __grid_constant__ CUtensorMap tm_w, const XrParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -357,11 +362,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive_expect_tx(fb, kWSlotBytes);
             }
             __syncwarp();
-            // w[k] channel-major: two boxes of 64 output channels x 64 input
-            // channels (128-byte swizzle)
-            if (lane < 2)
-              tma_load_3d(smem_addr(smem + p.off_w) + ws * kWSlotBytes + lane * 8192u, &tm_w,
-                          static_cast<int>(lane) * 64, c * 64, k, fb);
+            if constexpr (!kDgrad) {
+              // w[k] channel-major: two boxes of 64 output channels x 64
+              // input channels (128-byte swizzle)
+              if (lane < 2)
+                tma_load_3d(smem_addr(smem + p.off_w) + ws * kWSlotBytes + lane * 8192u, &tm_w,
+                            static_cast<int>(lane) * 64, c * 64, k, fb);
+            } else {
+              // w[26 - k]: 128 forward-ci rows with 64 forward-co entries
+              // each (K-major, 128-byte swizzle), one box
+              if (lane == 0)
+                tma_load_3d(smem_addr(smem + p.off_w) + ws * kWSlotBytes, &tm_w, c * 64, 0, 26 - k, fb);
+            }
             ++fills;
             if (++ws == kWSlots) {
               ws = 0;
@@ -384,7 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint64_t adesc0 = sw128_desc(smem_addr(smem + p.off_w), 8192u, 1024u);
+      // weights channel-major (forward) or K-major (input gradient)
+      const uint64_t adesc0 = sw128_desc(smem_addr(smem + p.off_w), kDgrad ? 16u : 8192u, 1024u);
+      constexpr uint64_t a_step = kDgrad ? kBStepUnits : kAStepUnits;
       const uint32_t g_base = smem_addr(smem + p.off_g);
       const uint32_t idesc = p.idesc;
       uint32_t ws = 0, wphase = 0, gs = 0, gphase = 0, consumed = 0, tile_i = 0, buf = 0, acc = 0;
@@ -433,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kShiftMode == 2) bd |= static_cast<uint64_t>(dxi) << 49;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-              umma_f16(d_tmem, ad + ks * kAStepUnits, bd + ks * kBStepUnits, idesc, acc);
+              umma_f16(d_tmem, ad + ks * a_step, bd + ks * kBStepUnits, idesc, acc);
               acc = 1;
             }
             umma_commit(smem_addr(&wempty[ws]));
@@ -552,15 +566,21 @@ spconv_status read_and_clear_xrun_device_error(cudaStream_t stream, unsigned int
 
 spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int32_t* slots,
                                int64_t slots_capacity, const int64_t* slot_count, const void* w,
-                               const void* bias, void* out, int64_t n, int32_t co, cudaStream_t stream) {
+                               const void* bias, void* out, int64_t n, int32_t co, bool dgrad,
+                               cudaStream_t stream) {
   spconv_status st = SPCONV_OK;
   EncodeTiledFn encode = xrun_encode_fn(&st);
   if (encode == nullptr) return st;
   CUtensorMap tm_w;
-  // weights (K, Ci, Co) row-major as a 3-D tensor (co, ci, k)
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(co), 128u, 27u};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(co) * 2u, static_cast<cuuint64_t>(co) * 128u * 2u};
-  cuuint32_t box[3] = {64u, 64u, 1u};
+  // Weights in their forward (K, Ci_fwd, Co_fwd) layout as a 3-D tensor
+  // (co_fwd, ci_fwd, k).  Forward: Ci_fwd = 128, boxes of 64 output x 64
+  // input channels.  Input gradient: Co_fwd = 128 is reduced and `co` output
+  // channels are Ci_fwd; boxes of 64 forward-co x 128 forward-ci.
+  const cuuint64_t wo = dgrad ? 128u : static_cast<cuuint64_t>(co);  // forward Co
+  const cuuint64_t wi = dgrad ? static_cast<cuuint64_t>(co) : 128u;  // forward Ci
+  cuuint64_t dims[3] = {wo, wi, 27u};
+  cuuint64_t strides[2] = {wo * 2u, wi * wo * 2u};
+  cuuint32_t box[3] = {64u, dgrad ? 128u : 64u, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box,
                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -578,10 +598,11 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
   p.n = n;
   p.co = co;
   p.co_count = co;
-  // D f32, A and B bf16, A (weights) channel-major, B (rows) K-major,
-  // N = 256, M = 128
-  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((static_cast<uint32_t>(kTileN) >> 3) << 17) |
-            ((128u >> 4) << 24);
+  // D f32, A and B bf16, A (weights) channel-major (forward) or K-major
+  // (input gradient), B (rows) K-major, N = 256, M = 128
+  const uint32_t a_mn_major = dgrad ? 0u : 1u;
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major << 15) |
+            ((static_cast<uint32_t>(kTileN) >> 3) << 17) | ((128u >> 4) << 24);
   uint32_t off = 0;
   p.off_g = off;
   off += kGStages * kGStageBytes;
@@ -601,13 +622,13 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
   const uint32_t smem_bytes = off + 1024u;  // slack for the 1024-byte alignment
   if (smem_bytes > 232448u) return fail(SPCONV_ERR_UNSUPPORTED, "x-run conv: shared memory layout too large");
 
-  if (!cuda_ok(cudaFuncSetAttribute(submconv_xrun_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem_bytes)),
+  auto kern = dgrad ? submconv_xrun_kernel<true> : submconv_xrun_kernel<false>;
+  if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes)),
                "cudaFuncSetAttribute", &st))
     return st;
   const int sms = sm_count();
   if (sms <= 0) return fail(SPCONV_ERR_CUDA, "could not query the SM count");
-  submconv_xrun_kernel<<<sms, kThreads, smem_bytes, stream>>>(tm_w, p);
+  kern<<<sms, kThreads, smem_bytes, stream>>>(tm_w, p);
   if (!cuda_ok(cudaGetLastError(), "submconv_xrun_kernel", &st)) return st;
   return SPCONV_OK;
 }

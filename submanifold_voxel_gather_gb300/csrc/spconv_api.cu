@@ -319,7 +319,29 @@ spconv_status spconv_submconv3d_xrun(const void* feats_dev, const int32_t* nmap_
   spconv_status st = spconv::check_device();
   if (st != SPCONV_OK) return st;
   st = spconv::launch_conv_xrun(feats_dev, nmap_dev, slots_dev, slots_capacity, slot_count_dev, w_dev, bias_dev,
-                                out_dev, N, Co, static_cast<cudaStream_t>(stream));
+                                out_dev, N, Co, false, static_cast<cudaStream_t>(stream));
+  return st == SPCONV_OK ? spconv::ok() : st;
+}
+
+spconv_status spconv_submconv3d_dgrad_xrun(const void* dout_dev, const int32_t* nmap_dev, const int32_t* slots_dev,
+                                           int64_t slots_capacity, const int64_t* slot_count_dev,
+                                           const void* w_dev, void* dfeats_dev, int64_t N, int32_t K, int32_t Ci,
+                                           int32_t Co, spconv_dtype dtype, void* stream) {
+  if (N < 1 || N >= (int64_t{1} << 30)) return fail(SPCONV_ERR_INVALID_ARG, "N must be in [1, 2^30)");
+  if (dtype != SPCONV_BF16 || K != 27 || Co != 128 || Ci < 16 || Ci > 128 || Ci % 16 != 0)
+    return fail(SPCONV_ERR_UNSUPPORTED,
+                "the x-run input gradient takes bf16, K = 27, Co = 128 and Ci in [16, 128], a multiple of 16");
+  if (dout_dev == nullptr || nmap_dev == nullptr || slots_dev == nullptr || slot_count_dev == nullptr ||
+      w_dev == nullptr || dfeats_dev == nullptr)
+    return fail(SPCONV_ERR_INVALID_ARG, "dout, nmap, slots, slot_count, w and dfeats must be non-NULL");
+  if (!spconv::aligned(dout_dev, 16) || !spconv::aligned(w_dev, 16) || !spconv::aligned(dfeats_dev, 16) ||
+      !spconv::aligned(nmap_dev, 4) || !spconv::aligned(slots_dev, 4) || !spconv::aligned(slot_count_dev, 8))
+    return fail(SPCONV_ERR_INVALID_ARG, "misaligned pointer");
+  if (slots_capacity < 1) return fail(SPCONV_ERR_INVALID_ARG, "slots_capacity must be >= 1");
+  spconv_status st = spconv::check_device();
+  if (st != SPCONV_OK) return st;
+  st = spconv::launch_conv_xrun(dout_dev, nmap_dev, slots_dev, slots_capacity, slot_count_dev, w_dev, nullptr,
+                                dfeats_dev, N, Ci, true, static_cast<cudaStream_t>(stream));
   return st == SPCONV_OK ? spconv::ok() : st;
 }
 

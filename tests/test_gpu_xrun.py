@@ -129,3 +129,25 @@ def test_xrun_conv_workload_sample(sv, oracle_mod, workload):
                                 threads=oracle_mod.host_threads())
     got = to_f64(out[torch.from_numpy(rows).cuda()])
     assert_within(got, ref, sabs, "bf16")
+
+
+@pytest.mark.parametrize("ci", [16, 64, 128])
+@pytest.mark.parametrize("name", ["random", "dense", "line", "isolated", "shuffled"])
+def test_xrun_dgrad_matches_oracle_and_plain(sv, oracle_mod, name, ci):
+    """Input gradient over the layout: Co = 128 reduced channels, Ci output
+    channels; against the oracle's scatter sum and the plain input gradient."""
+    import torch
+    coords = shapes()[name]
+    n = len(coords)
+    nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    dout = W.values(ci + n, 21, (n, 128), "bf16")
+    w = W.values(ci + n, 22, (27, ci, 128), "bf16", 1.0 / np.sqrt(27 * 128))
+    _, nm, slots, count = gpu_layout(sv, coords, nmap)
+    d, ww = torch_storage(dout, "bf16"), torch_storage(w, "bf16")
+    got = sv.submconv3d_dgrad_xrun(d, nm, slots, count, ww)
+    plain = sv.submconv3d_dgrad(d, nm, ww)
+    sv.device_status()
+    ref, dabs = oracle_mod.dgrad(dout, nmap, w, "bf16", threads=oracle_mod.host_threads())
+    assert_within(to_f64(got), ref, dabs, "bf16")
+    assert bool((got.float() == plain.float()).all())
+
