@@ -42,8 +42,11 @@ UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 DOMINANT_KERNEL = "submconv_tc_kernel<256, 1, 1, 0, 0>"
+XRUN_KERNEL = "submconv_xrun_kernel"
 KERNEL_SOURCES = ("submanifold_voxel_gather_gb300/csrc/conv_tc.cu",
                   "submanifold_voxel_gather_gb300/csrc/ptx.cuh")
+XRUN_SOURCES = ("submanifold_voxel_gather_gb300/csrc/conv_xrun.cu",
+                "submanifold_voxel_gather_gb300/csrc/ptx.cuh")
 
 
 def parse_args():
@@ -55,6 +58,9 @@ def parse_args():
     ap.add_argument("--workload", default="decoder")
     ap.add_argument("--layer", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--xrun", action="store_true",
+                    help="run the conv over the x-run slot layout (row-shifted operands); "
+                         "the layout is built in each step after the map")
     ap.add_argument("--no-numa-bind", action="store_true",
                     help="allocate the end-to-end pinned buffers without placing them near the GPU")
     ap.add_argument("--e2e-slots", type=int, default=3,
@@ -166,24 +172,24 @@ def peaks():
         return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(kernel=DOMINANT_KERNEL):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in (XRUN_SOURCES if kernel == XRUN_KERNEL else KERNEL_SOURCES):
         with open(os.path.join(ROOT, rel), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
-def recorded_traffic(workload):
+def recorded_traffic(workload, kernel=DOMINANT_KERNEL):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
-            rec = json.load(fh).get(DOMINANT_KERNEL, {})
+            rec = json.load(fh).get(kernel, {})
     except (OSError, ValueError):
         return None
-    if rec.get("source_sha256") != kernel_source_hash() or rec.get("workload") != workload:
+    if rec.get("source_sha256") != kernel_source_hash(kernel) or rec.get("workload") != workload:
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -550,9 +556,28 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     tf = "tf32" if dtype == "tf32" else None
 
+    xrun = None
+    if args.xrun:
+        cap = int(sv.load_library().spconv_xrun_slot_capacity(n))
+        xrun = {"slots": torch.empty(cap, dtype=torch.int32, device=dev),
+                "count": torch.empty(1, dtype=torch.int64, device=dev),
+                "ws": torch.empty(int(sv.load_library().spconv_xrun_workspace_size(n)), dtype=torch.uint8,
+                                  device=dev)}
+
+    def layout(c, nm, x, stream=None):
+        if x is not None:
+            sv.xrun_layout(c, nm, slots=x["slots"], slot_count=x["count"], workspace=x["ws"], stream=stream)
+
+    def conv(f, nm, ww, b, o, x, stream=None):
+        if x is not None:
+            sv.submconv3d_xrun(f, nm, x["slots"], x["count"], ww, b, out=o, stream=stream)
+        else:
+            sv.submconv3d(f, nm, ww, b, out=o, dtype=tf, stream=stream)
+
     def step():
         sv.build_nmap(coords, workspace=ws, out=nmap)
-        sv.submconv3d(feats, nmap, w, bias, out=out, dtype=tf)
+        layout(coords, nmap, xrun)
+        conv(feats, nmap, w, bias, out, xrun)
 
     for _ in range(max(args.warmup, 0)):
         step()
@@ -573,8 +598,9 @@ def run_ours(args):
     t_start.record(stream)
     for i in range(args.steps):
         sv.build_nmap(coords, workspace=ws, out=nmap)
+        layout(coords, nmap, xrun)
         ev[i][0].record(stream)
-        sv.submconv3d(feats, nmap, w, bias, out=out, dtype=tf)
+        conv(feats, nmap, w, bias, out, xrun)
         ev[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
@@ -596,13 +622,16 @@ def run_ours(args):
     torch.cuda.reset_peak_memory_stats(dev)
     base = torch.cuda.memory_allocated(dev)
     sv.build_nmap(coords, workspace=ws, out=nmap)
+    layout(coords, nmap, xrun)
     torch.cuda.synchronize(dev)
     during_build = torch.cuda.max_memory_allocated(dev) - base
     torch.cuda.reset_peak_memory_stats(dev)
-    sv.submconv3d(feats, nmap, w, bias, out=out, dtype=tf)
+    conv(feats, nmap, w, bias, out, xrun)
     torch.cuda.synchronize(dev)
     during_conv = torch.cuda.max_memory_allocated(dev) - base
     ws_bytes = ws.numel() * ws.element_size()
+    if xrun is not None:  # the slot layout's buffers are scratch of the step too
+        ws_bytes += sum(v.numel() * v.element_size() for v in xrun.values())
     peak_extra = {"bytes": ws_bytes + max(during_build, during_conv), "build_workspace_bytes": ws_bytes,
                   "allocated_during_build": during_build, "allocated_during_conv": during_conv,
                   "gather_materialised_bytes": 0,
@@ -648,6 +677,7 @@ def run_ours(args):
                 "w": torch.empty_like(w), "bias": torch.empty_like(bias),
                 "nmap": torch.empty_like(nmap), "ws": torch.empty_like(ws), "out": torch.empty_like(out),
                 "status": torch.full((1,), -99, dtype=torch.int32, device=dev),
+                "xrun": None if xrun is None else {k: torch.empty_like(v) for k, v in xrun.items()},
                 "h_out": torch.empty((n, co), dtype=feats.dtype).pin_memory()})
         if host_node is not None and host_node["bound"]:
             os.sched_setaffinity(0, prev_cpus)
@@ -660,7 +690,8 @@ def run_ours(args):
                 sl["w"].copy_(h_w, non_blocking=True)
                 sl["bias"].copy_(h_bias, non_blocking=True)
                 sv.build_nmap(sl["coords"], workspace=sl["ws"], out=sl["nmap"], status=sl["status"], stream=st)
-                sv.submconv3d(sl["feats"], sl["nmap"], sl["w"], sl["bias"], out=sl["out"], dtype=tf, stream=st)
+                layout(sl["coords"], sl["nmap"], sl["xrun"], stream=st)
+                conv(sl["feats"], sl["nmap"], sl["w"], sl["bias"], sl["out"], sl["xrun"], stream=st)
                 sl["h_out"].copy_(sl["out"], non_blocking=True)
 
         main = torch.cuda.current_stream(dev)
@@ -716,8 +747,9 @@ def run_ours(args):
     comp_bytes = n * ci * elem + n * co * elem + 4 * k * n + k * ci * co * elem + co * elem
     t_roof_ms = max(flops / (bf16_peak * 1e12), comp_bytes / (hbm_peak * 1e9)) * 1e3
     roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
-                "frac": achieved / bf16_peak, "traffic": recorded_traffic(args.workload),
-                "kernel": DOMINANT_KERNEL, "peak_source": f"{peak_kind} bf16 dense (burst)",
+                "frac": achieved / bf16_peak,
+                "traffic": recorded_traffic(args.workload, XRUN_KERNEL if args.xrun else DOMINANT_KERNEL),
+                "kernel": XRUN_KERNEL if args.xrun else DOMINANT_KERNEL, "peak_source": f"{peak_kind} bf16 dense (burst)",
                 "algorithmic_flops_per_launch": flops, "conv_ms": conv_avg_ms,
                 "compulsory_bytes": comp_bytes, "t_roof_ms": t_roof_ms,
                 "frac_of_roofline": t_roof_ms / conv_avg_ms}
@@ -765,7 +797,8 @@ def run_ours(args):
         # per step: the map build's six kernels (flag reset, range/order
         # check, table clear, insert, row query, voxel-hash query: the path
         # not taken returns at once) and one conv launch (Co <= 256)
-        "gpu_launches": (6 + (co + 255) // 256) * args.steps,
+        # (with --xrun: three layout kernels and one conv launch)
+        "gpu_launches": ((6 + 3 + 1) if args.xrun else (6 + (co + 255) // 256)) * args.steps,
         "clocks": clocks,
         "generation_s": gen_s,
         **({"per_config": per_config} if per_config is not None else {}),

@@ -342,6 +342,83 @@ spconv_status spconv_submconv3d_ordered(const void* feats_dev, const int32_t* nm
                                         int32_t Ci, int32_t Co, spconv_dtype dtype, void* stream);
 
 /*
+ * x-run slot layout for spconv_submconv3d_xrun.
+ *
+ * A run is a maximal sequence of consecutive voxel indices whose cells are
+ * consecutive in x on one (z, y) line.  The layout lists the voxels in index
+ * order as slots, with separator slots between runs, so that for every voxel
+ * slot s and dx in {-1, 0, +1}, slot s + dx stands for the cell (z, y, x + dx).
+ * A separator stands for the cell just outside its run.  Slot codes (int32):
+ * n >= 0 is voxel n; -2 - 2n is the cell right of voxel n (a run end);
+ * -3 - 2n is the cell left of voxel n (a run start).  Between two runs there
+ * is one separator when the first run's right cells and the next run's left
+ * cells have the same map entries for all nine (dz, dy), else two.  Any
+ * voxel order gives a valid layout; sorted (z, y, x) order gives long runs.
+ *
+ *  coords_dev      (N, 3) int32 (z, y, x), device.
+ *  nmap_dev        (K, N) int32 map built from these coordinates with the
+ *                  default lexicographic 3x3x3 offsets (K = 27).
+ *  slots_dev       int32, device, written: S slot codes.
+ *  slots_capacity  entries of slots_dev, >= spconv_xrun_slot_capacity(N)
+ *                  (3N + 1, the most a layout can need).
+ *  slot_count_dev  (1,) int64, device, written: S.
+ *  workspace_dev   device scratch of >= spconv_xrun_workspace_size(N)
+ *                  bytes, 8-byte aligned.
+ *
+ * Asynchronous on `stream`; no allocation.  Errors: SPCONV_ERR_INVALID_ARG
+ * (N outside [1, 2^30), NULL or misaligned pointers, small capacity),
+ * SPCONV_ERR_UNSUPPORTED (K != 27), SPCONV_ERR_WORKSPACE.
+ */
+size_t spconv_xrun_workspace_size(int64_t N);
+int64_t spconv_xrun_slot_capacity(int64_t N);
+spconv_status spconv_xrun_layout(const int32_t* coords_dev, const int32_t* nmap_dev, int64_t N, int32_t K,
+                                 int32_t* slots_dev, int64_t slots_capacity, int64_t* slot_count_dev,
+                                 void* workspace_dev, size_t workspace_bytes, void* stream);
+
+/*
+ * spconv_submconv3d over an x-run slot layout (spconv_xrun_layout).  For
+ * each (dz, dy) a 256-slot tile gathers one operand of 258 rows (the
+ * neighbour rows of the slots from one before the tile to one after it) and
+ * reads its three dx offsets as the same rows shifted by one: a tile gathers
+ * 9 x 258 rows instead of 27 x 256.  Separator slots cost MMA work; their
+ * outputs are dropped.  Same sum as spconv_submconv3d, within the same
+ * tolerance (products in bf16, fp32 accumulation, one rounding to bf16 after
+ * the bias); the order of the fp32 additions differs.
+ *
+ *  slots_dev, slot_count_dev  from spconv_xrun_layout on the same map; the
+ *                             kernel reads S from slot_count_dev and clamps
+ *                             it to slots_capacity (the entries of
+ *                             slots_dev), so no read leaves the buffer.
+ *                             Slot codes naming no voxel of [0, N) are
+ *                             treated as empty.
+ *  dtype                      SPCONV_BF16 only; K = 27, Ci = 128, Co a
+ *                             multiple of 16 in [16, 128].
+ *
+ * Other arguments, layouts and errors as spconv_submconv3d.  Other shapes
+ * return SPCONV_ERR_UNSUPPORTED.
+ */
+spconv_status spconv_submconv3d_xrun(const void* feats_dev, const int32_t* nmap_dev, const int32_t* slots_dev,
+                                     int64_t slots_capacity, const int64_t* slot_count_dev, const void* w_dev,
+                                     const void* bias_dev, void* out_dev, int64_t N, int32_t K, int32_t Ci,
+                                     int32_t Co, spconv_dtype dtype, void* stream);
+
+/*
+ * spconv_submconv3d_dgrad over an x-run slot layout: dfeats (N, Ci) from
+ * dout (N, Co), dfeats[n] = sum_k dout[nmap[k, n]] . w[K-1-k]^T (the map of
+ * the 3x3x3 offsets is symmetric), with the row-shifted operands of
+ * spconv_submconv3d_xrun gathered from dout.
+ *
+ *  dtype  SPCONV_BF16 only; K = 27, Co = 128 (the reduced channels), Ci a
+ *         multiple of 16 in [16, 128] (the output channels).
+ *
+ * Other arguments as spconv_submconv3d_xrun and spconv_submconv3d_dgrad.
+ */
+spconv_status spconv_submconv3d_dgrad_xrun(const void* dout_dev, const int32_t* nmap_dev, const int32_t* slots_dev,
+                                           int64_t slots_capacity, const int64_t* slot_count_dev,
+                                           const void* w_dev, void* dfeats_dev, int64_t N, int32_t K, int32_t Ci,
+                                           int32_t Co, spconv_dtype dtype, void* stream);
+
+/*
  * Wait for `stream`, then read and clear the current device's sticky kernel
  * error word.  Returns SPCONV_OK if no kernel of this library has reported
  * an internal error since the last call, else SPCONV_ERR_DEVICE with the

@@ -24,6 +24,7 @@ import numpy as np
 __all__ = [
     "SpconvError", "load_library", "library_path", "version", "workspace_size", "build_nmap",
     "submconv3d", "submconv3d_dgrad", "submconv3d_wgrad", "tile_order", "count_valid_pairs",
+    "xrun_layout", "submconv3d_xrun", "submconv3d_dgrad_xrun",
     "device_status",
     "default_offsets", "ACTIVATIONS",
     "F32", "TF32", "BF16",
@@ -94,6 +95,18 @@ def load_library() -> ctypes.CDLL:
         lib.spconv_submconv3d_ordered.restype = ctypes.c_int
         lib.spconv_tile_order.argtypes = [vp, i64, i32, vp, vp]
         lib.spconv_tile_order.restype = ctypes.c_int
+        lib.spconv_xrun_workspace_size.argtypes = [i64]
+        lib.spconv_xrun_workspace_size.restype = ctypes.c_size_t
+        lib.spconv_xrun_slot_capacity.argtypes = [i64]
+        lib.spconv_xrun_slot_capacity.restype = i64
+        lib.spconv_xrun_layout.argtypes = [vp, vp, i64, i32, vp, i64, vp, vp, ctypes.c_size_t, vp]
+        lib.spconv_xrun_layout.restype = ctypes.c_int
+        lib.spconv_submconv3d_xrun.argtypes = [vp, vp, vp, i64, vp, vp, vp, vp, i64, i32, i32, i32,
+                                               ctypes.c_int, vp]
+        lib.spconv_submconv3d_xrun.restype = ctypes.c_int
+        lib.spconv_submconv3d_dgrad_xrun.argtypes = [vp, vp, vp, i64, vp, vp, vp, i64, i32, i32, i32,
+                                                     ctypes.c_int, vp]
+        lib.spconv_submconv3d_dgrad_xrun.restype = ctypes.c_int
         lib.spconv_count_valid_pairs.argtypes = [vp, i64, i32, vp, vp]
         lib.spconv_count_valid_pairs.restype = ctypes.c_int
         lib.spconv_device_status.argtypes = [vp]
@@ -333,6 +346,95 @@ def tile_order(nmap, out=None, stream=None):
         if tuple(out.shape) != (n,):
             raise ValueError("out must have shape (N,)")
     _check(load_library().spconv_tile_order(_ptr(nmap), n, k, _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def xrun_layout(coords, nmap, slots=None, slot_count=None, workspace=None, stream=None):
+    """x-run slot layout for ``submconv3d_xrun`` (spconv_xrun_layout): returns
+    (slots, slot_count), an int32 CUDA tensor of spconv_xrun_slot_capacity(N)
+    entries whose first S hold the slot codes, and a (1,) int64 CUDA tensor
+    holding S.  ``nmap`` must come from the default 3x3x3 offsets."""
+    torch = _torch()
+    _require_cuda(coords, "coords", torch.int32)
+    _require_cuda(nmap, "nmap", torch.int32)
+    k, n = nmap.shape
+    if tuple(coords.shape) != (n, 3):
+        raise ValueError("coords must have shape (N, 3) matching nmap (K, N)")
+    lib = load_library()
+    cap = int(lib.spconv_xrun_slot_capacity(n))
+    if slots is None:
+        slots = torch.empty(cap, dtype=torch.int32, device=nmap.device)
+    else:
+        _require_cuda(slots, "slots", torch.int32)
+    if slot_count is None:
+        slot_count = torch.empty(1, dtype=torch.int64, device=nmap.device)
+    else:
+        _require_cuda(slot_count, "slot_count", torch.int64)
+    wbytes = int(lib.spconv_xrun_workspace_size(n))
+    if workspace is None:
+        workspace = torch.empty(wbytes, dtype=torch.uint8, device=nmap.device)
+    else:
+        _require_cuda(workspace, "workspace", torch.uint8)
+    _check(lib.spconv_xrun_layout(_ptr(coords), _ptr(nmap), n, k, _ptr(slots), slots.numel(), _ptr(slot_count),
+                                  _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+    return slots, slot_count
+
+
+def submconv3d_xrun(feats, nmap, slots, slot_count, w, bias=None, out=None, stream=None):
+    """``submconv3d`` over an x-run slot layout from ``xrun_layout``
+    (spconv_submconv3d_xrun): bf16, K = 27, Ci = 128, Co <= 128.  Returns out
+    (N, Co)."""
+    torch = _torch()
+    _require_cuda(feats, "feats", torch.bfloat16)
+    _require_cuda(nmap, "nmap", torch.int32)
+    _require_cuda(slots, "slots", torch.int32)
+    _require_cuda(slot_count, "slot_count", torch.int64)
+    _require_cuda(w, "w", torch.bfloat16)
+    if feats.dim() != 2 or w.dim() != 3 or nmap.dim() != 2:
+        raise ValueError("expected feats (N, Ci), nmap (K, N), w (K, Ci, Co)")
+    n, ci = feats.shape
+    k, co = w.shape[0], w.shape[2]
+    if tuple(nmap.shape) != (k, n) or w.shape[1] != ci:
+        raise ValueError("shapes of feats, nmap and w do not agree")
+    if bias is not None:
+        _require_cuda(bias, "bias", torch.bfloat16)
+    if out is None:
+        out = torch.empty((n, co), dtype=feats.dtype, device=feats.device)
+    else:
+        _require_cuda(out, "out", feats.dtype)
+        if tuple(out.shape) != (n, co):
+            raise ValueError("out must have shape (N, Co)")
+    _check(load_library().spconv_submconv3d_xrun(_ptr(feats), _ptr(nmap), _ptr(slots), slots.numel(),
+                                                 _ptr(slot_count), _ptr(w), _ptr(bias), _ptr(out), n, k, ci, co,
+                                                 BF16, _stream_handle(stream)))
+    return out
+
+
+def submconv3d_dgrad_xrun(dout, nmap, slots, slot_count, w, out=None, stream=None):
+    """``submconv3d_dgrad`` over an x-run slot layout from ``xrun_layout``
+    (spconv_submconv3d_dgrad_xrun): bf16, K = 27, Co = 128, Ci <= 128.
+    Returns dfeats (N, Ci)."""
+    torch = _torch()
+    _require_cuda(dout, "dout", torch.bfloat16)
+    _require_cuda(nmap, "nmap", torch.int32)
+    _require_cuda(slots, "slots", torch.int32)
+    _require_cuda(slot_count, "slot_count", torch.int64)
+    _require_cuda(w, "w", torch.bfloat16)
+    if dout.dim() != 2 or w.dim() != 3 or nmap.dim() != 2:
+        raise ValueError("expected dout (N, Co), nmap (K, N), w (K, Ci, Co)")
+    n, co = dout.shape
+    k, ci = w.shape[0], w.shape[1]
+    if tuple(nmap.shape) != (k, n) or w.shape[2] != co:
+        raise ValueError("shapes of dout, nmap and w do not agree")
+    if out is None:
+        out = torch.empty((n, ci), dtype=dout.dtype, device=dout.device)
+    else:
+        _require_cuda(out, "out", dout.dtype)
+        if tuple(out.shape) != (n, ci):
+            raise ValueError("out must have shape (N, Ci)")
+    _check(load_library().spconv_submconv3d_dgrad_xrun(_ptr(dout), _ptr(nmap), _ptr(slots), slots.numel(),
+                                                       _ptr(slot_count), _ptr(w), _ptr(out), n, k, ci, co, BF16,
+                                                       _stream_handle(stream)))
     return out
 
 

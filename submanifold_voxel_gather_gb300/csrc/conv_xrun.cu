@@ -1,0 +1,636 @@
+// Row-shifted submanifold convolution over an x-run slot layout (xrun.cu).
+//
+// Computes the same sum as conv_tc.cu,
+//
+//     out[n, co] = bias[co] + sum_k sum_ci feats[nmap[k, n], ci] * w[k, ci, co]
+//
+// (page "sparse_conv_metal.py", trellis-2-mrp-mlx: module docstring formula,
+// kernel-body sentinel skip, wrapper bias), for the lexicographic 3x3x3
+// offsets, Ci = 128 and Co <= 128, in bf16 with fp32 accumulation.
+//
+// Tiles are 256 consecutive slots of the layout.  For each (dz, dy) group
+// of offsets a tile gathers one operand G of 258 rows: the group's neighbour
+// row of every slot from one before the tile to one after it (a voxel slot
+// reads nmap[(dz, dy, 0), n]; a separator reads the cell just outside its
+// run, nmap[(dz, dy, +-1), n]).  The three offsets (dz, dy, dx) of the group
+// are then MMAs on G started 0, 1 or 2 rows in: slot s + dx always stands for
+// the cell x + dx of slot s's line.  So a tile gathers 9 x 258 rows instead
+// of 27 x 256, and the MMAs run on the same shared-memory rows three times.
+// Separator slots cost MMA work, and their outputs are dropped.
+//
+// Warp roles as in conv_tc.cu (persistent CTA per SM, 384 threads):
+//   warp 2     loader: per (tile, group) the 258 gathered row indices into a
+//              shared-memory ring, with a ballot flag when any is valid
+//              (groups with none are skipped);
+//   warps 8-11 gather producers: cp.async of G's rows (two 64-channel chunks,
+//              K-major, 128-byte swizzle) into two G stages;
+//   warp 0     weight producer: w[k]'s chunks by tiled TMA into a ring of
+//              four 16 KB slots, with the per-slot metadata;
+//   warp 1     MMA issuer: per kept group, 3 offsets x 2 chunks x 4 MMAs of
+//              M = 128 channels, N = 256 slots, K = 16, fp32 in tensor memory
+//              (two accumulator buffers);
+//   warps 4-7  epilogue: + bias, one rounding to bf16, rows of voxel slots
+//              stored, separator rows dropped.
+// Every mbarrier wait is bounded; on timeout the kernel records an error bit,
+// drains its own loads and MMAs, frees its tensor memory and returns.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace spconv {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kTileN = 256;                   // slots per tile (MMA N)
+constexpr int kGRows = kTileN + 2;            // gathered rows: one halo row each side
+constexpr int kGRowsAlloc = 264;              // rounded up to whole 8-row swizzle atoms
+constexpr int kGroups = 9;                    // (dz, dy) groups of the 3x3x3 offsets
+constexpr int kChunks = 2;                    // 64-channel chunks of Ci = 128
+constexpr uint32_t kGChunkBytes = kGRowsAlloc * 128u;           // 33,792 B (33 x 1024)
+constexpr uint32_t kGStageBytes = kChunks * kGChunkBytes;       // 67,584 B
+constexpr int kGStages = 2;
+constexpr uint32_t kWSlotBytes = 128u * 128u;                   // one offset's chunk: 16 KB
+constexpr int kWSlots = 4;
+constexpr int kXRing = 8;                     // loader ring rows
+constexpr int kRingRow = kGRowsAlloc;         // int32 entries per ring row
+constexpr int kProducerWarp0 = 8;
+constexpr int kProducerThreads = 128;
+constexpr int kEpilogueWarp0 = 4;
+constexpr uint64_t kAStepUnits = (16 * 128) >> 4;   // one K step of channel-major weights
+constexpr uint64_t kBStepUnits = (16 * 2) >> 4;     // one K step of K-major rows
+// The B descriptor of an operand shifted by dxi rows in its 1024-byte-aligned
+// chunk (128-byte swizzle, so the swizzle pattern repeats every 8 rows):
+//   0: start address + dxi * 128, base-offset field 0;
+//   1: start address + dxi * 128, base-offset field (start >> 7) & 7;
+//   2: start address on the chunk's row 0, base-offset field dxi.
+constexpr int kShiftMode = 1;
+
+enum : uint32_t { kMetaFirst = 1u, kMetaEnd = 2u };
+
+struct XrParams {
+  const __nv_bfloat16* feats;
+  const int32_t* nmap;
+  const int32_t* slots;
+  const int64_t* slot_count;
+  int64_t slots_capacity;  // entries of slots: S is clamped to it
+  const __nv_bfloat16* bias;
+  __nv_bfloat16* out;
+  int64_t n;
+  int32_t co;        // row stride of out and weights' Co
+  int32_t co_count;  // channels computed (== co, <= 128)
+  uint32_t idesc;
+  uint32_t off_g;
+  uint32_t off_w;
+  uint32_t off_ring;
+  uint32_t off_stage_out;
+  uint32_t off_bias;
+  uint32_t off_meta;
+  uint32_t off_bars;
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0u;
+}
+
+// Slot code of slot s (xrun.cu), or -1 outside [0, S).
+__device__ __forceinline__ int32_t slot_code(const int32_t* slots, int64_t s, int64_t S) {
+  return (s >= 0 && s < S) ? __ldg(slots + s) : -1;
+}
+
+// Gathered row of a slot code for group g (offsets 3g, 3g+1, 3g+2 are
+// dx = -1, 0, +1), or -1.
+__device__ __forceinline__ int32_t group_row(const int32_t* nmap, int64_t n, int32_t code, int g) {
+  int64_t v;
+  int k;
+  if (code >= 0) {
+    v = code;
+    k = 3 * g + 1;
+  } else if (code <= -2) {
+    const int32_t h = -2 - code;
+    v = h >> 1;
+    k = (h & 1) ? 3 * g : 3 * g + 2;
+  } else {
+    return -1;
+  }
+  if (v >= n) return -1;
+  const int32_t e = __ldg(nmap + static_cast<int64_t>(k) * n + v);
+  return (e >= 0 && e < n) ? e : -1;
+}
+
+// Ring position of gathered row r: producer warp r / 64 takes rows 4 j + s
+// (s = r % 4) as 16 consecutive words; rows 256 and 257 follow.
+__device__ __forceinline__ int ring_pos(int r) {
+  return r < kTileN ? (r >> 6) * 64 + (r & 3) * 16 + ((r & 63) >> 2) : r;
+}
+
+// Kept groups: every group with a valid row, and the last group of a tile
+// none of whose groups has one (a tile always has voxel slots, whose own
+// rows are valid in the (0, 0) group, so this is only a safeguard).
+__device__ __forceinline__ bool issue_group(uint32_t flag, int g, bool issued) {
+  return flag != 0u || (g == kGroups - 1 && !issued);
+}
+
+// kDgrad: input gradient, dfeats[n] = sum_k dout[nmap[k, n]] . w[26 - k]^T
+// (the map is symmetric); the gathered rows are dout's (Co = 128 reduced
+// channels) and the weights of offset k are w[26 - k] read from the forward
+// layout as a K-major operand, as in conv_tc.cu.
+template <bool kDgrad>
+__global__ void __launch_bounds__(kThreads, 1)
+    submconv_xrun_kernel(const __grid_constant__ CUtensorMap tm_w, const XrParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+
+  int32_t* ring = reinterpret_cast<int32_t*>(smem + p.off_ring);
+  __nv_bfloat16* stage_out = reinterpret_cast<__nv_bfloat16*>(smem + p.off_stage_out);
+  float* bias_s = reinterpret_cast<float*>(smem + p.off_bias);
+  uint32_t* wmeta = reinterpret_cast<uint32_t*>(smem + p.off_meta);
+  uint32_t* ring_flag = wmeta + kWSlots;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bars);
+  uint64_t* gfull = bars;
+  uint64_t* gempty = gfull + kGStages;
+  uint64_t* wfull = gempty + kGStages;
+  uint64_t* wempty = wfull + kWSlots;
+  uint64_t* ring_full = wempty + kWSlots;
+  uint64_t* ring_empty = ring_full + kXRing;
+  uint64_t* tmem_full = ring_empty + kXRing;
+  uint64_t* tmem_empty = tmem_full + 2;
+  uint64_t* drain = tmem_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint32_t* consumed_holder = tmem_holder + 1;
+  uint32_t* fills_holder = tmem_holder + 2;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < kGStages; ++s) {
+      mbar_init(smem_addr(&gfull[s]), kProducerThreads);
+      mbar_init(smem_addr(&gempty[s]), 1);
+    }
+    for (int s = 0; s < kWSlots; ++s) {
+      mbar_init(smem_addr(&wfull[s]), 1);
+      mbar_init(smem_addr(&wempty[s]), 1);
+    }
+    for (int i = 0; i < kXRing; ++i) {
+      mbar_init(smem_addr(&ring_full[i]), 32);
+      mbar_init(smem_addr(&ring_empty[i]), 32 + kProducerThreads);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&tmem_full[i]), 1);
+      mbar_init(smem_addr(&tmem_empty[i]), 4);
+    }
+    mbar_init(smem_addr(drain), 1);
+    *consumed_holder = 0;
+    *fills_holder = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  if (warp == 3) {
+    for (int j = lane; j < 128; j += 32)
+      bias_s[j] = (p.bias != nullptr && j < p.co_count) ? __bfloat162float(p.bias[j]) : 0.0f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int64_t n_rows = p.n;
+  const int64_t S = max(int64_t{0}, min(__ldg(p.slot_count), p.slots_capacity));
+  const int64_t num_tiles = (S + kTileN - 1) / kTileN;
+
+  if (warp == 2) {
+    // ------------------------------------------------------ loader
+    uint32_t e = 0, ephase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      const int64_t s0 = t * kTileN;
+      int32_t code[9];  // gathered rows r = lane + 32 j of the tile (r < 258)
+#pragma unroll
+      for (int j = 0; j < 9; ++j) {
+        const int r = static_cast<int>(lane) + 32 * j;
+        code[j] = r < kGRows ? slot_code(p.slots, s0 - 1 + r, S) : -1;
+      }
+      for (int g = 0; g < kGroups && ok; ++g) {
+        int32_t v[9];
+#pragma unroll
+        for (int j = 0; j < 9; ++j) v[j] = group_row(p.nmap, n_rows, code[j], g);
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ring_empty[e]), ephase ^ 1))) {
+          ok = false;
+          break;
+        }
+        bool any = false;
+#pragma unroll
+        for (int j = 0; j < 9; ++j) {
+          const int r = static_cast<int>(lane) + 32 * j;
+          if (r < kGRows) {
+            ring[e * kRingRow + ring_pos(r)] = v[j];
+            any |= v[j] >= 0;
+          }
+        }
+        const uint32_t ballot = __ballot_sync(0xffffffffu, any);
+        if (lane == 0) ring_flag[e] = ballot != 0u ? 1u : 0u;
+        mbar_arrive(smem_addr(&ring_full[e]));
+        if (++e == kXRing) {
+          e = 0;
+          ephase ^= 1;
+        }
+      }
+    }
+  } else if (warp >= kProducerWarp0) {
+    // ------------------------------------------------------ gather producers
+    const uint32_t aw = warp - kProducerWarp0;
+    const int sub_row = static_cast<int>(lane >> 3);
+    const int chunk16 = static_cast<int>(lane & 7);
+    const char* feats = reinterpret_cast<const char*>(p.feats);
+    const uint32_t dst_lane = (aw * 64u + static_cast<uint32_t>(sub_row)) * 128u;
+    const uint32_t sw_even = static_cast<uint32_t>(chunk16 ^ sub_row) << 4;
+    const uint32_t sw_odd = static_cast<uint32_t>(chunk16 ^ (sub_row + 4)) << 4;
+    // warp 0 also gathers rows 256 + sub_row (rows 258 and 259 are padding,
+    // zero-filled and never read); row & 7 == sub_row there
+    const uint32_t dst_extra = 256u * 128u + static_cast<uint32_t>(sub_row) * 128u + sw_even;
+    uint32_t stage = 0, st_phase = 0, e = 0, ephase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      bool issued = false;
+      for (int g = 0; g < kGroups && ok; ++g) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ring_full[e]), ephase))) {
+          ok = false;
+          break;
+        }
+        const bool go = issue_group(ring_flag[e], g, issued);
+        uint32_t vi[16];
+        uint32_t valid_bits = 0;
+        uint32_t xi = 0;
+        bool x_ok = false;
+        if (go) {
+          const int4* ip = reinterpret_cast<const int4*>(ring + e * kRingRow + static_cast<int>(aw) * 64 + sub_row * 16);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int4 v4 = ip[q];
+            const int32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              vi[4 * q + h] = w4[h] >= 0 ? static_cast<uint32_t>(w4[h]) : 0u;
+              valid_bits |= (w4[h] >= 0 ? 1u : 0u) << (4 * q + h);
+            }
+          }
+          if (aw == 0 && sub_row < 2) {
+            const int32_t xv = ring[e * kRingRow + kTileN + sub_row];
+            x_ok = xv >= 0;
+            xi = x_ok ? static_cast<uint32_t>(xv) : 0u;
+          }
+        }
+        mbar_arrive(smem_addr(&ring_empty[e]));
+        if (++e == kXRing) {
+          e = 0;
+          ephase ^= 1;
+        }
+        if (!go) continue;
+        issued = true;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&gempty[stage]), st_phase ^ 1))) {
+          ok = false;
+          break;
+        }
+        const uint32_t g_base = smem_addr(smem + p.off_g) + stage * kGStageBytes;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+          const char* chunk_base = feats + c * 128 + chunk16 * 16;
+          const uint32_t f_dst = g_base + c * kGChunkBytes + dst_lane;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            cp_async_16<false>(f_dst + 512u * j + ((j & 1) ? sw_odd : sw_even),
+                               chunk_base + static_cast<uint64_t>(vi[j]) * 256u, ((valid_bits >> j) & 1u) << 4);
+          if (aw == 0)
+            cp_async_16<false>(g_base + c * kGChunkBytes + dst_extra, chunk_base + static_cast<uint64_t>(xi) * 256u,
+                               x_ok ? 16u : 0u);
+        }
+        cp_async_arrive_noinc(smem_addr(&gfull[stage]));
+        if (++stage == kGStages) {
+          stage = 0;
+          st_phase ^= 1;
+        }
+      }
+    }
+    cp_async_wait_all();
+  } else if (warp == 0) {
+    // ------------------------------------------------------ weight producer
+    uint32_t ws = 0, wphase = 0, e = 0, ephase = 0, fills = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      bool issued = false;
+      for (int g = 0; g < kGroups && ok; ++g) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ring_full[e]), ephase))) {
+          ok = false;
+          break;
+        }
+        const bool go = issue_group(ring_flag[e], g, issued);
+        __syncwarp();
+        mbar_arrive(smem_addr(&ring_empty[e]));
+        if (++e == kXRing) {
+          e = 0;
+          ephase ^= 1;
+        }
+        if (!go) continue;
+        for (int dxi = 0; dxi < 3 && ok; ++dxi) {
+          const int k = 3 * g + dxi;
+          for (int c = 0; c < kChunks; ++c) {
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&wempty[ws]), wphase ^ 1))) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = smem_addr(&wfull[ws]);
+            if (lane == 0) {
+              wmeta[ws] = (dxi == 0 && c == 0 && !issued) ? kMetaFirst : 0u;
+              mbar_arrive_expect_tx(fb, kWSlotBytes);
+            }
+            __syncwarp();
+            if constexpr (!kDgrad) {
+              // w[k] channel-major: two boxes of 64 output channels x 64
+              // input channels (128-byte swizzle)
+              if (lane < 2)
+                tma_load_3d(smem_addr(smem + p.off_w) + ws * kWSlotBytes + lane * 8192u, &tm_w,
+                            static_cast<int>(lane) * 64, c * 64, k, fb);
+            } else {
+              // w[26 - k]: 128 forward-ci rows with 64 forward-co entries
+              // each (K-major, 128-byte swizzle), one box
+              if (lane == 0)
+                tma_load_3d(smem_addr(smem + p.off_w) + ws * kWSlotBytes, &tm_w, c * 64, 0, 26 - k, fb);
+            }
+            ++fills;
+            if (++ws == kWSlots) {
+              ws = 0;
+              wphase ^= 1;
+            }
+          }
+        }
+        issued = true;
+      }
+    }
+    // End of work: tells the MMA issuer to close the last tile.
+    if (ok && __all_sync(0xffffffffu, mbar_wait(smem_addr(&wempty[ws]), wphase ^ 1))) {
+      if (lane == 0) {
+        wmeta[ws] = kMetaEnd;
+        mbar_arrive(smem_addr(&wfull[ws]));
+      }
+      ++fills;
+    }
+    if (lane == 0) *fills_holder = fills;
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // weights channel-major (forward) or K-major (input gradient)
+      const uint64_t adesc0 = sw128_desc(smem_addr(smem + p.off_w), kDgrad ? 16u : 8192u, 1024u);
+      constexpr uint64_t a_step = kDgrad ? kBStepUnits : kAStepUnits;
+      const uint32_t g_base = smem_addr(smem + p.off_g);
+      const uint32_t idesc = p.idesc;
+      uint32_t ws = 0, wphase = 0, gs = 0, gphase = 0, consumed = 0, tile_i = 0, buf = 0, acc = 0;
+      uint32_t d_tmem = tmem_base;
+      bool open = false, ok = true;
+      while (ok) {
+        if (!mbar_wait(smem_addr(&wfull[ws]), wphase)) break;
+        tc_fence_after();
+        const uint32_t m = wmeta[ws];
+        if ((m & (kMetaFirst | kMetaEnd)) != 0u && open) {
+          umma_commit(smem_addr(&tmem_full[buf]));
+          ++tile_i;
+          open = false;
+        }
+        if ((m & kMetaEnd) != 0u) {
+          ++consumed;
+          break;
+        }
+        if ((m & kMetaFirst) != 0u) {
+          buf = tile_i & 1u;
+          if (!mbar_wait(smem_addr(&tmem_empty[buf]), ((tile_i >> 1) & 1u) ^ 1u)) break;
+          tc_fence_after();
+          d_tmem = tmem_base + buf * static_cast<uint32_t>(kTileN);
+          open = true;
+          acc = 0;
+        }
+        // the gathered rows were written by cp.async (generic proxy); the
+        // MMA reads them through the async proxy
+        if (!mbar_wait(smem_addr(&gfull[gs]), gphase)) break;
+        fence_proxy_async_smem();
+        tc_fence_after();
+        const uint32_t gaddr = g_base + gs * kGStageBytes;
+        for (int dxi = 0; dxi < 3 && ok; ++dxi) {
+          for (int c = 0; c < kChunks; ++c) {
+            if (dxi != 0 || c != 0) {
+              if (!mbar_wait(smem_addr(&wfull[ws]), wphase)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint64_t ad = adesc0 + ws * (kWSlotBytes >> 4);
+            const uint32_t baddr = gaddr + c * kGChunkBytes + (kShiftMode == 2 ? 0u : static_cast<uint32_t>(dxi) * 128u);
+            uint64_t bd = sw128_desc(baddr, 16u, 1024u);
+            if (kShiftMode == 1) bd |= static_cast<uint64_t>((baddr >> 7) & 7u) << 49;
+            if (kShiftMode == 2) bd |= static_cast<uint64_t>(dxi) << 49;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              umma_f16(d_tmem, ad + ks * a_step, bd + ks * kBStepUnits, idesc, acc);
+              acc = 1;
+            }
+            umma_commit(smem_addr(&wempty[ws]));
+            ++consumed;
+            if (++ws == kWSlots) {
+              ws = 0;
+              wphase ^= 1;
+            }
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_addr(&gempty[gs]));
+        if (++gs == kGStages) {
+          gs = 0;
+          gphase ^= 1;
+        }
+      }
+      *consumed_holder = consumed;
+      umma_commit(smem_addr(drain));
+      mbar_wait(smem_addr(drain), 0);
+    }
+    __syncwarp();
+  } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
+    // ------------------------------------------------------ epilogue
+    const uint32_t sub = warp & 3u;
+    const int et = static_cast<int>(threadIdx.x) - kEpilogueWarp0 * 32;  // 0..127
+    const int chunks_per_row = p.co_count / 8;
+    const int co_l = static_cast<int>(sub) * 32 + static_cast<int>(lane);
+    uint32_t tile_i = 0;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tile_i) {
+      const uint32_t buf = tile_i & 1u;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(smem_addr(&tmem_full[buf]), (tile_i >> 1) & 1u));
+      if (!epi_all(got)) break;
+      tc_fence_after();
+      const int64_t s0 = t * kTileN;
+      const uint32_t tcol = tmem_base + ((sub * 32u) << 16) + buf * static_cast<uint32_t>(kTileN);
+      for (int vc = 0; vc < kTileN / 32; ++vc) {
+        epi_bar();  // the previous chunk's staged rows have been stored
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tcol + vc * 32, v);
+        tmem_ld_wait();
+        if (co_l < p.co_count) {
+          const float b = bias_s[co_l];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) stage_out[i * 128 + co_l] = __float2bfloat16_rn(__uint_as_float(v[i]) + b);
+        }
+        epi_bar();
+        for (int q = et; q < 32 * chunks_per_row; q += 128) {
+          const int r = q / chunks_per_row;
+          const int c8 = q - r * chunks_per_row;
+          const int32_t code = slot_code(p.slots, s0 + vc * 32 + r, S);
+          if (code >= 0 && code < n_rows)
+            *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(code) * p.co + c8 * 8) =
+                *reinterpret_cast<const uint4*>(stage_out + r * 128 + c8 * 8);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&tmem_empty[buf]));
+    }
+  }
+
+  // ---------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0) {
+    // weight loads issued but never consumed exist only after a timed-out
+    // wait: wait (bounded) for them to land before the CTA's memory goes away
+    const uint32_t fills = *fills_holder;
+    for (uint32_t i = *consumed_holder; i < fills; ++i)
+      mbar_wait(smem_addr(&wfull[i % kWSlots]), (i / kWSlots) & 1u);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn xrun_encode_fn(spconv_status* st) {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                                       cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  if (fn == nullptr) *st = fail(SPCONV_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  return fn;
+}
+
+}  // namespace
+
+spconv_status read_and_clear_xrun_device_error(cudaStream_t stream, unsigned int* bits) {
+  spconv_status st = SPCONV_OK;
+  if (!cuda_ok(cudaStreamSynchronize(stream), "cudaStreamSynchronize", &st)) return st;
+  unsigned int mine = 0;
+  const unsigned int zero = 0;
+  if (!cuda_ok(cudaMemcpyFromSymbol(&mine, g_device_error, sizeof(unsigned int)),
+               "cudaMemcpyFromSymbol", &st))
+    return st;
+  if (!cuda_ok(cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned int)),
+               "cudaMemcpyToSymbol", &st))
+    return st;
+  *bits |= mine;
+  return SPCONV_OK;
+}
+
+spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int32_t* slots,
+                               int64_t slots_capacity, const int64_t* slot_count, const void* w,
+                               const void* bias, void* out, int64_t n, int32_t co, bool dgrad,
+                               cudaStream_t stream) {
+  spconv_status st = SPCONV_OK;
+  EncodeTiledFn encode = xrun_encode_fn(&st);
+  if (encode == nullptr) return st;
+  CUtensorMap tm_w;
+  // Weights in their forward (K, Ci_fwd, Co_fwd) layout as a 3-D tensor
+  // (co_fwd, ci_fwd, k).  Forward: Ci_fwd = 128, boxes of 64 output x 64
+  // input channels.  Input gradient: Co_fwd = 128 is reduced and `co` output
+  // channels are Ci_fwd; boxes of 64 forward-co x 128 forward-ci.
+  const cuuint64_t wo = dgrad ? 128u : static_cast<cuuint64_t>(co);  // forward Co
+  const cuuint64_t wi = dgrad ? static_cast<cuuint64_t>(co) : 128u;  // forward Ci
+  cuuint64_t dims[3] = {wo, wi, 27u};
+  cuuint64_t strides[2] = {wo * 2u, wi * wo * 2u};
+  cuuint32_t box[3] = {64u, dgrad ? 128u : 64u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box,
+                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPCONV_ERR_CUDA, "cuTensorMapEncodeTiled(w) failed: " + std::to_string(r));
+
+  XrParams p{};
+  p.feats = static_cast<const __nv_bfloat16*>(feats);
+  p.nmap = nmap;
+  p.slots = slots;
+  p.slot_count = slot_count;
+  p.slots_capacity = slots_capacity;
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.n = n;
+  p.co = co;
+  p.co_count = co;
+  // D f32, A and B bf16, A (weights) channel-major (forward) or K-major
+  // (input gradient), B (rows) K-major, N = 256, M = 128
+  const uint32_t a_mn_major = dgrad ? 0u : 1u;
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major << 15) |
+            ((static_cast<uint32_t>(kTileN) >> 3) << 17) | ((128u >> 4) << 24);
+  uint32_t off = 0;
+  p.off_g = off;
+  off += kGStages * kGStageBytes;
+  p.off_w = off;
+  off += kWSlots * kWSlotBytes;
+  p.off_ring = off;
+  off += kXRing * kRingRow * 4u;
+  p.off_stage_out = off;
+  off += 32u * 128u * 2u;
+  p.off_bias = off;
+  off += 128u * 4u;
+  p.off_meta = off;
+  off += (kWSlots + kXRing) * 4u;
+  off = (off + 7u) & ~7u;
+  p.off_bars = off;
+  off += (2u * kGStages + 2u * kWSlots + 2u * kXRing + 5u) * 8u + 16u;
+  const uint32_t smem_bytes = off + 1024u;  // slack for the 1024-byte alignment
+  if (smem_bytes > 232448u) return fail(SPCONV_ERR_UNSUPPORTED, "x-run conv: shared memory layout too large");
+
+  auto kern = dgrad ? submconv_xrun_kernel<true> : submconv_xrun_kernel<false>;
+  if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes)),
+               "cudaFuncSetAttribute", &st))
+    return st;
+  const int sms = sm_count();
+  if (sms <= 0) return fail(SPCONV_ERR_CUDA, "could not query the SM count");
+  kern<<<sms, kThreads, smem_bytes, stream>>>(tm_w, p);
+  if (!cuda_ok(cudaGetLastError(), "submconv_xrun_kernel", &st)) return st;
+  return SPCONV_OK;
+}
+
+}  // namespace spconv

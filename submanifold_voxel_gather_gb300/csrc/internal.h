@@ -81,5 +81,18 @@ spconv_status launch_wgrad_tc(const void* feats, const void* dout, const int32_t
 // gradient's ORs them in, so call the conv's first.
 spconv_status read_and_clear_device_error(cudaStream_t stream, unsigned int* bits);
 spconv_status read_and_clear_wgrad_device_error(cudaStream_t stream, unsigned int* bits);
+spconv_status read_and_clear_xrun_device_error(cudaStream_t stream, unsigned int* bits);
+
+// ---- x-run slot layout (xrun.cu) and the row-shifted conv (conv_xrun.cu)
+size_t xrun_workspace_bytes(int64_t n);
+int64_t xrun_slot_capacity(int64_t n);
+spconv_status launch_xrun_layout(const int32_t* coords, const int32_t* nmap, int64_t n, int32_t* slots,
+                                 int64_t cap, int64_t* slot_count, void* workspace, cudaStream_t stream);
+// bf16, lexicographic 3x3x3 offsets; 128 reduced channels (forward Ci, or
+// forward Co for the input gradient) and co <= 128 output channels
+spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int32_t* slots,
+                               int64_t slots_capacity, const int64_t* slot_count, const void* w,
+                               const void* bias, void* out, int64_t n, int32_t co, bool dgrad,
+                               cudaStream_t stream);
 
 }  // namespace spconv

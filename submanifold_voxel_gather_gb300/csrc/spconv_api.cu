@@ -275,6 +275,76 @@ spconv_status spconv_tile_order(const int32_t* nmap_dev, int64_t N, int32_t K, i
   return st == SPCONV_OK ? spconv::ok() : st;
 }
 
+size_t spconv_xrun_workspace_size(int64_t N) { return N < 0 ? 0 : spconv::xrun_workspace_bytes(N); }
+
+int64_t spconv_xrun_slot_capacity(int64_t N) { return N < 0 ? 0 : spconv::xrun_slot_capacity(N); }
+
+spconv_status spconv_xrun_layout(const int32_t* coords_dev, const int32_t* nmap_dev, int64_t N, int32_t K,
+                                 int32_t* slots_dev, int64_t slots_capacity, int64_t* slot_count_dev,
+                                 void* workspace_dev, size_t workspace_bytes, void* stream) {
+  if (N < 1 || N >= (int64_t{1} << 30)) return fail(SPCONV_ERR_INVALID_ARG, "N must be in [1, 2^30)");
+  if (K != 27) return fail(SPCONV_ERR_UNSUPPORTED, "the x-run layout needs the 27 lexicographic 3x3x3 offsets");
+  if (coords_dev == nullptr || nmap_dev == nullptr || slots_dev == nullptr || slot_count_dev == nullptr ||
+      workspace_dev == nullptr)
+    return fail(SPCONV_ERR_INVALID_ARG, "coords, nmap, slots, slot_count and workspace must be non-NULL");
+  if (!spconv::aligned(coords_dev, 4) || !spconv::aligned(nmap_dev, 4) || !spconv::aligned(slots_dev, 4) ||
+      !spconv::aligned(slot_count_dev, 8) || !spconv::aligned(workspace_dev, 8))
+    return fail(SPCONV_ERR_INVALID_ARG, "misaligned pointer (coords, nmap, slots: 4 bytes; slot_count, workspace: 8)");
+  if (slots_capacity < spconv::xrun_slot_capacity(N))
+    return fail(SPCONV_ERR_INVALID_ARG, "slots_capacity below spconv_xrun_slot_capacity(N)");
+  if (workspace_bytes < spconv::xrun_workspace_bytes(N))
+    return fail(SPCONV_ERR_WORKSPACE, "workspace smaller than spconv_xrun_workspace_size(N)");
+  spconv_status st = spconv::check_device();
+  if (st != SPCONV_OK) return st;
+  st = spconv::launch_xrun_layout(coords_dev, nmap_dev, N, slots_dev, slots_capacity, slot_count_dev,
+                                  workspace_dev, static_cast<cudaStream_t>(stream));
+  return st == SPCONV_OK ? spconv::ok() : st;
+}
+
+spconv_status spconv_submconv3d_xrun(const void* feats_dev, const int32_t* nmap_dev, const int32_t* slots_dev,
+                                     int64_t slots_capacity, const int64_t* slot_count_dev, const void* w_dev,
+                                     const void* bias_dev, void* out_dev, int64_t N, int32_t K, int32_t Ci,
+                                     int32_t Co, spconv_dtype dtype, void* stream) {
+  if (N < 1 || N >= (int64_t{1} << 30)) return fail(SPCONV_ERR_INVALID_ARG, "N must be in [1, 2^30)");
+  if (dtype != SPCONV_BF16 || K != 27 || Ci != 128 || Co < 16 || Co > 128 || Co % 16 != 0)
+    return fail(SPCONV_ERR_UNSUPPORTED, "the x-run conv takes bf16, K = 27, Ci = 128 and Co in [16, 128], a multiple of 16");
+  if (feats_dev == nullptr || nmap_dev == nullptr || slots_dev == nullptr || slot_count_dev == nullptr ||
+      w_dev == nullptr || out_dev == nullptr)
+    return fail(SPCONV_ERR_INVALID_ARG, "feats, nmap, slots, slot_count, w and out must be non-NULL");
+  if (!spconv::aligned(feats_dev, 16) || !spconv::aligned(w_dev, 16) || !spconv::aligned(out_dev, 16) ||
+      !spconv::aligned(nmap_dev, 4) || !spconv::aligned(slots_dev, 4) || !spconv::aligned(slot_count_dev, 8) ||
+      (bias_dev != nullptr && !spconv::aligned(bias_dev, 2)))
+    return fail(SPCONV_ERR_INVALID_ARG, "misaligned pointer");
+  if (slots_capacity < 1) return fail(SPCONV_ERR_INVALID_ARG, "slots_capacity must be >= 1");
+  spconv_status st = spconv::check_device();
+  if (st != SPCONV_OK) return st;
+  st = spconv::launch_conv_xrun(feats_dev, nmap_dev, slots_dev, slots_capacity, slot_count_dev, w_dev, bias_dev,
+                                out_dev, N, Co, false, static_cast<cudaStream_t>(stream));
+  return st == SPCONV_OK ? spconv::ok() : st;
+}
+
+spconv_status spconv_submconv3d_dgrad_xrun(const void* dout_dev, const int32_t* nmap_dev, const int32_t* slots_dev,
+                                           int64_t slots_capacity, const int64_t* slot_count_dev,
+                                           const void* w_dev, void* dfeats_dev, int64_t N, int32_t K, int32_t Ci,
+                                           int32_t Co, spconv_dtype dtype, void* stream) {
+  if (N < 1 || N >= (int64_t{1} << 30)) return fail(SPCONV_ERR_INVALID_ARG, "N must be in [1, 2^30)");
+  if (dtype != SPCONV_BF16 || K != 27 || Co != 128 || Ci < 16 || Ci > 128 || Ci % 16 != 0)
+    return fail(SPCONV_ERR_UNSUPPORTED,
+                "the x-run input gradient takes bf16, K = 27, Co = 128 and Ci in [16, 128], a multiple of 16");
+  if (dout_dev == nullptr || nmap_dev == nullptr || slots_dev == nullptr || slot_count_dev == nullptr ||
+      w_dev == nullptr || dfeats_dev == nullptr)
+    return fail(SPCONV_ERR_INVALID_ARG, "dout, nmap, slots, slot_count, w and dfeats must be non-NULL");
+  if (!spconv::aligned(dout_dev, 16) || !spconv::aligned(w_dev, 16) || !spconv::aligned(dfeats_dev, 16) ||
+      !spconv::aligned(nmap_dev, 4) || !spconv::aligned(slots_dev, 4) || !spconv::aligned(slot_count_dev, 8))
+    return fail(SPCONV_ERR_INVALID_ARG, "misaligned pointer");
+  if (slots_capacity < 1) return fail(SPCONV_ERR_INVALID_ARG, "slots_capacity must be >= 1");
+  spconv_status st = spconv::check_device();
+  if (st != SPCONV_OK) return st;
+  st = spconv::launch_conv_xrun(dout_dev, nmap_dev, slots_dev, slots_capacity, slot_count_dev, w_dev, nullptr,
+                                dfeats_dev, N, Ci, true, static_cast<cudaStream_t>(stream));
+  return st == SPCONV_OK ? spconv::ok() : st;
+}
+
 spconv_status spconv_submconv3d_ex(const void* feats_dev, const int32_t* nmap_dev,
                                    const void* w_dev, const void* bias_dev,
                                    const void* residual_dev, void* out_dev, int64_t N, int32_t K,
@@ -355,6 +425,8 @@ spconv_status spconv_device_status(void* stream) {
   spconv_status st = spconv::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &bits);
   if (st != SPCONV_OK) return st;
   st = spconv::read_and_clear_wgrad_device_error(static_cast<cudaStream_t>(stream), &bits);
+  if (st != SPCONV_OK) return st;
+  st = spconv::read_and_clear_xrun_device_error(static_cast<cudaStream_t>(stream), &bits);
   if (st != SPCONV_OK) return st;
   if (bits != 0) return fail(SPCONV_ERR_DEVICE, "device error bits 0x" + std::to_string(bits));
   return spconv::ok();

@@ -60,3 +60,35 @@ def oracle_full_map(name):
         _ORACLE_MAPS[name] = (coords, oracle.build_nmap(coords, W.offsets_3x3x3(),
                                                         threads=oracle.host_threads()))
     return _ORACLE_MAPS[name]
+
+
+def layout_reference(coords, nmap):
+    """Slot codes of the x-run layout, from its definition."""
+    n = len(coords)
+    nm = nmap.astype(np.int64)
+    nm[(nm < 0) | (nm >= n)] = n
+    c = coords.astype(np.int64)
+    cont_next = np.zeros(n, bool)
+    cont_next[:-1] = (c[1:, 0] == c[:-1, 0]) & (c[1:, 1] == c[:-1, 1]) & (c[1:, 2] == c[:-1, 2] + 1)
+    idx = np.arange(n)
+    after = np.zeros(n, np.int64)
+    ends = np.nonzero(~cont_next)[0]
+    inner = ends[ends < n - 1]
+    compat = (nm[2::3][:, inner] == nm[0::3][:, inner + 1]).all(axis=0)
+    after[inner] = np.where(compat, 1, 2)
+    after[n - 1] = 1 if (nm[2::3, n - 1] != n).any() else 0
+    before0 = 1 if (nm[0::3, 0] != n).any() else 0
+    cnt = 1 + after
+    cnt[0] += before0
+    pos = np.cumsum(cnt) - cnt
+    vpos = pos.copy()
+    vpos[0] += before0
+    slots = np.full(int(cnt.sum()), -1, np.int64)
+    slots[vpos] = idx
+    if before0:
+        slots[0] = -3
+    a1 = idx[after >= 1]
+    slots[vpos[a1] + 1] = -2 - 2 * a1
+    a2 = idx[after == 2]
+    slots[vpos[a2] + 2] = -3 - 2 * (a2 + 1)
+    return slots.astype(np.int32)

@@ -130,6 +130,43 @@ def test_order_entry_points_validate_without_gpu(lib):
     assert _status(od(None, None, None, None, None, None, 0, 27, 16, 16, 2, None))[0] == 0
 
 
+def test_xrun_entry_points_validate_without_gpu(lib):
+    fake = ctypes.c_void_p(0x100000)  # never dereferenced: validation fails first
+    n = 10
+    cap = lib.spconv_xrun_slot_capacity(n)
+    ws = lib.spconv_xrun_workspace_size(n)
+    assert cap == 3 * n + 1
+    assert ws >= n + 8
+    assert lib.spconv_xrun_slot_capacity(-1) == 0 and lib.spconv_xrun_workspace_size(-1) == 0
+    xl = lib.spconv_xrun_layout
+    assert _status(xl(fake, fake, 0, 27, fake, cap, fake, fake, ws, None))[0] == -1
+    assert _status(xl(fake, fake, 1 << 30, 27, fake, 1 << 32, fake, fake, 1 << 40, None))[0] == -1
+    assert _status(xl(fake, fake, n, 26, fake, cap, fake, fake, ws, None))[0] == -2
+    assert _status(xl(None, fake, n, 27, fake, cap, fake, fake, ws, None))[0] == -1
+    assert _status(xl(fake, fake, n, 27, fake, cap - 1, fake, fake, ws, None))[0] == -1
+    assert _status(xl(fake, fake, n, 27, fake, cap, ctypes.c_void_p(0x100004), fake, ws, None))[0] == -1
+    assert _status(xl(fake, fake, n, 27, fake, cap, fake, fake, ws - 1, None))[0] == -3
+    xc = lib.spconv_submconv3d_xrun
+    assert _status(xc(fake, fake, fake, 31, fake, fake, None, fake, n, 27, 128, 128, 0, None))[0] == -2
+    assert _status(xc(fake, fake, fake, 31, fake, fake, None, fake, n, 27, 64, 128, 2, None))[0] == -2
+    assert _status(xc(fake, fake, fake, 31, fake, fake, None, fake, n, 27, 128, 256, 2, None))[0] == -2
+    assert _status(xc(fake, fake, fake, 31, fake, fake, None, fake, n, 27, 128, 24, 2, None))[0] == -2
+    assert _status(xc(fake, fake, fake, 31, fake, fake, None, fake, n, 125, 128, 128, 2, None))[0] == -2
+    assert _status(xc(fake, fake, None, 31, fake, fake, None, fake, n, 27, 128, 128, 2, None))[0] == -1
+    assert _status(xc(fake, fake, fake, 31, fake, ctypes.c_void_p(0x100008), None, fake, n, 27, 128, 128, 2,
+                      None))[0] == -1
+    assert _status(xc(fake, fake, fake, 31, fake, fake, None, fake, 0, 27, 128, 128, 2, None))[0] == -1
+    assert _status(xc(fake, fake, fake, 0, fake, fake, None, fake, n, 27, 128, 128, 2, None))[0] == -1
+    xd = lib.spconv_submconv3d_dgrad_xrun
+    assert _status(xd(fake, fake, fake, 31, fake, fake, fake, n, 27, 128, 64, 2, None))[0] == -2
+    assert _status(xd(fake, fake, fake, 31, fake, fake, fake, n, 27, 256, 128, 2, None))[0] == -2
+    assert _status(xd(fake, fake, fake, 31, fake, fake, fake, n, 27, 64, 128, 0, None))[0] == -2
+    assert _status(xd(fake, fake, None, 31, fake, fake, fake, n, 27, 64, 128, 2, None))[0] == -1
+    assert _status(xd(fake, fake, fake, 31, fake, ctypes.c_void_p(0x100008), fake, n, 27, 64, 128, 2,
+                      None))[0] == -1
+    assert _status(xd(fake, fake, fake, 0, fake, fake, fake, n, 27, 64, 128, 2, None))[0] == -1
+
+
 def test_python_binding_rejects_cpu_tensors(lib):
     torch = pytest.importorskip("torch")
     with pytest.raises(TypeError):

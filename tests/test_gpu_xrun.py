@@ -1,0 +1,153 @@
+"""x-run slot layout and the row-shifted convolution on the GPU.
+
+The layout is compared entry for entry with its definition written out in
+numpy (runs of consecutive indices with consecutive x on one line; one
+separator between runs whose outer cells have equal map entries in all nine
+(dz, dy) groups, else two; outer separators of the first and last voxel only
+when one of their outer cells is active).  The convolution is compared with
+the oracle's exact sum (|gpu - exact| <= 4e-3 * sum|terms|) and with the
+plain tensor-core convolution, which forms each output's sum in the same
+order and so gives the same values."""
+import numpy as np
+import pytest
+
+import workloads as W
+from helpers import assert_within, layout_reference, sample_rows, to_f64, torch_storage
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import submanifold_voxel_gather_gb300 as mod
+    from submanifold_voxel_gather_gb300 import build
+    build.build()
+    return mod
+
+
+def gpu_layout(sv, coords, nmap):
+    import torch
+    c = torch.from_numpy(np.ascontiguousarray(coords, dtype=np.int32)).cuda()
+    nm = torch.from_numpy(np.ascontiguousarray(nmap, dtype=np.int32)).cuda()
+    slots, count = sv.xrun_layout(c, nm)
+    s = int(count.item())
+    return slots[:s].cpu().numpy(), nm, slots, count
+
+
+def shapes():
+    rng = np.random.default_rng(5)
+    out = {
+        "random": W.random_occupancy(16, 0.3, 41),
+        "dense": W.random_occupancy(12, 0.9, 42),
+        "line": np.array([[3, 4, x] for x in range(700)], np.int32),
+        "isolated": np.array([[2 * z, 2 * y, 2 * x] for z in range(9) for y in range(9) for x in range(9)],
+                             np.int32),
+        "single": np.array([[5, 5, 5]], np.int32),
+    }
+    sh = W.random_occupancy(16, 0.3, 43)
+    out["shuffled"] = sh[rng.permutation(len(sh))]
+    return out
+
+
+@pytest.mark.parametrize("name", ["random", "dense", "line", "isolated", "single", "shuffled"])
+def test_layout_matches_definition(sv, oracle_mod, name):
+    coords = shapes()[name]
+    nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    got, _, _, _ = gpu_layout(sv, coords, nmap)
+    ref = layout_reference(coords, nmap)
+    assert got.shape == ref.shape
+    assert np.array_equal(got, ref)
+    # every voxel appears exactly once
+    v = got[got >= 0]
+    assert np.array_equal(np.sort(v), np.arange(len(coords)))
+
+
+def run_xrun(sv, coords, nmap, feats, w, b):
+    import torch
+    _, nm, slots, count = gpu_layout(sv, coords, nmap)
+    f, ww = torch_storage(feats, "bf16"), torch_storage(w, "bf16")
+    bb = None if b is None else torch_storage(b, "bf16")
+    out = sv.submconv3d_xrun(f, nm, slots, count, ww, bb)
+    plain = sv.submconv3d(f, nm, ww, bb)
+    sv.device_status()
+    return out, plain
+
+
+@pytest.mark.parametrize("co", [16, 64, 128])
+@pytest.mark.parametrize("name", ["random", "dense", "line", "isolated", "single", "shuffled"])
+def test_xrun_conv_matches_oracle_and_plain(sv, oracle_mod, name, co):
+    coords = shapes()[name]
+    n = len(coords)
+    nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    feats = W.values(co + n, 11, (n, 128), "bf16")
+    w = W.values(co + n, 12, (27, 128, co), "bf16", 1.0 / np.sqrt(27 * 128))
+    b = W.values(co + n, 13, (co,), "bf16", 0.1)
+    out, plain = run_xrun(sv, coords, nmap, feats, w, b)
+    ref, sabs = oracle_mod.conv(feats, nmap, w, b, "bf16", threads=oracle_mod.host_threads())
+    assert_within(to_f64(out), ref, sabs, "bf16")
+    assert bool((out.float() == plain.float()).all())
+
+
+def test_xrun_conv_without_bias(sv, oracle_mod):
+    coords = shapes()["random"]
+    n = len(coords)
+    nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    feats = W.values(7, 11, (n, 128), "bf16")
+    w = W.values(7, 12, (27, 128, 128), "bf16", 1.0 / np.sqrt(27 * 128))
+    out, plain = run_xrun(sv, coords, nmap, feats, w, None)
+    ref, sabs = oracle_mod.conv(feats, nmap, w, None, "bf16", threads=oracle_mod.host_threads())
+    assert_within(to_f64(out), ref, sabs, "bf16")
+    assert bool((out.float() == plain.float()).all())
+
+
+@pytest.mark.parametrize("workload", ["medium", "decoder"])
+def test_xrun_conv_workload_sample(sv, oracle_mod, workload):
+    """Full-size seeded workloads: the layout against its definition, the
+    conv against the plain conv everywhere and the oracle on sampled rows."""
+    import torch
+    wl = W.make(workload)
+    layer = wl.layers[0]
+    coords = wl.coords
+    c = torch.from_numpy(coords).cuda()
+    nm = sv.build_nmap(c)
+    slots, count = sv.xrun_layout(c, nm)
+    s = int(count.item())
+    nmap = nm.cpu().numpy()
+    if workload == "medium":
+        assert np.array_equal(slots[:s].cpu().numpy(), layout_reference(coords, nmap))
+    f, ww = torch_storage(layer.feats, "bf16"), torch_storage(layer.w, "bf16")
+    bb = torch_storage(layer.bias, "bf16")
+    out = sv.submconv3d_xrun(f, nm, slots, count, ww, bb)
+    plain = sv.submconv3d(f, nm, ww, bb)
+    sv.device_status()
+    assert bool((out.float() == plain.float()).all())
+    rows = sample_rows(wl.N, 1500, seed=3)
+    ref, sabs = oracle_mod.conv(layer.feats, nmap, layer.w, layer.bias, "bf16", rows=rows,
+                                threads=oracle_mod.host_threads())
+    got = to_f64(out[torch.from_numpy(rows).cuda()])
+    assert_within(got, ref, sabs, "bf16")
+
+
+@pytest.mark.parametrize("ci", [16, 64, 128])
+@pytest.mark.parametrize("name", ["random", "dense", "line", "isolated", "shuffled"])
+def test_xrun_dgrad_matches_oracle_and_plain(sv, oracle_mod, name, ci):
+    """Input gradient over the layout: Co = 128 reduced channels, Ci output
+    channels; against the oracle's scatter sum and the plain input gradient."""
+    import torch
+    coords = shapes()[name]
+    n = len(coords)
+    nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    dout = W.values(ci + n, 21, (n, 128), "bf16")
+    w = W.values(ci + n, 22, (27, ci, 128), "bf16", 1.0 / np.sqrt(27 * 128))
+    _, nm, slots, count = gpu_layout(sv, coords, nmap)
+    d, ww = torch_storage(dout, "bf16"), torch_storage(w, "bf16")
+    got = sv.submconv3d_dgrad_xrun(d, nm, slots, count, ww)
+    plain = sv.submconv3d_dgrad(d, nm, ww)
+    sv.device_status()
+    ref, dabs = oracle_mod.dgrad(dout, nmap, w, "bf16", threads=oracle_mod.host_threads())
+    assert_within(to_f64(got), ref, dabs, "bf16")
+    assert bool((got.float() == plain.float()).all())
+
