@@ -797,11 +797,12 @@ def run_ours(args):
         "peak_extra": peak_extra,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        # per step: the map build's six kernels (flag reset, range/order
-        # check, table clear, insert, row query, voxel-hash query: the path
-        # not taken returns at once) and one conv launch (Co <= 256)
-        # (with --xrun: three layout kernels and one conv launch)
-        "gpu_launches": ((6 + 3 + 1) if args.xrun else (6 + (co + 255) // 256)) * args.steps,
+        # per step: the map build's eight kernels (flag reset, range/order/box
+        # check, clear, insert, dense-row prefix, dense-row query, row-hash
+        # query, voxel-hash query: the paths not taken return at once) and
+        # one conv launch (Co <= 256) (with --xrun: three layout kernels and
+        # one conv launch)
+        "gpu_launches": ((8 + 3 + 1) if args.xrun else (8 + (co + 255) // 256)) * args.steps,
         "clocks": clocks,
         "generation_s": gen_s,
         **({"per_config": per_config} if per_config is not None else {}),

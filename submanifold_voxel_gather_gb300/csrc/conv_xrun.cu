@@ -67,7 +67,7 @@ constexpr uint64_t kBStepUnits = (16 * 2) >> 4;     // one K step of K-major row
 //   0: start address + dxi * 128, base-offset field 0;
 //   1: start address + dxi * 128, base-offset field (start >> 7) & 7;
 //   2: start address on the chunk's row 0, base-offset field dxi.
-constexpr int kShiftMode = 1;
+constexpr int kShiftMode = 0;
 
 enum : uint32_t { kMetaFirst = 1u, kMetaEnd = 2u };
 

@@ -9,8 +9,23 @@
 // paths, chosen on the device from that verdict (every kernel of the other
 // path returns at once):
 //
-// Sorted input (what a voxeliser emits).  Each (z, y) row of cells is a
-// contiguous run of voxels, so a hash of rows (row -> index of its first
+// Sorted input whose bounding box is small enough (the usual case: a
+// voxeliser emits sorted coordinates in a bounded grid).  Each (z, y) row of
+// cells is a contiguous run of voxels, and the box's rows are laid out
+// densely in the workspace: per row the index of its first voxel, and per
+// 32 cells of a row an occupancy word with the count of the row's voxels
+// before it.  A neighbour at x is then one word load: present if its bit is
+// set, at index row start + count before the word + popcount of the lower
+// bits.  No search and no probe:
+//
+//   clear   row starts := -1, words := 0
+//   insert  the first voxel of each row writes the row start; every voxel
+//           sets its bit (one atomic OR per word and warp)
+//   prefix  one warp per row: exclusive prefix of the words' popcounts
+//   query   one thread per voxel: per (dz, dy) row one row-start load, then
+//           one word load per dx
+//
+// Sorted input with a larger box.  A hash of rows (row -> index of its first
 // voxel, table sized from the row count) is enough:
 //
 //   clear   the row table's slots := EMPTY
@@ -57,6 +72,10 @@ constexpr unsigned long long kEmptyKey = ~0ull;
 constexpr size_t kFlagBytes = 256;
 
 enum : int { kFlagDuplicate = 1, kFlagRange = 2, kFlagFull = 4, kFlagUnsorted = 8 };
+
+// Flag words: [0] error / order bits, [1] (z, y) row count, [2..7] the
+// bounding box (z min, z max, y min, y max, x min, x max).
+enum : int { kFlagBoxMin = 2 };
 
 enum : int8_t { kRoleProbe = 0, kRoleMirror = 1, kRoleSelf = 2 };
 
@@ -163,12 +182,55 @@ __device__ __forceinline__ unsigned long long voxel_key(const int32_t* __restric
   return pack_coord(__ldg(coords + 3 * j), __ldg(coords + 3 * j + 1), __ldg(coords + 3 * j + 2));
 }
 
-// flags[0] := 0 (error and order bits), flags[1] := 0 (row count).
+// flags[0] := 0 (error and order bits), flags[1] := 0 (row count), the
+// bounding box := empty.
 __global__ void build_reset_kernel(int* flags) {
   if (threadIdx.x == 0) {
     flags[0] = 0;
     flags[1] = 0;
+    for (int a = 0; a < 3; ++a) {
+      flags[kFlagBoxMin + 2 * a] = INT_MAX;
+      flags[kFlagBoxMin + 2 * a + 1] = INT_MIN;
+    }
   }
+}
+
+// The dense row layout of a sorted input's bounding box (see the header).
+struct DenseRows {
+  int32_t zmin, ymin, xmin;
+  int32_t nz, ny, nx;  // box extents
+  int32_t wpr;         // occupancy words per row
+  uint32_t rows;       // nz * ny
+  uint2* words;        // rows * wpr entries {occupancy bits, voxels of the row before the word}
+  int32_t* row_start;  // rows entries, -1 for an empty row
+};
+
+// Whether the build takes the dense path (sorted, in range, and the box's
+// rows fit in the workspace's table region of table_bytes), and its layout.
+// Every kernel decides from the same flag words, so they all agree.
+__device__ __forceinline__ bool dense_rows(const int* flags, void* table, unsigned long long table_bytes,
+                                           DenseRows* d) {
+  if (flags[0] & (kFlagRange | kFlagUnsorted)) return false;
+  const int zmin = flags[kFlagBoxMin], zmax = flags[kFlagBoxMin + 1];
+  const int ymin = flags[kFlagBoxMin + 2], ymax = flags[kFlagBoxMin + 3];
+  const int xmin = flags[kFlagBoxMin + 4], xmax = flags[kFlagBoxMin + 5];
+  if (zmax < zmin || ymax < ymin || xmax < xmin) return false;
+  const unsigned long long nz = zmax - zmin + 1ull, ny = ymax - ymin + 1ull, nx = xmax - xmin + 1ull;
+  const unsigned long long wpr = (nx + 31ull) >> 5;
+  const unsigned long long rows = nz * ny;
+  if (rows >= (1ull << 31) || rows * wpr >= (1ull << 31)) return false;
+  if (rows * wpr * 8ull + rows * 4ull > table_bytes) return false;
+  d->zmin = zmin;
+  d->ymin = ymin;
+  d->xmin = xmin;
+  d->nz = static_cast<int32_t>(nz);
+  d->ny = static_cast<int32_t>(ny);
+  d->nx = static_cast<int32_t>(nx);
+  d->wpr = static_cast<int32_t>(wpr);
+  d->rows = static_cast<uint32_t>(rows);
+  d->words = static_cast<uint2*>(table);
+  d->row_start = reinterpret_cast<int32_t*>(d->words + rows * wpr);
+  return true;
 }
 
 // Coordinate range, strict (z, y, x) order and the number of (z, y) rows.
@@ -182,28 +244,55 @@ __global__ void __launch_bounds__(kThreads) order_check_kernel(const int32_t* __
     rows = 0;
   }
   __syncthreads();
+  __shared__ int box[6];
+  if (threadIdx.x < 6) box[threadIdx.x] = (threadIdx.x & 1) ? INT_MIN : INT_MAX;
+  __syncthreads();
   int my_bits = 0;
   unsigned int my_rows = 0;
+  int lo[3] = {INT_MAX, INT_MAX, INT_MAX}, hi[3] = {INT_MIN, INT_MIN, INT_MIN};
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
     const int z = __ldg(coords + 3 * i), y = __ldg(coords + 3 * i + 1), x = __ldg(coords + 3 * i + 2);
     if (!in_grid(z) || !in_grid(y) || !in_grid(x)) my_bits |= kFlagRange;
     if (i + 1 < n && !(pack_coord(z, y, x) < voxel_key(coords, i + 1))) my_bits |= kFlagUnsorted;
     if (i == 0 || __ldg(coords + 3 * (i - 1)) != z || __ldg(coords + 3 * (i - 1) + 1) != y) ++my_rows;
+    lo[0] = min(lo[0], z);
+    hi[0] = max(hi[0], z);
+    lo[1] = min(lo[1], y);
+    hi[1] = max(hi[1], y);
+    lo[2] = min(lo[2], x);
+    hi[2] = max(hi[2], x);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     my_bits |= __shfl_xor_sync(0xffffffffu, my_bits, off);
     my_rows += __shfl_xor_sync(0xffffffffu, my_rows, off);
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      lo[a] = min(lo[a], __shfl_xor_sync(0xffffffffu, lo[a], off));
+      hi[a] = max(hi[a], __shfl_xor_sync(0xffffffffu, hi[a], off));
+    }
   }
   if ((threadIdx.x & 31) == 0) {
     if (my_bits) atomicOr(&bits, my_bits);
     if (my_rows) atomicAdd(&rows, my_rows);
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      atomicMin(&box[2 * a], lo[a]);
+      atomicMax(&box[2 * a + 1], hi[a]);
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     if (bits) atomicOr(flags, bits);
     if (rows) atomicAdd(reinterpret_cast<unsigned int*>(flags + 1), rows);
+  }
+  if (threadIdx.x < 6) {
+    if (threadIdx.x & 1) {
+      if (box[threadIdx.x] != INT_MIN) atomicMax(flags + kFlagBoxMin + threadIdx.x, box[threadIdx.x]);
+    } else if (box[threadIdx.x] != INT_MAX) {
+      atomicMin(flags + kFlagBoxMin + threadIdx.x, box[threadIdx.x]);
+    }
   }
 }
 
@@ -217,6 +306,13 @@ __global__ void hash_clear_kernel(Slot* table, unsigned long long cap, int* flag
   const unsigned long long tid = static_cast<unsigned long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   // whole 16-byte slots (EMPTY key, value -1): full-sector stores
   int4* slots = reinterpret_cast<int4*>(table);
+  DenseRows d;
+  if (dense_rows(flags, table, cap * sizeof(Slot), &d)) {  // sorted, small box: the dense rows
+    const unsigned long long nw = static_cast<unsigned long long>(d.rows) * d.wpr;
+    for (unsigned long long i = tid; i < nw; i += stride) d.words[i] = make_uint2(0u, 0u);
+    for (unsigned long long i = tid; i < d.rows; i += stride) d.row_start[i] = -1;
+    return;
+  }
   if (!(f & kFlagUnsorted)) {  // sorted input: only the row table
     const unsigned long long cap_r = row_capacity(static_cast<unsigned int>(flags[1]));
     for (unsigned long long i = tid; i < cap_r; i += stride) slots[i] = make_int4(-1, -1, -1, -1);
@@ -237,9 +333,31 @@ __global__ void hash_clear_kernel(Slot* table, unsigned long long cap, int* flag
 __global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n, Slot* table,
                                    unsigned long long mask, int* flags) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n) return;
   const int f = flags[0];
   if (f & kFlagRange) return;
+  DenseRows d;
+  if (dense_rows(flags, table, (mask + 1ull) * sizeof(Slot), &d)) {
+    // dense rows: the first voxel of each row writes the row start, every
+    // voxel sets its occupancy bit (the voxels of one word and warp combine
+    // their bits first: one atomic OR each)
+    const bool live = i < n;
+    uint32_t word = 0xFFFFFFFFu, bit = 0u;
+    if (live) {
+      const int z = coords[3 * i], y = coords[3 * i + 1], x = coords[3 * i + 2];
+      const uint32_t row = static_cast<uint32_t>(z - d.zmin) * static_cast<uint32_t>(d.ny) +
+                           static_cast<uint32_t>(y - d.ymin);
+      const uint32_t cx = static_cast<uint32_t>(x - d.xmin);
+      word = row * static_cast<uint32_t>(d.wpr) + (cx >> 5);
+      bit = 1u << (cx & 31u);
+      if (i == 0 || coords[3 * (i - 1)] != z || coords[3 * (i - 1) + 1] != y)
+        d.row_start[row] = static_cast<int32_t>(i);
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, word);
+    const uint32_t bits = __reduce_or_sync(peers, bit);
+    if (live && (threadIdx.x & 31u) == static_cast<uint32_t>(__ffs(peers) - 1)) atomicOr(&d.words[word].x, bits);
+    return;
+  }
+  if (i >= n) return;
   const int z = coords[3 * i], y = coords[3 * i + 1], x = coords[3 * i + 2];
   if (!(f & kFlagUnsorted)) {
     // sorted input: the first voxel of each (z, y) row inserts the row
@@ -302,6 +420,95 @@ __global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n
   atomicOr(flags, kFlagFull);
 }
 
+// Dense rows: per row (one warp each), the count of the row's voxels before
+// each occupancy word (exclusive prefix of the words' popcounts).
+__global__ void __launch_bounds__(kThreads) dense_prefix_kernel(int* flags, void* table,
+                                                                unsigned long long table_bytes) {
+  DenseRows d;
+  if (!dense_rows(flags, table, table_bytes, &d)) return;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t warps = gridDim.x * (blockDim.x >> 5);
+  for (uint32_t row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < d.rows; row += warps) {
+    if (d.row_start[row] < 0) continue;  // empty row: never read
+    uint2* w = d.words + static_cast<size_t>(row) * d.wpr;
+    uint32_t carry = 0;
+    for (int32_t base = 0; base < d.wpr; base += 32) {
+      const int32_t j = base + static_cast<int32_t>(lane);
+      const uint32_t c = j < d.wpr ? __popc(w[j].x) : 0u;
+      uint32_t incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= static_cast<uint32_t>(off)) incl += v;
+      }
+      if (j < d.wpr) w[j].y = carry + incl - c;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+}
+
+// Dense rows: the voxel at (zq, yq, xq), or `missing`.
+__device__ __forceinline__ int32_t dense_lookup(const DenseRows& d, int32_t rs, uint32_t wbase, int xq,
+                                               int32_t missing) {
+  const uint32_t cx = static_cast<uint32_t>(xq - d.xmin);
+  if (rs < 0 || cx >= static_cast<uint32_t>(d.nx)) return missing;
+  const uint2 e = __ldg(d.words + wbase + (cx >> 5));
+  const uint32_t b = cx & 31u;
+  if (((e.x >> b) & 1u) == 0u) return missing;
+  return rs + static_cast<int32_t>(e.y + __popc(e.x & ((1u << b) - 1u)));
+}
+
+// Sorted input, dense rows: nmap[k, n] for every offset, by one row-start
+// load per (dz, dy) row and one occupancy-word load per offset.
+template <bool kStd27>
+__global__ void __launch_bounds__(kThreads)
+    nmap_query_dense_kernel(const int32_t* __restrict__ coords, int64_t n, void* table,
+                            unsigned long long table_bytes, const int* __restrict__ flags,
+                            const __grid_constant__ QueryPlan plan, int32_t* __restrict__ nmap) {
+  DenseRows d;
+  if (!dense_rows(flags, table, table_bytes, &d)) return;
+  const int32_t i = static_cast<int32_t>(blockIdx.x) * static_cast<int32_t>(blockDim.x) + static_cast<int32_t>(threadIdx.x);
+  if (i >= n) return;
+  const int32_t missing = static_cast<int32_t>(n);
+  const int z = __ldg(coords + 3 * static_cast<int64_t>(i)), y = __ldg(coords + 3 * static_cast<int64_t>(i) + 1);
+  const int x = __ldg(coords + 3 * static_cast<int64_t>(i) + 2);
+  auto row_of = [&](int zq, int yq, int32_t* rs, uint32_t* wbase) {
+    const uint32_t rz = static_cast<uint32_t>(zq - d.zmin), ry = static_cast<uint32_t>(yq - d.ymin);
+    *rs = -1;
+    *wbase = 0;
+    if (rz < static_cast<uint32_t>(d.nz) && ry < static_cast<uint32_t>(d.ny)) {
+      const uint32_t row = rz * static_cast<uint32_t>(d.ny) + ry;
+      *rs = __ldg(d.row_start + row);
+      *wbase = row * static_cast<uint32_t>(d.wpr);
+    }
+  };
+  if constexpr (kStd27) {
+#pragma unroll
+    for (int dz = -1; dz <= 1; ++dz) {
+#pragma unroll
+      for (int dy = -1; dy <= 1; ++dy) {
+        const int k0 = 9 * (dz + 1) + 3 * (dy + 1);  // offset (dz, dy, -1); +1, +2 follow
+        int32_t rs;
+        uint32_t wbase;
+        row_of(z + dz, y + dy, &rs, &wbase);
+        nmap[static_cast<int64_t>(k0) * n + i] = dense_lookup(d, rs, wbase, x - 1, missing);
+        nmap[static_cast<int64_t>(k0 + 1) * n + i] =
+            (dz == 0 && dy == 0) ? i : dense_lookup(d, rs, wbase, x, missing);
+        nmap[static_cast<int64_t>(k0 + 2) * n + i] = dense_lookup(d, rs, wbase, x + 1, missing);
+      }
+    }
+  } else {
+    for (int32_t g = 0; g < plan.groups; ++g) {
+      int32_t rs;
+      uint32_t wbase;
+      row_of(z + plan.grp_dz[g], y + plan.grp_dy[g], &rs, &wbase);
+      const int m0 = plan.grp_first[g], m1 = m0 + plan.grp_count[g];
+      for (int m = m0; m < m1; ++m)
+        nmap[static_cast<int64_t>(plan.mem_k[m]) * n + i] = dense_lookup(d, rs, wbase, x + plan.mem_dx[m], missing);
+    }
+  }
+}
+
 // Sorted input: nmap[k, n] for every offset, by row probe + search.  The
 // loop is short on instructions (this kernel is issue-bound): 32-bit
 // indices, a 32-bit row hash, and for the lexicographic 3x3x3 offset list
@@ -311,10 +518,12 @@ __global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n
 template <bool kStd27>
 __global__ void __launch_bounds__(kThreads)
     nmap_query_rows_kernel(const int32_t* __restrict__ coords, int64_t n, const Slot* __restrict__ table,
-                           const int* __restrict__ flags, const __grid_constant__ QueryPlan plan,
-                           int32_t* __restrict__ nmap) {
+                           unsigned long long table_bytes, const int* __restrict__ flags,
+                           const __grid_constant__ QueryPlan plan, int32_t* __restrict__ nmap) {
   const int f = flags[0];
   if (f & (kFlagRange | kFlagUnsorted)) return;
+  DenseRows dr;
+  if (dense_rows(flags, const_cast<Slot*>(table), table_bytes, &dr)) return;  // the dense query runs
   const int32_t i = static_cast<int32_t>(blockIdx.x) * static_cast<int32_t>(blockDim.x) + static_cast<int32_t>(threadIdx.x);
   if (i >= n) return;
   const int32_t n32 = static_cast<int32_t>(n);
@@ -599,13 +808,24 @@ spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOff
   hash_insert_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, flags);
   if (!cuda_ok(cudaGetLastError(), "hash_insert_kernel launch", &st)) return st;
 
+  // Dense-row path (sorted input, small box): per-row word prefixes, then
+  // the query; both return at once on the other paths.
+  const unsigned long long table_bytes = static_cast<unsigned long long>(cap) * sizeof(Slot);
+  dense_prefix_kernel<<<16u * static_cast<unsigned>(sms), kThreads, 0, stream>>>(flags, table, table_bytes);
+  if (!cuda_ok(cudaGetLastError(), "dense_prefix_kernel launch", &st)) return st;
   bool std27 = k == 27;
   for (int32_t a = 0; a < k && std27; ++a)
     std27 = offs.d[3 * a] == a / 9 - 1 && offs.d[3 * a + 1] == (a / 3) % 3 - 1 && offs.d[3 * a + 2] == a % 3 - 1;
   if (std27)
-    nmap_query_rows_kernel<true><<<grid, kThreads, 0, stream>>>(coords, n, table, flags, plan, nmap);
+    nmap_query_dense_kernel<true><<<grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags, plan, nmap);
   else
-    nmap_query_rows_kernel<false><<<grid, kThreads, 0, stream>>>(coords, n, table, flags, plan, nmap);
+    nmap_query_dense_kernel<false><<<grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags, plan, nmap);
+  if (!cuda_ok(cudaGetLastError(), "nmap_query_dense_kernel launch", &st)) return st;
+
+  if (std27)
+    nmap_query_rows_kernel<true><<<grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags, plan, nmap);
+  else
+    nmap_query_rows_kernel<false><<<grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags, plan, nmap);
   if (!cuda_ok(cudaGetLastError(), "nmap_query_rows_kernel launch", &st)) return st;
   nmap_query_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, flags, plan, k, nmap);
   if (!cuda_ok(cudaGetLastError(), "nmap_query_kernel launch", &st)) return st;

@@ -103,6 +103,22 @@ def test_nmap_large_configs(sv, oracle_mod, name):
     assert vp >= n
 
 
+def test_nmap_sorted_paths_dense_and_row_hash(sv, oracle_mod):
+    """Sorted input takes the dense-row path when its bounding box fits in the
+    workspace (every workload here), else the row hash: the small workload
+    with one voxel added at the far corner of the grid (still sorted) has a
+    box of 2^60 cells and takes the row hash.  Both give the oracle's map."""
+    small = W.coords_only("small")
+    np.testing.assert_array_equal(gpu_nmap(sv, small), oracle_mod.build_nmap(small, W.offsets_3x3x3()))
+    hi = (1 << 20) - 1
+    wide = np.concatenate([small, np.array([[hi, hi, hi]], np.int32)])
+    for offs in (W.offsets_3x3x3(), W.offsets_cube(2)):
+        np.testing.assert_array_equal(gpu_nmap(sv, wide, offs), oracle_mod.build_nmap(wide, offs))
+    # generic offset lists on the dense path too
+    np.testing.assert_array_equal(gpu_nmap(sv, small, W.offsets_cube(2)),
+                                  oracle_mod.build_nmap(small, W.offsets_cube(2)))
+
+
 def test_async_build_matches_and_reports_on_device(sv, oracle_mod):
     """spconv_build_nmap_async: the same map, the verdict written to device
     memory (no host wait); two builds in flight on two streams; a duplicate
