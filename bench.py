@@ -41,7 +41,7 @@ METRIC = "submconv3d TFLOP/s (2·valid_pairs·Ci·Co) & voxels/s; % of bf16 tens
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
-DOMINANT_KERNEL = "submconv_tc_kernel<256, 1, 1, 0, 0>"
+DOMINANT_KERNEL = "submconv_tc_kernel<256, 1, 1, 0, 0, 0>"
 XRUN_KERNEL = "submconv_xrun_kernel"
 KERNEL_SOURCES = ("submanifold_voxel_gather_gb300/csrc/conv_tc.cu",
                   "submanifold_voxel_gather_gb300/csrc/ptx.cuh")
