@@ -218,6 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 2) {
     // ------------------------------------------------------ loader
+    // All nine groups' map entries of a tile are loaded at once (81
+    // independent loads per lane): the entries come from device memory, and
+    // one round trip per group was measured to starve the MMAs (16.7 ms at
+    // decoder scale against 7.7 ms with the loads taken out).  The ring's
+    // eight rows then cover the next tile's round trip.
     uint32_t e = 0, ephase = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -228,10 +233,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = static_cast<int>(lane) + 32 * j;
         code[j] = r < kGRows ? slot_code(p.slots, s0 - 1 + r, S) : -1;
       }
-      for (int g = 0; g < kGroups && ok; ++g) {
-        int32_t v[9];
+      int32_t v[kGroups][9];
 #pragma unroll
-        for (int j = 0; j < 9; ++j) v[j] = group_row(p.nmap, n_rows, code[j], g);
+      for (int g = 0; g < kGroups; ++g)
+#pragma unroll
+        for (int j = 0; j < 9; ++j) v[g][j] = group_row(p.nmap, n_rows, code[j], g);
+#pragma unroll
+      for (int g = 0; g < kGroups; ++g) {
+        if (!ok) break;
         if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ring_empty[e]), ephase ^ 1))) {
           ok = false;
           break;
@@ -241,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 9; ++j) {
           const int r = static_cast<int>(lane) + 32 * j;
           if (r < kGRows) {
-            ring[e * kRingRow + ring_pos(r)] = v[j];
-            any |= v[j] >= 0;
+            ring[e * kRingRow + ring_pos(r)] = v[g][j];
+            any |= v[g][j] >= 0;
           }
         }
         const uint32_t ballot = __ballot_sync(0xffffffffu, any);

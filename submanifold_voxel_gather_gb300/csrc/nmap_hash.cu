@@ -524,8 +524,11 @@ __global__ void __launch_bounds__(kThreads)
   if (f & (kFlagRange | kFlagUnsorted)) return;
   DenseRows dr;
   if (dense_rows(flags, const_cast<Slot*>(table), table_bytes, &dr)) return;  // the dense query runs
-  const int32_t i = static_cast<int32_t>(blockIdx.x) * static_cast<int32_t>(blockDim.x) + static_cast<int32_t>(threadIdx.x);
-  if (i >= n) return;
+  // grid-stride over the voxels: a small grid, so that the launch costs
+  // little on the builds that take another path
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i64 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i64 < n; i64 += stride) {
+  const int32_t i = static_cast<int32_t>(i64);  // N < 2^31 - 1
   const int32_t n32 = static_cast<int32_t>(n);
   const uint32_t rmask = static_cast<uint32_t>(row_capacity(static_cast<unsigned int>(flags[1])) - 1ull);
   const int32_t* xs = coords + 2;
@@ -591,6 +594,7 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
   }
+  }
 }
 
 // Any other input order: hash probes (one offset of each opposite pair).
@@ -600,8 +604,8 @@ __global__ void __launch_bounds__(kThreads)
                       const __grid_constant__ QueryPlan plan, int32_t k_count, int32_t* __restrict__ nmap) {
   const int f = flags[0];
   if ((f & kFlagRange) || !(f & kFlagUnsorted)) return;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n) return;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;  // small grid, as above
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
   const int z = coords[3 * i], y = coords[3 * i + 1], x = coords[3 * i + 2];
   const int32_t missing = static_cast<int32_t>(n);
   for (int32_t k = 0; k < k_count; ++k) {
@@ -632,6 +636,7 @@ __global__ void __launch_bounds__(kThreads)
       if (mk >= 0 && found != missing) nmap[static_cast<int64_t>(mk) * n + found] = static_cast<int32_t>(i);
     }
     nmap[static_cast<int64_t>(k) * n + i] = found;
+  }
   }
 }
 
@@ -822,12 +827,15 @@ spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOff
     nmap_query_dense_kernel<false><<<grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags, plan, nmap);
   if (!cuda_ok(cudaGetLastError(), "nmap_query_dense_kernel launch", &st)) return st;
 
+  // the row-hash and voxel-hash queries: grid-stride kernels on at most 16
+  // blocks per SM (cheap when their path is not taken)
+  const unsigned small_grid = grid < 16u * static_cast<unsigned>(sms) ? grid : 16u * static_cast<unsigned>(sms);
   if (std27)
-    nmap_query_rows_kernel<true><<<grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags, plan, nmap);
+    nmap_query_rows_kernel<true><<<small_grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags, plan, nmap);
   else
-    nmap_query_rows_kernel<false><<<grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags, plan, nmap);
+    nmap_query_rows_kernel<false><<<small_grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags, plan, nmap);
   if (!cuda_ok(cudaGetLastError(), "nmap_query_rows_kernel launch", &st)) return st;
-  nmap_query_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, flags, plan, k, nmap);
+  nmap_query_kernel<<<small_grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, flags, plan, k, nmap);
   if (!cuda_ok(cudaGetLastError(), "nmap_query_kernel launch", &st)) return st;
 
   if (status_dev != nullptr) {
