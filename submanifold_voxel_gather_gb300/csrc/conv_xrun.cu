@@ -112,24 +112,19 @@ __device__ __forceinline__ int32_t slot_code(const int32_t* slots, int64_t s, in
   return (s >= 0 && s < S) ? __ldg(slots + s) : -1;
 }
 
-// Gathered row of a slot code for group g (offsets 3g, 3g+1, 3g+2 are
-// dx = -1, 0, +1), or -1.
-__device__ __forceinline__ int32_t group_row(const int32_t* nmap, int64_t n, int32_t code, int g) {
-  int64_t v;
-  int k;
-  if (code >= 0) {
-    v = code;
-    k = 3 * g + 1;
-  } else if (code <= -2) {
-    const int32_t h = -2 - code;
-    v = h >> 1;
-    k = (h & 1) ? 3 * g : 3 * g + 2;
-  } else {
-    return -1;
-  }
-  if (v >= n) return -1;
-  const int32_t e = __ldg(nmap + static_cast<int64_t>(k) * n + v);
-  return (e >= 0 && e < n) ? e : -1;
+// Map entry that holds the gathered row of a slot code for group g (offsets
+// 3g, 3g+1, 3g+2 are dx = -1, 0, +1): a voxel slot n reads nmap[3g+1, n], a
+// run-end separator of voxel n the cell right of it, nmap[3g+2, n], and a
+// run-start separator the cell left of it, nmap[3g, n].  Branch-free (the
+// loader issues all its loads before it uses any): an empty slot gives
+// entry 0 and valid = false.
+__device__ __forceinline__ int64_t group_entry(int64_t n, int32_t code, int g, bool* valid) {
+  const int32_t h = -2 - code;
+  const bool vox = code >= 0, sep = code <= -2;
+  const int64_t v = vox ? code : (h >> 1);
+  const int k = vox ? 3 * g + 1 : ((h & 1) ? 3 * g : 3 * g + 2);
+  *valid = (vox || sep) && v < n;
+  return *valid ? static_cast<int64_t>(k) * n + v : 0;
 }
 
 // Ring position of gathered row r: producer warp r / 64 takes rows 4 j + s
@@ -218,11 +213,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 2) {
     // ------------------------------------------------------ loader
-    // All nine groups' map entries of a tile are loaded at once (81
-    // independent loads per lane): the entries come from device memory, and
-    // one round trip per group was measured to starve the MMAs (16.7 ms at
-    // decoder scale against 7.7 ms with the loads taken out).  The ring's
-    // eight rows then cover the next tile's round trip.
     uint32_t e = 0, ephase = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -233,33 +223,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = static_cast<int>(lane) + 32 * j;
         code[j] = r < kGRows ? slot_code(p.slots, s0 - 1 + r, S) : -1;
       }
-      int32_t v[kGroups][9];
+      // Three groups at a time: addresses first, then their 27 loads, then
+      // the checks, so the loads are independent and in flight together
+      // (each load waited for in turn starved the MMAs: 16.7 ms at decoder
+      // scale against 7.7 ms with the loads taken out).
 #pragma unroll
-      for (int g = 0; g < kGroups; ++g)
+      for (int gb = 0; gb < kGroups; gb += 3) {
+        int32_t v[3][9];
+        uint32_t ok_bits[3];
 #pragma unroll
-        for (int j = 0; j < 9; ++j) v[g][j] = group_row(p.nmap, n_rows, code[j], g);
+        for (int q = 0; q < 3; ++q) {
+          ok_bits[q] = 0;
 #pragma unroll
-      for (int g = 0; g < kGroups; ++g) {
-        if (!ok) break;
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ring_empty[e]), ephase ^ 1))) {
-          ok = false;
-          break;
-        }
-        bool any = false;
-#pragma unroll
-        for (int j = 0; j < 9; ++j) {
-          const int r = static_cast<int>(lane) + 32 * j;
-          if (r < kGRows) {
-            ring[e * kRingRow + ring_pos(r)] = v[g][j];
-            any |= v[g][j] >= 0;
+          for (int j = 0; j < 9; ++j) {
+            bool valid;
+            const int64_t at = group_entry(n_rows, code[j], gb + q, &valid);
+            ok_bits[q] |= (valid ? 1u : 0u) << j;
+            v[q][j] = __ldg(p.nmap + at);
           }
         }
-        const uint32_t ballot = __ballot_sync(0xffffffffu, any);
-        if (lane == 0) ring_flag[e] = ballot != 0u ? 1u : 0u;
-        mbar_arrive(smem_addr(&ring_full[e]));
-        if (++e == kXRing) {
-          e = 0;
-          ephase ^= 1;
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          if (!ok) break;
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ring_empty[e]), ephase ^ 1))) {
+            ok = false;
+            break;
+          }
+          bool any = false;
+#pragma unroll
+          for (int j = 0; j < 9; ++j) {
+            const int r = static_cast<int>(lane) + 32 * j;
+            const int32_t x = (((ok_bits[q] >> j) & 1u) != 0u && v[q][j] >= 0 && v[q][j] < n_rows) ? v[q][j] : -1;
+            if (r < kGRows) {
+              ring[e * kRingRow + ring_pos(r)] = x;
+              any |= x >= 0;
+            }
+          }
+          const uint32_t ballot = __ballot_sync(0xffffffffu, any);
+          if (lane == 0) ring_flag[e] = ballot != 0u ? 1u : 0u;
+          mbar_arrive(smem_addr(&ring_full[e]));
+          if (++e == kXRing) {
+            e = 0;
+            ephase ^= 1;
+          }
         }
       }
     }
