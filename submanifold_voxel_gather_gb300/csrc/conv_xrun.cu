@@ -53,6 +53,12 @@ constexpr int kChunks = 2;                    // 64-channel chunks of Ci = 128
 constexpr uint32_t kGChunkBytes = kGRowsAlloc * 128u;           // 33,792 B (33 x 1024)
 constexpr uint32_t kGStageBytes = kChunks * kGChunkBytes;       // 67,584 B
 constexpr int kGStages = 2;
+// The G memory is used as a ring of kGBufs chunk buffers (one 64-channel
+// chunk of a group's rows each), filled and released chunk by chunk: a
+// buffer is refilled once the 12 MMAs (3 offsets x 4) that read it are done,
+// not the group's 24 (measured: with two whole-group stages the fill of
+// group g + 2 waited for all of group g's MMAs).
+constexpr int kGBufs = kGStages * kChunks;
 constexpr uint32_t kWSlotBytes = 128u * 128u;                   // one offset's chunk: 16 KB
 constexpr int kWSlots = 4;
 constexpr int kXRing = 8;                     // loader ring rows
@@ -160,8 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* ring_flag = wmeta + kWSlots;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bars);
   uint64_t* gfull = bars;
-  uint64_t* gempty = gfull + kGStages;
-  uint64_t* wfull = gempty + kGStages;
+  uint64_t* gempty = gfull + kGBufs;
+  uint64_t* wfull = gempty + kGBufs;
   uint64_t* wempty = wfull + kWSlots;
   uint64_t* ring_full = wempty + kWSlots;
   uint64_t* ring_empty = ring_full + kXRing;
@@ -173,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* fills_holder = tmem_holder + 2;
 
   if (warp == 0 && lane == 0) {
-    for (int s = 0; s < kGStages; ++s) {
+    for (int s = 0; s < kGBufs; ++s) {
       mbar_init(smem_addr(&gfull[s]), kProducerThreads);
       mbar_init(smem_addr(&gempty[s]), 1);
     }
@@ -320,27 +326,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!go) continue;
         issued = true;
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&gempty[stage]), st_phase ^ 1))) {
-          ok = false;
-          break;
-        }
-        const uint32_t g_base = smem_addr(smem + p.off_g) + stage * kGStageBytes;
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&gempty[stage]), st_phase ^ 1))) {
+            ok = false;
+            break;
+          }
+          const uint32_t g_base = smem_addr(smem + p.off_g) + stage * kGChunkBytes;
           const char* chunk_base = feats + c * 128 + chunk16 * 16;
-          const uint32_t f_dst = g_base + c * kGChunkBytes + dst_lane;
+          const uint32_t f_dst = g_base + dst_lane;
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             cp_async_16<false>(f_dst + 512u * j + ((j & 1) ? sw_odd : sw_even),
                                chunk_base + static_cast<uint64_t>(vi[j]) * 256u, ((valid_bits >> j) & 1u) << 4);
           if (aw == 0)
-            cp_async_16<false>(g_base + c * kGChunkBytes + dst_extra, chunk_base + static_cast<uint64_t>(xi) * 256u,
+            cp_async_16<false>(g_base + dst_extra, chunk_base + static_cast<uint64_t>(xi) * 256u,
                                x_ok ? 16u : 0u);
-        }
-        cp_async_arrive_noinc(smem_addr(&gfull[stage]));
-        if (++stage == kGStages) {
-          stage = 0;
-          st_phase ^= 1;
+          cp_async_arrive_noinc(smem_addr(&gfull[stage]));
+          if (++stage == kGBufs) {
+            stage = 0;
+            st_phase ^= 1;
+          }
         }
       }
     }
@@ -364,9 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ephase ^= 1;
         }
         if (!go) continue;
-        for (int dxi = 0; dxi < 3 && ok; ++dxi) {
-          const int k = 3 * g + dxi;
-          for (int c = 0; c < kChunks; ++c) {
+        // chunk by chunk, the group's three offsets (the order the MMAs use)
+        for (int c = 0; c < kChunks && ok; ++c) {
+          for (int dxi = 0; dxi < 3; ++dxi) {
+            const int k = 3 * g + dxi;
             if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&wempty[ws]), wphase ^ 1))) {
               ok = false;
               break;
@@ -440,14 +447,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           open = true;
           acc = 0;
         }
-        // the gathered rows were written by cp.async (generic proxy); the
-        // MMA reads them through the async proxy
-        if (!mbar_wait(smem_addr(&gfull[gs]), gphase)) break;
-        fence_proxy_async_smem();
-        tc_fence_after();
-        const uint32_t gaddr = g_base + gs * kGStageBytes;
-        for (int dxi = 0; dxi < 3 && ok; ++dxi) {
-          for (int c = 0; c < kChunks; ++c) {
+        // Chunk by chunk: the chunk's rows (one G buffer), then the
+        // group's three offsets on them, the operand started 0, 1 or 2 rows
+        // in; the buffer is released after its 12 MMAs.
+        for (int c = 0; c < kChunks && ok; ++c) {
+          // the gathered rows were written by cp.async (generic proxy); the
+          // MMA reads them through the async proxy
+          if (!mbar_wait(smem_addr(&gfull[gs]), gphase)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t gaddr = g_base + gs * kGChunkBytes;
+          for (int dxi = 0; dxi < 3; ++dxi) {
             if (dxi != 0 || c != 0) {
               if (!mbar_wait(smem_addr(&wfull[ws]), wphase)) {
                 ok = false;
@@ -456,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
             }
             const uint64_t ad = adesc0 + ws * (kWSlotBytes >> 4);
-            const uint32_t baddr = gaddr + c * kGChunkBytes + (kShiftMode == 2 ? 0u : static_cast<uint32_t>(dxi) * 128u);
+            const uint32_t baddr = gaddr + (kShiftMode == 2 ? 0u : static_cast<uint32_t>(dxi) * 128u);
             uint64_t bd = sw128_desc(baddr, 16u, 1024u);
             if (kShiftMode == 1) bd |= static_cast<uint64_t>((baddr >> 7) & 7u) << 49;
             if (kShiftMode == 2) bd |= static_cast<uint64_t>(dxi) << 49;
@@ -472,13 +485,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               wphase ^= 1;
             }
           }
+          if (!ok) break;
+          umma_commit(smem_addr(&gempty[gs]));
+          if (++gs == kGBufs) {
+            gs = 0;
+            gphase ^= 1;
+          }
         }
         if (!ok) break;
-        umma_commit(smem_addr(&gempty[gs]));
-        if (++gs == kGStages) {
-          gs = 0;
-          gphase ^= 1;
-        }
       }
       *consumed_holder = consumed;
       umma_commit(smem_addr(drain));
@@ -633,7 +647,7 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
   off += (kWSlots + kXRing) * 4u;
   off = (off + 7u) & ~7u;
   p.off_bars = off;
-  off += (2u * kGStages + 2u * kWSlots + 2u * kXRing + 5u) * 8u + 16u;
+  off += (2u * kGBufs + 2u * kWSlots + 2u * kXRing + 5u) * 8u + 16u;
   const uint32_t smem_bytes = off + 1024u;  // slack for the 1024-byte alignment
   if (smem_bytes > 232448u) return fail(SPCONV_ERR_UNSUPPORTED, "x-run conv: shared memory layout too large");
 
