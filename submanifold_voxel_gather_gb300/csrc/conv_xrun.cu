@@ -51,14 +51,12 @@ constexpr int kGRowsAlloc = 264;              // rounded up to whole 8-row swizz
 constexpr int kGroups = 9;                    // (dz, dy) groups of the 3x3x3 offsets
 constexpr int kChunks = 2;                    // 64-channel chunks of Ci = 128
 constexpr uint32_t kGChunkBytes = kGRowsAlloc * 128u;           // 33,792 B (33 x 1024)
-constexpr uint32_t kGStageBytes = kChunks * kGChunkBytes;       // 67,584 B
-constexpr int kGStages = 2;
-// The G memory is used as a ring of kGBufs chunk buffers (one 64-channel
-// chunk of a group's rows each), filled and released chunk by chunk: a
-// buffer is refilled once the 12 MMAs (3 offsets x 4) that read it are done,
-// not the group's 24 (measured: with two whole-group stages the fill of
-// group g + 2 waited for all of group g's MMAs).
-constexpr int kGBufs = kGStages * kChunks;
+// The G memory is a ring of kGBufs chunk buffers (one 64-channel chunk of a
+// group's rows each), filled and released chunk by chunk: a buffer is
+// refilled once the 12 MMAs (3 offsets x 4) that read it are done, not the
+// group's 24 (measured: with two whole-group stages the fill of group g + 2
+// waited for all of group g's MMAs).
+constexpr int kGBufs = 4;
 constexpr uint32_t kWSlotBytes = 128u * 128u;                   // one offset's chunk: 16 KB
 constexpr int kWSlots = 4;
 constexpr int kXRing = 8;                     // loader ring rows
@@ -634,7 +632,7 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
             ((static_cast<uint32_t>(kTileN) >> 3) << 17) | ((128u >> 4) << 24);
   uint32_t off = 0;
   p.off_g = off;
-  off += kGStages * kGStageBytes;
+  off += kGBufs * kGChunkBytes;
   p.off_w = off;
   off += kWSlots * kWSlotBytes;
   p.off_ring = off;

@@ -6,8 +6,10 @@ separator between runs whose outer cells have equal map entries in all nine
 (dz, dy) groups, else two; outer separators of the first and last voxel only
 when one of their outer cells is active).  The convolution is compared with
 the oracle's exact sum (|gpu - exact| <= 4e-3 * sum|terms|) and with the
-plain tensor-core convolution, which forms each output's sum in the same
-order and so gives the same values."""
+plain tensor-core convolution: the two add each output's products in
+different orders (the row-shifted kernel runs a group's three offsets chunk
+by chunk), so their fp32 sums may round to neighbouring bf16 values; they
+must agree to within one bf16 rounding step everywhere."""
 import numpy as np
 import pytest
 
@@ -26,6 +28,21 @@ def sv():
     from submanifold_voxel_gather_gb300 import build
     build.build()
     return mod
+
+
+def assert_near_plain(out, plain, scale=None):
+    """Within one bf16 rounding step (2^-7 of the larger magnitude) of the
+    plain convolution everywhere, plus 1e-4 of the output's sum |terms|
+    (``scale``, numpy; else the largest |output|) for the different fp32
+    summation order, and equal on most entries."""
+    import torch
+    a, b = out.float(), plain.float()
+    diff = (a - b).abs()
+    slack = (1e-4 * torch.from_numpy(np.asarray(scale, np.float32)).to(a.device) if scale is not None
+             else 1e-4 * b.abs().max())
+    step = 2.0 ** -7 * a.abs().maximum(b.abs()) + slack
+    assert bool((diff <= step).all()), float((diff / step).max())
+    assert float((diff == 0).float().mean()) >= 0.9
 
 
 def gpu_layout(sv, coords, nmap):
@@ -88,7 +105,7 @@ def test_xrun_conv_matches_oracle_and_plain(sv, oracle_mod, name, co):
     out, plain = run_xrun(sv, coords, nmap, feats, w, b)
     ref, sabs = oracle_mod.conv(feats, nmap, w, b, "bf16", threads=oracle_mod.host_threads())
     assert_within(to_f64(out), ref, sabs, "bf16")
-    assert bool((out.float() == plain.float()).all())
+    assert_near_plain(out, plain, sabs)
 
 
 def test_xrun_conv_without_bias(sv, oracle_mod):
@@ -100,13 +117,14 @@ def test_xrun_conv_without_bias(sv, oracle_mod):
     out, plain = run_xrun(sv, coords, nmap, feats, w, None)
     ref, sabs = oracle_mod.conv(feats, nmap, w, None, "bf16", threads=oracle_mod.host_threads())
     assert_within(to_f64(out), ref, sabs, "bf16")
-    assert bool((out.float() == plain.float()).all())
+    assert_near_plain(out, plain, sabs)
 
 
 @pytest.mark.parametrize("workload", ["medium", "decoder"])
 def test_xrun_conv_workload_sample(sv, oracle_mod, workload):
     """Full-size seeded workloads: the layout against its definition, the
-    conv against the plain conv everywhere and the oracle on sampled rows."""
+    conv near the plain conv everywhere and against the oracle on sampled
+    rows."""
     import torch
     wl = W.make(workload)
     layer = wl.layers[0]
@@ -123,7 +141,7 @@ def test_xrun_conv_workload_sample(sv, oracle_mod, workload):
     out = sv.submconv3d_xrun(f, nm, slots, count, ww, bb)
     plain = sv.submconv3d(f, nm, ww, bb)
     sv.device_status()
-    assert bool((out.float() == plain.float()).all())
+    assert_near_plain(out, plain)
     rows = sample_rows(wl.N, 1500, seed=3)
     ref, sabs = oracle_mod.conv(layer.feats, nmap, layer.w, layer.bias, "bf16", rows=rows,
                                 threads=oracle_mod.host_threads())
@@ -149,5 +167,5 @@ def test_xrun_dgrad_matches_oracle_and_plain(sv, oracle_mod, name, ci):
     sv.device_status()
     ref, dabs = oracle_mod.dgrad(dout, nmap, w, "bf16", threads=oracle_mod.host_threads())
     assert_within(to_f64(got), ref, dabs, "bf16")
-    assert bool((got.float() == plain.float()).all())
+    assert_near_plain(got, plain, dabs)
 
