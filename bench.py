@@ -58,9 +58,12 @@ def parse_args():
     ap.add_argument("--workload", default="decoder")
     ap.add_argument("--layer", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--xrun", action="store_true",
-                    help="run the conv over the x-run slot layout (row-shifted operands); "
-                         "the layout is built in each step after the map")
+    ap.add_argument("--path", choices=["auto", "tiles", "xrun"], default="auto",
+                    help="conv path: 'tiles' = spconv_submconv3d (voxel tiles); 'xrun' = the x-run "
+                         "slot layout (built in each step after the map) and the row-shifted conv; "
+                         "'auto' = xrun where the layer's shape allows it (bf16, Ci = 128, Co <= 128, "
+                         "the 27 lexicographic offsets), else tiles")
+    ap.add_argument("--xrun", action="store_true", help="same as --path xrun")
     ap.add_argument("--no-numa-bind", action="store_true",
                     help="allocate the end-to-end pinned buffers without placing them near the GPU")
     ap.add_argument("--e2e-slots", type=int, default=3,
@@ -440,6 +443,34 @@ def per_config_lines(torch, sv, dev, bf16_peak, hbm_peak, sm_max_mhz, reps=10, c
             "max_err_over_S": err_over_s(torch, out, rows, ref, sabs),
             "tol": oracle.TOL[dt], "rows_checked": int(len(rows)),
             "l2": "flushed before every timed launch"}
+        if xrun_supported(layer, wl):
+            # the row-shifted conv over the x-run slot layout, same inputs
+            lib = sv.load_library()
+            slots = torch.empty(int(lib.spconv_xrun_slot_capacity(n)), dtype=torch.int32, device=dev)
+            count = torch.empty(1, dtype=torch.int64, device=dev)
+            xws = torch.empty(int(lib.spconv_xrun_workspace_size(n)), dtype=torch.uint8, device=dev)
+            for _ in range(3):
+                sv.xrun_layout(coords, nmap, slots=slots, slot_count=count, workspace=xws)
+                sv.submconv3d_xrun(feats, nmap, slots, count, w, bias, out=out)
+            for e in ev:
+                flush.zero_()
+                e[0].record(stream)
+                sv.xrun_layout(coords, nmap, slots=slots, slot_count=count, workspace=xws)
+                e[1].record(stream)
+                flush.zero_()
+                e[2].record(stream)
+                sv.submconv3d_xrun(feats, nmap, slots, count, w, bias, out=out)
+                e[3].record(stream)
+            torch.cuda.synchronize(dev)
+            sv.device_status()
+            layout_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / reps
+            xconv_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / reps
+            xt = flops / (xconv_ms * 1e-3) / 1e12
+            lines[key]["xrun"] = {
+                "conv_ms": xconv_ms, "layout_ms": layout_ms, "tflops": xt, "frac": xt / peak,
+                "frac_of_roofline": t_roof / xconv_ms, "slots": int(count.item()),
+                "max_err_over_S": err_over_s(torch, out, rows, ref, sabs)}
+            del slots, count, xws
         if name == materialized_on and dt == "bf16":
             mat = materialized_baseline(torch, sv, feats, nmap, w, bias, out)
             mat["workload"] = f"{name}: N={n}, {ci}->{co} {dt}"
@@ -472,7 +503,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": layer.dtype,
         "data": "synthetic (seeded generator)",
-        "config": workload_config(wl, layer),
+        "config": workload_config(wl, layer, xrun=use_xrun(args, layer, wl)),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{rows_total // args.steps} seeded output rows per step "
                                    f"(neighbour map by sort + binary search, fp64 conv loop nest)"},
@@ -482,10 +513,10 @@ def run_reference(args):
     return 0
 
 
-def workload_config(wl, layer, pairs=None):
+def workload_config(wl, layer, pairs=None, xrun=False):
     cfg = {"workload": f"decoder-scale: {wl.note}" if wl.name == "decoder" else f"{wl.name}: {wl.note}",
            "N": wl.N, "K": wl.K, "Ci": layer.Ci, "Co": layer.Co, "seed": wl.seed,
-           "step": "build_nmap + submconv3d",
+           "step": ("build_nmap + xrun_layout + submconv3d_xrun" if xrun else "build_nmap + submconv3d"),
            "l2": "inputs larger than L2 (no flush between steps)"}
     if pairs is not None:
         cfg["valid_pairs"] = pairs
@@ -529,6 +560,22 @@ def copy_bandwidths(torch, dev, d_in, h_in, d_out, h_out, streams, reps=3):
             "both_gbs": (h2d + d2h) / t_both / 1e6}
 
 
+def xrun_supported(layer, wl):
+    """Shapes the row-shifted conv takes: bf16, Ci = 128, Co <= 128, the 27
+    lexicographic 3x3x3 offsets."""
+    import workloads as W
+    return (layer.dtype == "bf16" and layer.Ci == 128 and layer.Co <= 128 and
+            np.array_equal(np.asarray(wl.offsets), W.offsets_3x3x3()))
+
+
+def use_xrun(args, layer, wl):
+    if args.xrun or args.path == "xrun":
+        if not xrun_supported(layer, wl):
+            raise SystemExit("the x-run path takes bf16, Ci = 128, Co <= 128 and the 27 lexicographic offsets")
+        return True
+    return args.path == "auto" and xrun_supported(layer, wl)
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -556,6 +603,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     tf = "tf32" if dtype == "tf32" else None
 
+    args.xrun = use_xrun(args, layer, wl)
     xrun = None
     if args.xrun:
         cap = int(sv.load_library().spconv_xrun_slot_capacity(n))
@@ -786,7 +834,7 @@ def run_ours(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
         "data": "synthetic (seeded generator; decoder-scale voxel shells, random-init weights)",
-        "config": workload_config(wl, layer, pairs),
+        "config": workload_config(wl, layer, pairs, xrun=args.xrun),
         "voxels_per_s": world * n / (ms_per_step * 1e-3),
         "conv_tflops": achieved,
         "build_ms": ms_per_step - conv_avg_ms,

@@ -66,12 +66,11 @@ constexpr int kProducerThreads = 128;
 constexpr int kEpilogueWarp0 = 4;
 constexpr uint64_t kAStepUnits = (16 * 128) >> 4;   // one K step of channel-major weights
 constexpr uint64_t kBStepUnits = (16 * 2) >> 4;     // one K step of K-major rows
-// The B descriptor of an operand shifted by dxi rows in its 1024-byte-aligned
-// chunk (128-byte swizzle, so the swizzle pattern repeats every 8 rows):
-//   0: start address + dxi * 128, base-offset field 0;
-//   1: start address + dxi * 128, base-offset field (start >> 7) & 7;
-//   2: start address on the chunk's row 0, base-offset field dxi.
-constexpr int kShiftMode = 0;
+// An operand shifted by dxi rows in its 1024-byte-aligned chunk is the
+// same 128-byte-swizzled descriptor with the start address moved dxi * 128
+// bytes and the base-offset field left at 0: the tensor core takes the
+// swizzle phase from the absolute address bits (measured on GB300 against a
+// host GEMM for shifts 0..8; the shifted MMAs also run at the full rate).
 
 enum : uint32_t { kMetaFirst = 1u, kMetaEnd = 2u };
 
@@ -467,10 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
             }
             const uint64_t ad = adesc0 + ws * (kWSlotBytes >> 4);
-            const uint32_t baddr = gaddr + (kShiftMode == 2 ? 0u : static_cast<uint32_t>(dxi) * 128u);
-            uint64_t bd = sw128_desc(baddr, 16u, 1024u);
-            if (kShiftMode == 1) bd |= static_cast<uint64_t>((baddr >> 7) & 7u) << 49;
-            if (kShiftMode == 2) bd |= static_cast<uint64_t>(dxi) << 49;
+            const uint64_t bd = sw128_desc(gaddr + static_cast<uint32_t>(dxi) * 128u, 16u, 1024u);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               umma_f16(d_tmem, ad + ks * a_step, bd + ks * kBStepUnits, idesc, acc);
