@@ -54,6 +54,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "epilogue.cuh"
@@ -98,6 +99,7 @@ struct TcParams {
   int32_t co_count;  // channels of this launch (<= 256)
   int32_t act;       // spconv_activation
   int32_t dgrad;     // input gradient: selects the kDgrad instantiation
+  int32_t tma_out;   // plain bf16 epilogue in voxel order: each 32-row block of out is written by one TMA store
   int32_t num_chunks;
   int32_t cps;       // 64-channel chunks per stage: 2 when Ci % 128 == 0 and Co <= 128, else 1
   uint32_t stages;
@@ -211,7 +213,8 @@ __device__ __forceinline__ void transpose_weight_chunk(const uint8_t* raw, uint8
 // transposed in shared memory by warp 3 (kind::tf32 reads K-major A only).
 template <int TILE_N, int MBLK, bool kHoist, bool kDgrad, bool kSplit, bool kTf32>
 __global__ void __launch_bounds__(kThreads, 1)
-    submconv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const TcParams p) {
+    submconv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_out,
+                       const TcParams p) {
   constexpr int kRowsPerWarp = TILE_N / 4;       // gathered rows per producer warp
   constexpr int kIdxPerLane = kRowsPerWarp / 4;  // 4 rows per warp instruction
   static_assert(kRowsPerWarp == 64, "ring layout: 64 rows per gather producer warp");
@@ -283,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *raw_consumed_holder = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_w);
+    if (p.tma_out) tma_prefetch_desc(&tm_out);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_holder), p.tmem_cols);
@@ -788,6 +792,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+      } else if (!fused && p.tma_out) {
+        // The staged block (32 rows x MBLK * 128 channels, the rows of out
+        // in voxel order) goes out as one TMA store: the thread stores would
+        // queue on the load/store pipe behind the gathers (measured: with
+        // two M blocks and one accumulator buffer the MMAs waited 41% of the
+        // time for the epilogue).  Rows past N and channels past Co fall
+        // outside the tensor and are not written.
+        for (int vc = 0; vc < TILE_N / 32; ++vc) {
+          if (et == 0) bulk_wait_read_all();  // the previous block's store has read the buffer
+          epilogue_bar();
+#pragma unroll
+          for (int mb = 0; mb < MBLK; ++mb) {
+            const int co_l = mb * 128 + static_cast<int>(sub) * 32 + static_cast<int>(lane);
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tcol + mb * TILE_N + vc * 32, v);
+            tmem_ld_wait();
+            if (co_l < p.co_count) {
+              const float b = bias_s[co_l];
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                stage_out[i * kOutStride + co_l] = __float2bfloat16_rn(__uint_as_float(v[i]) + b);
+            }
+          }
+          fence_proxy_async_smem();  // the store reads the block through the async proxy
+          epilogue_bar();
+          if (et == 0 && n0 + vc * 32 < n_rows) {
+            tma_store_2d(&tm_out, smem_addr(stage_out), p.co_base, static_cast<int32_t>(n0 + vc * 32));
+            bulk_commit_group();
+          }
+        }
       } else if (!fused) {
         for (int vc = 0; vc < TILE_N / 32; ++vc) {
           epilogue_bar();  // the previous chunk's staged rows have been stored
@@ -863,6 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&tmem_empty[buf]));
     }
+    if (p.tma_out && et == 0) bulk_wait_all();  // the last stores are complete
   }
 
   // ---------------------------------------------------------- teardown
@@ -909,7 +944,7 @@ EncodeTiledFn encode_fn(spconv_status* st) {
 }
 
 template <int TILE_N, int MBLK, bool kHoist, bool kDgrad, bool kSplit, bool kTf32>
-spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t stream) {
+spconv_status launch_shape(const CUtensorMap& tm_w, const CUtensorMap& tm_out, TcParams p, cudaStream_t stream) {
   const int sms = sm_count();
   if (sms <= 0) return fail(SPCONV_ERR_CUDA, "could not query the SM count");
   p.num_tiles = (p.n + TILE_N - 1) / TILE_N;
@@ -961,15 +996,16 @@ spconv_status launch_shape(const CUtensorMap& tm_w, TcParams p, cudaStream_t str
                                     static_cast<int>(smem_bytes)),
                "cudaFuncSetAttribute", &st))
     return st;
-  kern<<<grid, kThreads, smem_bytes, stream>>>(tm_w, p);
+  kern<<<grid, kThreads, smem_bytes, stream>>>(tm_w, tm_out, p);
   if (!cuda_ok(cudaGetLastError(), "submconv_tc_kernel launch", &st)) return st;
   return SPCONV_OK;
 }
 
 template <int MBLK, bool kHoist, bool kSplit, bool kTf32 = false>
-spconv_status launch_dir(const CUtensorMap& tm_w, const TcParams& p, cudaStream_t stream) {
-  return p.dgrad != 0 ? launch_shape<256, MBLK, kHoist, true, kSplit, kTf32>(tm_w, p, stream)
-                      : launch_shape<256, MBLK, kHoist, false, kSplit, kTf32>(tm_w, p, stream);
+spconv_status launch_dir(const CUtensorMap& tm_w, const CUtensorMap& tm_out, const TcParams& p,
+                         cudaStream_t stream) {
+  return p.dgrad != 0 ? launch_shape<256, MBLK, kHoist, true, kSplit, kTf32>(tm_w, tm_out, p, stream)
+                      : launch_shape<256, MBLK, kHoist, false, kSplit, kTf32>(tm_w, tm_out, p, stream);
 }
 
 }  // namespace
@@ -1046,21 +1082,39 @@ spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_
     // Ci = 256, Co = 128 2.27 -> 2.05 ms; with Ci = 128 they cost 1-4%).
     const bool split = p.cps == 2 && p.num_chunks > 2;
     const bool hoist = p.num_chunks >= 2;
+    // Output by TMA stores (plain bf16 epilogue, voxel order): out viewed as
+    // a (N, Co) tensor, boxes of 32 rows x one launch's M blocks of channels.
+    CUtensorMap tm_out;
+    std::memset(&tm_out, 0, sizeof tm_out);
+    p.tma_out = 0;
+    if (!tf32 && order == nullptr && residual == nullptr && act == SPCONV_ACT_NONE) {
+      const cuuint32_t box_co = p.co_count <= 128 ? 128u : 256u;
+      cuuint64_t odims[2] = {static_cast<cuuint64_t>(co), static_cast<cuuint64_t>(n)};
+      cuuint64_t ostrides[1] = {static_cast<cuuint64_t>(co) * 2u};
+      cuuint32_t obox[2] = {box_co, 32u};
+      cuuint32_t oestr[2] = {1, 1};
+      CUresult ro = encode(&tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, odims, ostrides, obox, oestr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (ro != CUDA_SUCCESS)
+        return fail(SPCONV_ERR_CUDA, "cuTensorMapEncodeTiled(out) failed: " + std::to_string(ro));
+      p.tma_out = 1;
+    }
     if (tf32) {
       // one 32-channel chunk per stage (48 KB, or 64 KB with two M blocks)
       p.cps = 1;
       if (p.co_count <= 128)
-        st = hoist ? launch_dir<1, true, false, true>(tm_w, p, stream)
-                   : launch_dir<1, false, false, true>(tm_w, p, stream);
+        st = hoist ? launch_dir<1, true, false, true>(tm_w, tm_out, p, stream)
+                   : launch_dir<1, false, false, true>(tm_w, tm_out, p, stream);
       else
-        st = hoist ? launch_dir<2, true, false, true>(tm_w, p, stream)
-                   : launch_dir<2, false, false, true>(tm_w, p, stream);
+        st = hoist ? launch_dir<2, true, false, true>(tm_w, tm_out, p, stream)
+                   : launch_dir<2, false, false, true>(tm_w, tm_out, p, stream);
     } else if (split)
-      st = launch_dir<1, true, true>(tm_w, p, stream);
+      st = launch_dir<1, true, true>(tm_w, tm_out, p, stream);
     else if (p.co_count <= 128)
-      st = hoist ? launch_dir<1, true, false>(tm_w, p, stream) : launch_dir<1, false, false>(tm_w, p, stream);
+      st = hoist ? launch_dir<1, true, false>(tm_w, tm_out, p, stream) : launch_dir<1, false, false>(tm_w, tm_out, p, stream);
     else
-      st = hoist ? launch_dir<2, true, false>(tm_w, p, stream) : launch_dir<2, false, false>(tm_w, p, stream);
+      st = hoist ? launch_dir<2, true, false>(tm_w, tm_out, p, stream) : launch_dir<2, false, false>(tm_w, tm_out, p, stream);
     if (st != SPCONV_OK) return st;
   }
   return SPCONV_OK;

@@ -90,6 +90,7 @@ struct XrParams {
   uint32_t off_w;
   uint32_t off_ring;
   uint32_t off_stage_out;
+  uint32_t off_codes;  // the epilogue's copy of the current tile's 256 slot codes
   uint32_t off_bias;
   uint32_t off_meta;
   uint32_t off_bars;
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   int32_t* ring = reinterpret_cast<int32_t*>(smem + p.off_ring);
   __nv_bfloat16* stage_out = reinterpret_cast<__nv_bfloat16*>(smem + p.off_stage_out);
+  int32_t* codes_s = reinterpret_cast<int32_t*>(smem + p.off_codes);
   float* bias_s = reinterpret_cast<float*>(smem + p.off_bias);
   uint32_t* wmeta = reinterpret_cast<uint32_t*>(smem + p.off_meta);
   uint32_t* ring_flag = wmeta + kWSlots;
@@ -507,8 +509,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int64_t s0 = t * kTileN;
       const uint32_t tcol = tmem_base + ((sub * 32u) << 16) + buf * static_cast<uint32_t>(kTileN);
+      // The tile's slot codes (the output row of each slot), read once and
+      // coalesced: a row's store then never waits on a load of its code.
+      epi_bar();  // the previous tile's codes are no longer read
+      codes_s[et] = slot_code(p.slots, s0 + et, S);
+      codes_s[et + 128] = slot_code(p.slots, s0 + et + 128, S);
       for (int vc = 0; vc < kTileN / 32; ++vc) {
-        epi_bar();  // the previous chunk's staged rows have been stored
+        epi_bar();  // the previous chunk's staged rows have been stored (and the codes are in)
         uint32_t v[32];
         tmem_ld_32x32b_x32(tcol + vc * 32, v);
         tmem_ld_wait();
@@ -521,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = et; q < 32 * chunks_per_row; q += 128) {
           const int r = q / chunks_per_row;
           const int c8 = q - r * chunks_per_row;
-          const int32_t code = slot_code(p.slots, s0 + vc * 32 + r, S);
+          const int32_t code = codes_s[vc * 32 + r];
           if (code >= 0 && code < n_rows)
             *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(code) * p.co + c8 * 8) =
                 *reinterpret_cast<const uint4*>(stage_out + r * 128 + c8 * 8);
@@ -635,6 +642,8 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
   off += kXRing * kRingRow * 4u;
   p.off_stage_out = off;
   off += 32u * 128u * 2u;
+  p.off_codes = off;
+  off += kTileN * 4u;
   p.off_bias = off;
   off += 128u * 4u;
   p.off_meta = off;
