@@ -553,6 +553,8 @@ def copy_bandwidths(torch, dev, d_in, h_in, d_out, h_out, streams, reps=3):
         with torch.cuda.stream(streams[1]):
             h_out.copy_(d_out, non_blocking=True)
 
+    up()      # untimed first use of each path (the first copy of a process can be slow)
+    down()
     t_up = timed(up)
     t_down = timed(down)
     t_both = timed(lambda: (up(), down()))
