@@ -148,7 +148,13 @@ __device__ __forceinline__ bool issue_group(uint32_t flag, int g, bool issued) {
 // (the map is symmetric); the gathered rows are dout's (Co = 128 reduced
 // channels) and the weights of offset k are w[26 - k] read from the forward
 // layout as a K-major operand, as in conv_tc.cu.
-template <bool kDgrad>
+// kPair: CTA pairs (clusters of two) share the weight stream.  The two CTAs
+// of a pair take tiles 2i and 2i + 1 of each step (an odd tile count leaves
+// the second CTA an empty last tile) and keep every group, so both consume
+// the same weight slots in the same order; each loads one half of every
+// slot and multicasts it to both, and a slot is refilled once both CTAs'
+// MMAs are done with it.  Each SM then streams half the weight bytes.
+template <bool kDgrad, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     submconv_xrun_kernel(const __grid_constant__ CUtensorMap tm_w, const XrParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -184,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kWSlots; ++s) {
       mbar_init(smem_addr(&wfull[s]), 1);
-      mbar_init(smem_addr(&wempty[s]), 1);
+      mbar_init(smem_addr(&wempty[s]), kPair ? 2 : 1);
     }
     for (int i = 0; i < kXRing; ++i) {
       mbar_init(smem_addr(&ring_full[i]), 32);
@@ -210,17 +216,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();  // the peer's barriers exist before any multicast targets them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int64_t n_rows = p.n;
   const int64_t S = max(int64_t{0}, min(__ldg(p.slot_count), p.slots_capacity));
   const int64_t num_tiles = (S + kTileN - 1) / kTileN;
+  // Tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...; a pair steps over its
+  // two tiles together, so the second CTA may get one tile past the end
+  // (all of its slots empty: gathers zero-fill, nothing is stored).
+  const uint32_t rank = kPair ? cluster_cta_rank() : 0u;
+  const int64_t t_end = num_tiles + static_cast<int64_t>(rank);
 
   if (warp == 2) {
     // ------------------------------------------------------ loader
     uint32_t e = 0, ephase = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    for (int64_t t = blockIdx.x; t < t_end && ok; t += gridDim.x) {
       const int64_t s0 = t * kTileN;
       int32_t code[9];  // gathered rows r = lane + 32 j of the tile (r < 258)
 #pragma unroll
@@ -288,14 +300,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t dst_extra = 256u * 128u + static_cast<uint32_t>(sub_row) * 128u + sw_even;
     uint32_t stage = 0, st_phase = 0, e = 0, ephase = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    for (int64_t t = blockIdx.x; t < t_end && ok; t += gridDim.x) {
       bool issued = false;
       for (int g = 0; g < kGroups && ok; ++g) {
         if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ring_full[e]), ephase))) {
           ok = false;
           break;
         }
-        const bool go = issue_group(ring_flag[e], g, issued);
+        const bool go = kPair || issue_group(ring_flag[e], g, issued);
         uint32_t vi[16];
         uint32_t valid_bits = 0;
         uint32_t xi = 0;
@@ -354,14 +366,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------ weight producer
     uint32_t ws = 0, wphase = 0, e = 0, ephase = 0, fills = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    for (int64_t t = blockIdx.x; t < t_end && ok; t += gridDim.x) {
       bool issued = false;
       for (int g = 0; g < kGroups && ok; ++g) {
         if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ring_full[e]), ephase))) {
           ok = false;
           break;
         }
-        const bool go = issue_group(ring_flag[e], g, issued);
+        const bool go = kPair || issue_group(ring_flag[e], g, issued);
         __syncwarp();
         mbar_arrive(smem_addr(&ring_empty[e]));
         if (++e == kXRing) {
@@ -383,7 +395,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive_expect_tx(fb, kWSlotBytes);
             }
             __syncwarp();
-            if constexpr (!kDgrad) {
+            if constexpr (kPair) {
+              // this CTA's half of the slot, multicast to both CTAs: forward,
+              // 64 output channels x 64 input channels; input gradient, 64
+              // forward-ci rows with 64 forward-co entries (8 KB either way)
+              if (lane == 0) {
+                const uint32_t dst = smem_addr(smem + p.off_w) + ws * kWSlotBytes + rank * 8192u;
+                if constexpr (!kDgrad)
+                  tma_load_3d_multicast(dst, &tm_w, static_cast<int>(rank) * 64, c * 64, k, fb, 0x3);
+                else
+                  tma_load_3d_multicast(dst, &tm_w, c * 64, static_cast<int>(rank) * 64, 26 - k, fb, 0x3);
+              }
+            } else if constexpr (!kDgrad) {
               // w[k] channel-major: two boxes of 64 output channels x 64
               // input channels (128-byte swizzle)
               if (lane < 2)
@@ -474,7 +497,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               umma_f16(d_tmem, ad + ks * a_step, bd + ks * kBStepUnits, idesc, acc);
               acc = 1;
             }
-            umma_commit(smem_addr(&wempty[ws]));
+            if constexpr (kPair)
+              umma_commit_multicast(smem_addr(&wempty[ws]), 0x3);  // both CTAs' copies of the slot
+            else
+              umma_commit(smem_addr(&wempty[ws]));
             ++consumed;
             if (++ws == kWSlots) {
               ws = 0;
@@ -502,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int chunks_per_row = p.co_count / 8;
     const int co_l = static_cast<int>(sub) * 32 + static_cast<int>(lane);
     uint32_t tile_i = 0;
-    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tile_i) {
+    for (int64_t t = blockIdx.x; t < t_end; t += gridDim.x, ++tile_i) {
       const uint32_t buf = tile_i & 1u;
       const bool got = __all_sync(0xffffffffu, mbar_wait(smem_addr(&tmem_full[buf]), (tile_i >> 1) & 1u));
       if (!epi_all(got)) break;
@@ -551,6 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(smem_addr(&wfull[i % kWSlots]), (i / kWSlots) & 1u);
   }
   __syncthreads();
+  // No load or commit of the peer targets this CTA's memory any more.
+  if constexpr (kPair) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
@@ -610,7 +638,9 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
   const cuuint64_t wi = dgrad ? static_cast<cuuint64_t>(co) : 128u;  // forward Ci
   cuuint64_t dims[3] = {wo, wi, 27u};
   cuuint64_t strides[2] = {wo * 2u, wi * wo * 2u};
-  cuuint32_t box[3] = {64u, dgrad ? 128u : 64u, 1u};
+  // Paired CTAs load half a slot each: 64 x 64 boxes for the input gradient too.
+  constexpr bool kPaired = true;
+  cuuint32_t box[3] = {64u, (dgrad && !kPaired) ? 128u : 64u, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box,
                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -654,14 +684,31 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
   const uint32_t smem_bytes = off + 1024u;  // slack for the 1024-byte alignment
   if (smem_bytes > 232448u) return fail(SPCONV_ERR_UNSUPPORTED, "x-run conv: shared memory layout too large");
 
-  auto kern = dgrad ? submconv_xrun_kernel<true> : submconv_xrun_kernel<false>;
+  auto kern = dgrad ? submconv_xrun_kernel<true, kPaired> : submconv_xrun_kernel<false, kPaired>;
   if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes)),
                "cudaFuncSetAttribute", &st))
     return st;
   const int sms = sm_count();
   if (sms <= 0) return fail(SPCONV_ERR_CUDA, "could not query the SM count");
-  kern<<<sms, kThreads, smem_bytes, stream>>>(tm_w, p);
-  if (!cuda_ok(cudaGetLastError(), "submconv_xrun_kernel", &st)) return st;
+  // Clusters of two CTAs, as many as fit at once (one CTA per SM).
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
+  int clusters = 0;
+  if (!cuda_ok(cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg), "cudaOccupancyMaxActiveClusters", &st))
+    return st;
+  if (clusters < 1) return fail(SPCONV_ERR_UNSUPPORTED, "x-run conv: no CTA pair fits on this device");
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * (clusters < sms / 2 ? clusters : sms / 2)), 1, 1);
+  if (!cuda_ok(cudaLaunchKernelEx(&cfg, kern, tm_w, p), "submconv_xrun_kernel", &st)) return st;
   return SPCONV_OK;
 }
 
