@@ -448,14 +448,14 @@ def per_config_lines(torch, sv, dev, bf16_peak, hbm_peak, sm_max_mhz, reps=10, c
             lib = sv.load_library()
             slots = torch.empty(int(lib.spconv_xrun_slot_capacity(n)), dtype=torch.int32, device=dev)
             count = torch.empty(1, dtype=torch.int64, device=dev)
-            xws = torch.empty(int(lib.spconv_xrun_workspace_size(n)), dtype=torch.uint8, device=dev)
+            xws = torch.empty(int(lib.spconv_build_nmap_xrun_workspace_size(n)), dtype=torch.uint8, device=dev)
             for _ in range(3):
-                sv.xrun_layout(coords, nmap, slots=slots, slot_count=count, workspace=xws)
+                sv.build_nmap_xrun(coords, out=nmap, slots=slots, slot_count=count, workspace=xws)
                 sv.submconv3d_xrun(feats, nmap, slots, count, w, bias, out=out)
             for e in ev:
                 flush.zero_()
                 e[0].record(stream)
-                sv.xrun_layout(coords, nmap, slots=slots, slot_count=count, workspace=xws)
+                sv.build_nmap_xrun(coords, out=nmap, slots=slots, slot_count=count, workspace=xws)
                 e[1].record(stream)
                 flush.zero_()
                 e[2].record(stream)
@@ -463,11 +463,11 @@ def per_config_lines(torch, sv, dev, bf16_peak, hbm_peak, sm_max_mhz, reps=10, c
                 e[3].record(stream)
             torch.cuda.synchronize(dev)
             sv.device_status()
-            layout_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / reps
+            xbuild_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / reps  # map + layout
             xconv_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / reps
             xt = flops / (xconv_ms * 1e-3) / 1e12
             lines[key]["xrun"] = {
-                "conv_ms": xconv_ms, "layout_ms": layout_ms, "tflops": xt, "frac": xt / peak,
+                "conv_ms": xconv_ms, "build_ms": xbuild_ms, "tflops": xt, "frac": xt / peak,
                 "frac_of_roofline": t_roof / xconv_ms, "slots": int(count.item()),
                 "max_err_over_S": err_over_s(torch, out, rows, ref, sabs)}
             del slots, count, xws
@@ -601,22 +601,26 @@ def run_ours(args):
     bias = to_device(torch, layer.bias, dtype, dev)
     nmap = torch.empty((k, n), dtype=torch.int32, device=dev)
     out = torch.empty((n, co), dtype=feats.dtype, device=dev)
-    ws = torch.empty(sv.workspace_size(n), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     tf = "tf32" if dtype == "tf32" else None
 
     args.xrun = use_xrun(args, layer, wl)
     xrun = None
+    lib = sv.load_library()
     if args.xrun:
-        cap = int(sv.load_library().spconv_xrun_slot_capacity(n))
-        xrun = {"slots": torch.empty(cap, dtype=torch.int32, device=dev),
-                "count": torch.empty(1, dtype=torch.int64, device=dev),
-                "ws": torch.empty(int(sv.load_library().spconv_xrun_workspace_size(n)), dtype=torch.uint8,
-                                  device=dev)}
+        # the map and the x-run slot layout come from one call (one workspace)
+        xrun = {"slots": torch.empty(int(lib.spconv_xrun_slot_capacity(n)), dtype=torch.int32, device=dev),
+                "count": torch.empty(1, dtype=torch.int64, device=dev)}
+        ws = torch.empty(int(lib.spconv_build_nmap_xrun_workspace_size(n)), dtype=torch.uint8, device=dev)
+    else:
+        ws = torch.empty(sv.workspace_size(n), dtype=torch.uint8, device=dev)
 
-    def layout(c, nm, x, stream=None):
+    def build(c, nm, w_s, x, status=None, stream=None):
         if x is not None:
-            sv.xrun_layout(c, nm, slots=x["slots"], slot_count=x["count"], workspace=x["ws"], stream=stream)
+            sv.build_nmap_xrun(c, out=nm, slots=x["slots"], slot_count=x["count"], workspace=w_s, status=status,
+                               stream=stream)
+        else:
+            sv.build_nmap(c, workspace=w_s, out=nm, status=status, stream=stream)
 
     def conv(f, nm, ww, b, o, x, stream=None):
         if x is not None:
@@ -625,8 +629,7 @@ def run_ours(args):
             sv.submconv3d(f, nm, ww, b, out=o, dtype=tf, stream=stream)
 
     def step():
-        sv.build_nmap(coords, workspace=ws, out=nmap)
-        layout(coords, nmap, xrun)
+        build(coords, nmap, ws, xrun)
         conv(feats, nmap, w, bias, out, xrun)
 
     for _ in range(max(args.warmup, 0)):
@@ -647,8 +650,7 @@ def run_ours(args):
     time.sleep(0.3)
     t_start.record(stream)
     for i in range(args.steps):
-        sv.build_nmap(coords, workspace=ws, out=nmap)
-        layout(coords, nmap, xrun)
+        build(coords, nmap, ws, xrun)
         ev[i][0].record(stream)
         conv(feats, nmap, w, bias, out, xrun)
         ev[i][1].record(stream)
@@ -671,8 +673,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     torch.cuda.reset_peak_memory_stats(dev)
     base = torch.cuda.memory_allocated(dev)
-    sv.build_nmap(coords, workspace=ws, out=nmap)
-    layout(coords, nmap, xrun)
+    build(coords, nmap, ws, xrun)
     torch.cuda.synchronize(dev)
     during_build = torch.cuda.max_memory_allocated(dev) - base
     torch.cuda.reset_peak_memory_stats(dev)
@@ -739,8 +740,7 @@ def run_ours(args):
                 sl["feats"].copy_(h_feats, non_blocking=True)
                 sl["w"].copy_(h_w, non_blocking=True)
                 sl["bias"].copy_(h_bias, non_blocking=True)
-                sv.build_nmap(sl["coords"], workspace=sl["ws"], out=sl["nmap"], status=sl["status"], stream=st)
-                layout(sl["coords"], sl["nmap"], sl["xrun"], stream=st)
+                build(sl["coords"], sl["nmap"], sl["ws"], sl["xrun"], status=sl["status"], stream=st)
                 conv(sl["feats"], sl["nmap"], sl["w"], sl["bias"], sl["out"], sl["xrun"], stream=st)
                 sl["h_out"].copy_(sl["out"], non_blocking=True)
 

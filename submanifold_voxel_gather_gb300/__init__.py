@@ -101,6 +101,10 @@ def load_library() -> ctypes.CDLL:
         lib.spconv_xrun_slot_capacity.restype = i64
         lib.spconv_xrun_layout.argtypes = [vp, vp, i64, i32, vp, i64, vp, vp, ctypes.c_size_t, vp]
         lib.spconv_xrun_layout.restype = ctypes.c_int
+        lib.spconv_build_nmap_xrun_workspace_size.argtypes = [i64]
+        lib.spconv_build_nmap_xrun_workspace_size.restype = ctypes.c_size_t
+        lib.spconv_build_nmap_xrun.argtypes = [vp, i64, vp, vp, i64, vp, vp, ctypes.c_size_t, vp, vp]
+        lib.spconv_build_nmap_xrun.restype = ctypes.c_int
         lib.spconv_submconv3d_xrun.argtypes = [vp, vp, vp, i64, vp, vp, vp, vp, i64, i32, i32, i32,
                                                ctypes.c_int, vp]
         lib.spconv_submconv3d_xrun.restype = ctypes.c_int
@@ -378,6 +382,47 @@ def xrun_layout(coords, nmap, slots=None, slot_count=None, workspace=None, strea
     _check(lib.spconv_xrun_layout(_ptr(coords), _ptr(nmap), n, k, _ptr(slots), slots.numel(), _ptr(slot_count),
                                   _ptr(workspace), workspace.numel(), _stream_handle(stream)))
     return slots, slot_count
+
+
+def build_nmap_xrun(coords, out=None, slots=None, slot_count=None, workspace=None, status=None, stream=None):
+    """The map (default 3x3x3 offsets) and the x-run slot layout in one call
+    (spconv_build_nmap_xrun): returns (nmap, slots, slot_count) as
+    ``build_nmap`` and ``xrun_layout`` would.  ``status``: an int32 CUDA
+    tensor of one element that receives the verdict without a host wait;
+    None waits and raises on a bad input."""
+    torch = _torch()
+    _require_cuda(coords, "coords", torch.int32)
+    if coords.dim() != 2 or coords.shape[1] != 3:
+        raise ValueError("coords must have shape (N, 3)")
+    n = coords.shape[0]
+    lib = load_library()
+    dev = coords.device
+    if out is None:
+        out = torch.empty((27, n), dtype=torch.int32, device=dev)
+    else:
+        _require_cuda(out, "out", torch.int32)
+        if tuple(out.shape) != (27, n):
+            raise ValueError("out must have shape (27, N)")
+    cap = int(lib.spconv_xrun_slot_capacity(n))
+    if slots is None:
+        slots = torch.empty(cap, dtype=torch.int32, device=dev)
+    else:
+        _require_cuda(slots, "slots", torch.int32)
+    if slot_count is None:
+        slot_count = torch.empty(1, dtype=torch.int64, device=dev)
+    else:
+        _require_cuda(slot_count, "slot_count", torch.int64)
+    wbytes = int(lib.spconv_build_nmap_xrun_workspace_size(n))
+    if workspace is None:
+        workspace = torch.empty(wbytes, dtype=torch.uint8, device=dev)
+    else:
+        _require_cuda(workspace, "workspace", torch.uint8)
+    if status is not None:
+        _require_cuda(status, "status", torch.int32)
+    _check(lib.spconv_build_nmap_xrun(_ptr(coords), n, _ptr(out), _ptr(slots), slots.numel(), _ptr(slot_count),
+                                      _ptr(workspace), workspace.numel(),
+                                      None if status is None else _ptr(status), _stream_handle(stream)))
+    return out, slots, slot_count
 
 
 def submconv3d_xrun(feats, nmap, slots, slot_count, w, bias=None, out=None, stream=None):

@@ -29,9 +29,14 @@ size_t hash_capacity(int64_t n);
 // With status_dev == nullptr the call waits for `stream` and returns the
 // build's verdict; otherwise it writes the verdict (an spconv_status) to
 // status_dev on the stream and returns without waiting.
+// With xflags (lexicographic 3x3x3 offsets), the dense-row query also
+// writes the x-run layout's per-voxel flags there and sets the word at
+// xrun_flags_ready(workspace); the other build paths leave both alone.
 spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOffsets& offs,
                                 int32_t k, int32_t* nmap, void* workspace, cudaStream_t stream,
-                                int32_t* status_dev = nullptr);
+                                int32_t* status_dev = nullptr, uint8_t* xflags = nullptr);
+// The word of a build workspace that tells whether the x-run flags were written.
+const int* xrun_flags_ready(const void* workspace);
 // Device address of the allocation-free variant's static scratch on the
 // current device (looked up on every call).
 spconv_status noalloc_scratch(void** scratch);
@@ -86,8 +91,13 @@ spconv_status read_and_clear_xrun_device_error(cudaStream_t stream, unsigned int
 // ---- x-run slot layout (xrun.cu) and the row-shifted conv (conv_xrun.cu)
 size_t xrun_workspace_bytes(int64_t n);
 int64_t xrun_slot_capacity(int64_t n);
+// flags_ready (optional): a word that, when set on the device, says the
+// per-voxel flags at xrun_flags(workspace) were already written (by the map
+// build's dense query); the layout then only reads them.
 spconv_status launch_xrun_layout(const int32_t* coords, const int32_t* nmap, int64_t n, int32_t* slots,
-                                 int64_t cap, int64_t* slot_count, void* workspace, cudaStream_t stream);
+                                 int64_t cap, int64_t* slot_count, void* workspace, cudaStream_t stream,
+                                 const int* flags_ready = nullptr);
+uint8_t* xrun_flags(void* workspace);
 // bf16, lexicographic 3x3x3 offsets; 128 reduced channels (forward Ci, or
 // forward Co for the input gradient) and co <= 128 output channels
 spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int32_t* slots,

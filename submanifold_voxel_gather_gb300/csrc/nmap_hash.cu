@@ -74,8 +74,9 @@ constexpr size_t kFlagBytes = 256;
 enum : int { kFlagDuplicate = 1, kFlagRange = 2, kFlagFull = 4, kFlagUnsorted = 8 };
 
 // Flag words: [0] error / order bits, [1] (z, y) row count, [2..7] the
-// bounding box (z min, z max, y min, y max, x min, x max).
-enum : int { kFlagBoxMin = 2 };
+// bounding box (z min, z max, y min, y max, x min, x max), [8] set when the
+// dense query has written the x-run layout's per-voxel flags.
+enum : int { kFlagBoxMin = 2, kFlagXrunReady = 8 };
 
 enum : int8_t { kRoleProbe = 0, kRoleMirror = 1, kRoleSelf = 2 };
 
@@ -188,6 +189,7 @@ __global__ void build_reset_kernel(int* flags) {
   if (threadIdx.x == 0) {
     flags[0] = 0;
     flags[1] = 0;
+    flags[kFlagXrunReady] = 0;
     for (int a = 0; a < 3; ++a) {
       flags[kFlagBoxMin + 2 * a] = INT_MAX;
       flags[kFlagBoxMin + 2 * a + 1] = INT_MIN;
@@ -460,15 +462,29 @@ __device__ __forceinline__ int32_t dense_lookup(const DenseRows& d, int32_t rs, 
 
 // Sorted input, dense rows: nmap[k, n] for every offset, by one row-start
 // load per (dz, dy) row and one occupancy-word load per offset.
-template <bool kStd27>
+// kXFlags (lexicographic 3x3x3 list only): also the x-run layout's flag of
+// each voxel (xrun.cu), from the entries in registers: bits 0-1 the
+// separators after the voxel (0 inside a run; at a run end 1 when its nine
+// (dz, dy, +1) entries equal the next voxel's nine (dz, dy, -1) entries,
+// else 2; after the last voxel 1 when one of its (dz, dy, +1) cells is
+// active), bit 2 a separator before voxel 0 (one of its (dz, dy, -1) cells
+// is active).  The next voxel's entries come from the next lane; the last
+// lane of a warp computes them itself.
+template <bool kStd27, bool kXFlags>
 __global__ void __launch_bounds__(kThreads)
     nmap_query_dense_kernel(const int32_t* __restrict__ coords, int64_t n, void* table,
-                            unsigned long long table_bytes, const int* __restrict__ flags,
-                            const __grid_constant__ QueryPlan plan, int32_t* __restrict__ nmap) {
+                            unsigned long long table_bytes, int* flags,
+                            const __grid_constant__ QueryPlan plan, int32_t* __restrict__ nmap,
+                            uint8_t* __restrict__ xflags) {
+  static_assert(!kXFlags || kStd27, "x-run flags need the lexicographic 3x3x3 offsets");
   DenseRows d;
   if (!dense_rows(flags, table, table_bytes, &d)) return;
-  const int32_t i = static_cast<int32_t>(blockIdx.x) * static_cast<int32_t>(blockDim.x) + static_cast<int32_t>(threadIdx.x);
-  if (i >= n) return;
+  const int64_t i64 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool live = i64 < n;
+  if (!kXFlags && !live) return;
+  // (with kXFlags every lane of a warp stays for the shuffles; lanes past
+  // the end compute the last voxel's entries and store nothing)
+  const int32_t i = live ? static_cast<int32_t>(i64) : static_cast<int32_t>(n - 1);
   const int32_t missing = static_cast<int32_t>(n);
   const int z = __ldg(coords + 3 * static_cast<int64_t>(i)), y = __ldg(coords + 3 * static_cast<int64_t>(i) + 1);
   const int x = __ldg(coords + 3 * static_cast<int64_t>(i) + 2);
@@ -483,19 +499,65 @@ __global__ void __launch_bounds__(kThreads)
     }
   };
   if constexpr (kStd27) {
+    int32_t left[9], right[9];  // (dz, dy, -1) and (dz, dy, +1) entries, group g = 3 (dz + 1) + dy + 1
 #pragma unroll
     for (int dz = -1; dz <= 1; ++dz) {
 #pragma unroll
       for (int dy = -1; dy <= 1; ++dy) {
-        const int k0 = 9 * (dz + 1) + 3 * (dy + 1);  // offset (dz, dy, -1); +1, +2 follow
+        const int g = 3 * (dz + 1) + (dy + 1);
+        const int k0 = 3 * g;  // offset (dz, dy, -1); +1, +2 follow
         int32_t rs;
         uint32_t wbase;
         row_of(z + dz, y + dy, &rs, &wbase);
-        nmap[static_cast<int64_t>(k0) * n + i] = dense_lookup(d, rs, wbase, x - 1, missing);
-        nmap[static_cast<int64_t>(k0 + 1) * n + i] =
-            (dz == 0 && dy == 0) ? i : dense_lookup(d, rs, wbase, x, missing);
-        nmap[static_cast<int64_t>(k0 + 2) * n + i] = dense_lookup(d, rs, wbase, x + 1, missing);
+        left[g] = dense_lookup(d, rs, wbase, x - 1, missing);
+        right[g] = dense_lookup(d, rs, wbase, x + 1, missing);
+        if (live) {
+          nmap[static_cast<int64_t>(k0) * n + i] = left[g];
+          nmap[static_cast<int64_t>(k0 + 1) * n + i] =
+              (dz == 0 && dy == 0) ? i : dense_lookup(d, rs, wbase, x, missing);
+          nmap[static_cast<int64_t>(k0 + 2) * n + i] = right[g];
+        }
       }
+    }
+    if constexpr (kXFlags) {
+      int32_t next_left[9];
+#pragma unroll
+      for (int g = 0; g < 9; ++g) next_left[g] = __shfl_down_sync(0xffffffffu, left[g], 1);
+      if ((threadIdx.x & 31u) == 31u && live && i + 1 < n) {
+        const int64_t j = static_cast<int64_t>(i) + 1;
+        const int zn = __ldg(coords + 3 * j), yn = __ldg(coords + 3 * j + 1), xn = __ldg(coords + 3 * j + 2);
+#pragma unroll
+        for (int g = 0; g < 9; ++g) {
+          int32_t rs;
+          uint32_t wbase;
+          row_of(zn + g / 3 - 1, yn + g % 3 - 1, &rs, &wbase);
+          next_left[g] = dense_lookup(d, rs, wbase, xn - 1, missing);
+        }
+      }
+      if (live) {
+        uint32_t f = 0;
+        if (right[4] == missing) {  // no voxel at x + 1: a run ends here
+          if (i + 1 >= n) {
+            bool any = false;
+#pragma unroll
+            for (int g = 0; g < 9; ++g) any |= right[g] != missing;
+            f = any ? 1u : 0u;
+          } else {
+            bool same = true;
+#pragma unroll
+            for (int g = 0; g < 9; ++g) same &= right[g] == next_left[g];
+            f = same ? 1u : 2u;
+          }
+        }
+        if (i == 0) {
+          bool any = false;
+#pragma unroll
+          for (int g = 0; g < 9; ++g) any |= left[g] != missing;
+          if (any) f |= 4u;
+        }
+        xflags[i] = static_cast<uint8_t>(f);
+      }
+      if (blockIdx.x == 0 && threadIdx.x == 0) flags[kFlagXrunReady] = 1;
     }
   } else {
     for (int32_t g = 0; g < plan.groups; ++g) {
@@ -703,6 +765,10 @@ __global__ void __launch_bounds__(kOrderThreads)
 
 }  // namespace
 
+const int* xrun_flags_ready(const void* workspace) {
+  return static_cast<const int*>(workspace) + kFlagXrunReady;
+}
+
 size_t hash_capacity(int64_t n) {
   size_t cap = 64;
   while (cap < static_cast<size_t>(2 * n)) cap <<= 1;
@@ -724,7 +790,7 @@ __global__ void flags_to_status_kernel(const int* flags, int32_t* status) {
 
 spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOffsets& offs,
                                 int32_t k, int32_t* nmap, void* workspace, cudaStream_t stream,
-                                int32_t* status_dev) {
+                                int32_t* status_dev, uint8_t* xflags) {
   const size_t cap = hash_capacity(n);
   int* flags = static_cast<int*>(workspace);
   Slot* table = reinterpret_cast<Slot*>(static_cast<char*>(workspace) + kFlagBytes);
@@ -821,10 +887,15 @@ spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOff
   bool std27 = k == 27;
   for (int32_t a = 0; a < k && std27; ++a)
     std27 = offs.d[3 * a] == a / 9 - 1 && offs.d[3 * a + 1] == (a / 3) % 3 - 1 && offs.d[3 * a + 2] == a % 3 - 1;
-  if (std27)
-    nmap_query_dense_kernel<true><<<grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags, plan, nmap);
+  if (std27 && xflags != nullptr)
+    nmap_query_dense_kernel<true, true><<<grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags, plan,
+                                                                       nmap, xflags);
+  else if (std27)
+    nmap_query_dense_kernel<true, false><<<grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags, plan,
+                                                                        nmap, nullptr);
   else
-    nmap_query_dense_kernel<false><<<grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags, plan, nmap);
+    nmap_query_dense_kernel<false, false><<<grid, kThreads, 0, stream>>>(coords, n, table, table_bytes, flags,
+                                                                         plan, nmap, nullptr);
   if (!cuda_ok(cudaGetLastError(), "nmap_query_dense_kernel launch", &st)) return st;
 
   // the row-hash and voxel-hash queries: grid-stride kernels on at most 16

@@ -301,6 +301,47 @@ spconv_status spconv_xrun_layout(const int32_t* coords_dev, const int32_t* nmap_
   return st == SPCONV_OK ? spconv::ok() : st;
 }
 
+size_t spconv_build_nmap_xrun_workspace_size(int64_t N) {
+  if (N < 0) return 0;
+  return (spconv_build_nmap_workspace_size(N) + 255) / 256 * 256 + spconv::xrun_workspace_bytes(N);
+}
+
+spconv_status spconv_build_nmap_xrun(const int32_t* coords_dev, int64_t N, int32_t* nmap_dev, int32_t* slots_dev,
+                                     int64_t slots_capacity, int64_t* slot_count_dev, void* workspace_dev,
+                                     size_t workspace_bytes, int32_t* status_dev, void* stream) {
+  if (N < 1 || N >= (int64_t{1} << 30)) return fail(SPCONV_ERR_INVALID_ARG, "N must be in [1, 2^30)");
+  if (coords_dev == nullptr || nmap_dev == nullptr || slots_dev == nullptr || slot_count_dev == nullptr ||
+      workspace_dev == nullptr)
+    return fail(SPCONV_ERR_INVALID_ARG, "coords, nmap, slots, slot_count and workspace must be non-NULL");
+  if (!spconv::aligned(coords_dev, 4) || !spconv::aligned(nmap_dev, 4) || !spconv::aligned(slots_dev, 4) ||
+      !spconv::aligned(slot_count_dev, 8) || !spconv::aligned(workspace_dev, 256) ||
+      (status_dev != nullptr && !spconv::aligned(status_dev, 4)))
+    return fail(SPCONV_ERR_INVALID_ARG,
+                "misaligned pointer (coords, nmap, slots, status: 4 bytes; slot_count: 8; workspace: 256)");
+  if (slots_capacity < spconv::xrun_slot_capacity(N))
+    return fail(SPCONV_ERR_INVALID_ARG, "slots_capacity below spconv_xrun_slot_capacity(N)");
+  if (workspace_bytes < spconv_build_nmap_xrun_workspace_size(N))
+    return fail(SPCONV_ERR_WORKSPACE, "workspace smaller than spconv_build_nmap_xrun_workspace_size(N)");
+  spconv_status st = spconv::check_device();
+  if (st != SPCONV_OK) return st;
+  spconv::BuildOffsets offs;
+  std::memset(&offs, 0, sizeof offs);
+  for (int32_t a = 0; a < 27; ++a) {  // the lexicographic 3x3x3 list, (dz, dy, dx)
+    offs.d[3 * a] = a / 9 - 1;
+    offs.d[3 * a + 1] = (a / 3) % 3 - 1;
+    offs.d[3 * a + 2] = a % 3 - 1;
+  }
+  void* ws_build = workspace_dev;
+  void* ws_layout = static_cast<char*>(workspace_dev) + (spconv_build_nmap_workspace_size(N) + 255) / 256 * 256;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = spconv::launch_build_nmap(coords_dev, N, offs, 27, nmap_dev, ws_build, s, status_dev,
+                                 spconv::xrun_flags(ws_layout));
+  if (st != SPCONV_OK) return st;
+  st = spconv::launch_xrun_layout(coords_dev, nmap_dev, N, slots_dev, slots_capacity, slot_count_dev, ws_layout, s,
+                                  spconv::xrun_flags_ready(ws_build));
+  return st == SPCONV_OK ? spconv::ok() : st;
+}
+
 spconv_status spconv_submconv3d_xrun(const void* feats_dev, const int32_t* nmap_dev, const int32_t* slots_dev,
                                      int64_t slots_capacity, const int64_t* slot_count_dev, const void* w_dev,
                                      const void* bias_dev, void* out_dev, int64_t N, int32_t K, int32_t Ci,

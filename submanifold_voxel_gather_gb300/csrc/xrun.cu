@@ -49,14 +49,20 @@ __device__ __forceinline__ bool same_run(const int32_t* coords, int64_t a) {
 
 // Per voxel: bits 0-1 = separators after it (0..2), bit 2 = a separator
 // before it (voxel 0 only).  Block sums of the slot counts 1 + both.
+// With `ready` set (the map build's dense query wrote the flags from the
+// entries it had in registers), the flags are only read.
 __global__ void __launch_bounds__(kXrunBlock) xrun_count_kernel(const int32_t* __restrict__ coords,
                                                                 const int32_t* __restrict__ nmap, int64_t n,
                                                                 uint8_t* __restrict__ flags,
-                                                                int64_t* __restrict__ block_sums) {
+                                                                int64_t* __restrict__ block_sums,
+                                                                const int* __restrict__ ready) {
   __shared__ int64_t warp_sums[kXrunBlock / 32];
   const int64_t i = static_cast<int64_t>(blockIdx.x) * kXrunBlock + threadIdx.x;
+  const bool pre = ready != nullptr && *ready != 0;
   uint32_t f = 0;
-  if (i < n) {
+  if (i < n && pre) {
+    f = flags[i];
+  } else if (i < n) {
     const bool run_end = i + 1 >= n || !same_run(coords, i);
     if (run_end) {
       if (i + 1 >= n) {
@@ -163,18 +169,22 @@ size_t xrun_workspace_bytes(int64_t n) {
 
 int64_t xrun_slot_capacity(int64_t n) { return 3 * n + 1; }
 
+uint8_t* xrun_flags(void* workspace) { return static_cast<uint8_t*>(workspace); }
+
 // Workspace: per-voxel flags (N bytes, rounded up to 256), the block sums,
 // and an overflow word (set if the slots would pass `cap`; never with
 // cap >= xrun_slot_capacity(n)).
 spconv_status launch_xrun_layout(const int32_t* coords, const int32_t* nmap, int64_t n, int32_t* slots,
-                                 int64_t cap, int64_t* slot_count, void* workspace, cudaStream_t stream) {
+                                 int64_t cap, int64_t* slot_count, void* workspace, cudaStream_t stream,
+                                 const int* flags_ready) {
   const int64_t nb = (n + kXrunBlock - 1) / kXrunBlock;
   uint8_t* flags = static_cast<uint8_t*>(workspace);
   int64_t* block_sums = reinterpret_cast<int64_t*>(static_cast<uint8_t*>(workspace) + ((n + 255) / 256) * 256);
   int32_t* overflow = reinterpret_cast<int32_t*>(block_sums + nb);
   spconv_status st = SPCONV_OK;
   if (!cuda_ok(cudaMemsetAsync(overflow, 0, sizeof(int32_t), stream), "cudaMemsetAsync", &st)) return st;
-  xrun_count_kernel<<<static_cast<unsigned>(nb), kXrunBlock, 0, stream>>>(coords, nmap, n, flags, block_sums);
+  xrun_count_kernel<<<static_cast<unsigned>(nb), kXrunBlock, 0, stream>>>(coords, nmap, n, flags, block_sums,
+                                                                         flags_ready);
   if (!cuda_ok(cudaGetLastError(), "xrun_count_kernel", &st)) return st;
   xrun_scan_kernel<<<1, kXrunBlock, 0, stream>>>(block_sums, nb, slot_count);
   if (!cuda_ok(cudaGetLastError(), "xrun_scan_kernel", &st)) return st;

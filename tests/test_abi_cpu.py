@@ -167,6 +167,24 @@ def test_xrun_entry_points_validate_without_gpu(lib):
     assert _status(xd(fake, fake, fake, 0, fake, fake, fake, n, 27, 64, 128, 2, None))[0] == -1
 
 
+def test_fused_build_and_layout_validates_without_gpu(lib):
+    fake = ctypes.c_void_p(0x100000)  # never dereferenced: validation fails first
+    n = 10
+    cap = lib.spconv_xrun_slot_capacity(n)
+    ws = lib.spconv_build_nmap_xrun_workspace_size(n)
+    assert ws >= lib.spconv_build_nmap_workspace_size(n) + lib.spconv_xrun_workspace_size(n)
+    assert lib.spconv_build_nmap_xrun_workspace_size(-1) == 0
+    bx = lib.spconv_build_nmap_xrun
+    assert _status(bx(fake, 0, fake, fake, cap, fake, fake, ws, None, None))[0] == -1
+    assert _status(bx(fake, 1 << 30, fake, fake, 1 << 32, fake, fake, 1 << 40, None, None))[0] == -1
+    assert _status(bx(None, n, fake, fake, cap, fake, fake, ws, None, None))[0] == -1
+    assert _status(bx(fake, n, fake, fake, cap - 1, fake, fake, ws, None, None))[0] == -1
+    assert _status(bx(fake, n, fake, fake, cap, ctypes.c_void_p(0x100004), fake, ws, None, None))[0] == -1
+    assert _status(bx(fake, n, fake, fake, cap, fake, ctypes.c_void_p(0x100080), ws, None, None))[0] == -1
+    assert _status(bx(fake, n, fake, fake, cap, fake, fake, ws, ctypes.c_void_p(0x100002), None))[0] == -1
+    assert _status(bx(fake, n, fake, fake, cap, fake, fake, ws - 1, None, None))[0] == -3
+
+
 def test_python_binding_rejects_cpu_tensors(lib):
     torch = pytest.importorskip("torch")
     with pytest.raises(TypeError):

@@ -169,3 +169,47 @@ def test_xrun_dgrad_matches_oracle_and_plain(sv, oracle_mod, name, ci):
     assert_within(to_f64(got), ref, dabs, "bf16")
     assert_near_plain(got, plain, dabs)
 
+
+
+@pytest.mark.parametrize("name", ["random", "dense", "line", "isolated", "single", "shuffled", "small", "wide"])
+def test_fused_build_and_layout_equal_the_two_calls(sv, oracle_mod, name):
+    """spconv_build_nmap_xrun gives the oracle's map and the layout of its
+    definition (the dense-row build writes the layout's flags itself; shuffled
+    input and a box too large for the dense rows take the other build paths,
+    where the layout reads the map), equal to build_nmap + xrun_layout."""
+    import torch
+    if name == "small":
+        coords = W.coords_only("small")
+    elif name == "wide":  # sorted, but a bounding box of 2^60 cells: the row-hash build
+        coords = np.concatenate([W.coords_only("small"), np.array([[(1 << 20) - 1] * 3], np.int32)])
+    else:
+        coords = shapes()[name]
+    c = torch.from_numpy(np.ascontiguousarray(coords, dtype=np.int32)).cuda()
+    nm, slots, count = sv.build_nmap_xrun(c)
+    s = int(count.item())
+    ref_map = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    np.testing.assert_array_equal(nm.cpu().numpy(), ref_map)
+    np.testing.assert_array_equal(slots[:s].cpu().numpy(), layout_reference(coords, ref_map))
+    nm2 = sv.build_nmap(c)
+    slots2, count2 = sv.xrun_layout(c, nm2)
+    assert int(count2.item()) == s
+    assert torch.equal(slots[:s], slots2[:s])
+    status = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    nm3, slots3, count3 = sv.build_nmap_xrun(c, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and torch.equal(nm3, nm) and int(count3.item()) == s
+    assert torch.equal(slots3[:s], slots[:s])
+
+
+def test_fused_build_and_layout_at_full_size(sv, oracle_mod):
+    """Decoder-scale workload (11.8 M voxels, dense-row build): the fused
+    call's map and layout equal the two separate calls'."""
+    import torch
+    c = torch.from_numpy(W.coords_only("decoder")).cuda()
+    nm, slots, count = sv.build_nmap_xrun(c)
+    nm2 = sv.build_nmap(c)
+    slots2, count2 = sv.xrun_layout(c, nm2)
+    assert torch.equal(nm, nm2)
+    assert int(count.item()) == int(count2.item())
+    s = int(count.item())
+    assert torch.equal(slots[:s], slots2[:s])
