@@ -703,9 +703,17 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
-  int clusters = 0;
-  if (!cuda_ok(cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg), "cudaOccupancyMaxActiveClusters", &st))
-    return st;
+  // co-resident pairs, looked up once per device and direction
+  constexpr int kMaxDevices = 64;
+  static int cached[kMaxDevices][2] = {};
+  int dev = 0;
+  if (!cuda_ok(cudaGetDevice(&dev), "cudaGetDevice", &st)) return st;
+  int clusters = (dev >= 0 && dev < kMaxDevices) ? cached[dev][dgrad ? 1 : 0] : 0;
+  if (clusters <= 0) {
+    if (!cuda_ok(cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg), "cudaOccupancyMaxActiveClusters", &st))
+      return st;
+    if (dev >= 0 && dev < kMaxDevices) cached[dev][dgrad ? 1 : 0] = clusters;
+  }
   if (clusters < 1) return fail(SPCONV_ERR_UNSUPPORTED, "x-run conv: no CTA pair fits on this device");
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (clusters < sms / 2 ? clusters : sms / 2)), 1, 1);
   if (!cuda_ok(cudaLaunchKernelEx(&cfg, kern, tm_w, p), "submconv_xrun_kernel", &st)) return st;
