@@ -462,14 +462,10 @@ __device__ __forceinline__ int32_t dense_lookup(const DenseRows& d, int32_t rs, 
 
 // Sorted input, dense rows: nmap[k, n] for every offset, by one row-start
 // load per (dz, dy) row and one occupancy-word load per offset.
-// kXFlags (lexicographic 3x3x3 list only): also the x-run layout's flag of
-// each voxel (xrun.cu), from the entries in registers: bits 0-1 the
-// separators after the voxel (0 inside a run; at a run end 1 when its nine
-// (dz, dy, +1) entries equal the next voxel's nine (dz, dy, -1) entries,
-// else 2; after the last voxel 1 when one of its (dz, dy, +1) cells is
-// active), bit 2 a separator before voxel 0 (one of its (dz, dy, -1) cells
-// is active).  The next voxel's entries come from the next lane; the last
-// lane of a warp computes them itself.
+// kXFlags (lexicographic 3x3x3 list only): also what the x-run layout
+// (xrun.cu) needs of each voxel, from the entries in registers: bit 0 the
+// voxel ends a run (no voxel at x + 1), bit 1 one of its nine (dz, dy, +1)
+// cells is active, bit 2 one of its nine (dz, dy, -1) cells is active.
 template <bool kStd27, bool kXFlags>
 __global__ void __launch_bounds__(kThreads)
     nmap_query_dense_kernel(const int32_t* __restrict__ coords, int64_t n, void* table,
@@ -480,11 +476,9 @@ __global__ void __launch_bounds__(kThreads)
   DenseRows d;
   if (!dense_rows(flags, table, table_bytes, &d)) return;
   const int64_t i64 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const bool live = i64 < n;
-  if (!kXFlags && !live) return;
-  // (with kXFlags every lane of a warp stays for the shuffles; lanes past
-  // the end compute the last voxel's entries and store nothing)
-  const int32_t i = live ? static_cast<int32_t>(i64) : static_cast<int32_t>(n - 1);
+  if (i64 >= n) return;
+  constexpr bool live = true;
+  const int32_t i = static_cast<int32_t>(i64);
   const int32_t missing = static_cast<int32_t>(n);
   const int z = __ldg(coords + 3 * static_cast<int64_t>(i)), y = __ldg(coords + 3 * static_cast<int64_t>(i) + 1);
   const int x = __ldg(coords + 3 * static_cast<int64_t>(i) + 2);
@@ -520,42 +514,15 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     if constexpr (kXFlags) {
-      int32_t next_left[9];
-#pragma unroll
-      for (int g = 0; g < 9; ++g) next_left[g] = __shfl_down_sync(0xffffffffu, left[g], 1);
-      if ((threadIdx.x & 31u) == 31u && live && i + 1 < n) {
-        const int64_t j = static_cast<int64_t>(i) + 1;
-        const int zn = __ldg(coords + 3 * j), yn = __ldg(coords + 3 * j + 1), xn = __ldg(coords + 3 * j + 2);
+      if (live) {
+        bool any_right = false, any_left = false;
 #pragma unroll
         for (int g = 0; g < 9; ++g) {
-          int32_t rs;
-          uint32_t wbase;
-          row_of(zn + g / 3 - 1, yn + g % 3 - 1, &rs, &wbase);
-          next_left[g] = dense_lookup(d, rs, wbase, xn - 1, missing);
+          any_right |= right[g] != missing;
+          any_left |= left[g] != missing;
         }
-      }
-      if (live) {
-        uint32_t f = 0;
-        if (right[4] == missing) {  // no voxel at x + 1: a run ends here
-          if (i + 1 >= n) {
-            bool any = false;
-#pragma unroll
-            for (int g = 0; g < 9; ++g) any |= right[g] != missing;
-            f = any ? 1u : 0u;
-          } else {
-            bool same = true;
-#pragma unroll
-            for (int g = 0; g < 9; ++g) same &= right[g] == next_left[g];
-            f = same ? 1u : 2u;
-          }
-        }
-        if (i == 0) {
-          bool any = false;
-#pragma unroll
-          for (int g = 0; g < 9; ++g) any |= left[g] != missing;
-          if (any) f |= 4u;
-        }
-        xflags[i] = static_cast<uint8_t>(f);
+        xflags[i] = static_cast<uint8_t>((right[4] == missing ? 1u : 0u) | (any_right ? 2u : 0u) |
+                                         (any_left ? 4u : 0u));
       }
       if (blockIdx.x == 0 && threadIdx.x == 0) flags[kFlagXrunReady] = 1;
     }

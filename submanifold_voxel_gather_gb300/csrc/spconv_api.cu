@@ -335,7 +335,7 @@ spconv_status spconv_build_nmap_xrun(const int32_t* coords_dev, int64_t N, int32
   void* ws_layout = static_cast<char*>(workspace_dev) + (spconv_build_nmap_workspace_size(N) + 255) / 256 * 256;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = spconv::launch_build_nmap(coords_dev, N, offs, 27, nmap_dev, ws_build, s, status_dev,
-                                 spconv::xrun_flags(ws_layout));
+                                 spconv::xrun_raw_bits(ws_layout, N));
   if (st != SPCONV_OK) return st;
   st = spconv::launch_xrun_layout(coords_dev, nmap_dev, N, slots_dev, slots_capacity, slot_count_dev, ws_layout, s,
                                   spconv::xrun_flags_ready(ws_build));

@@ -49,19 +49,38 @@ __device__ __forceinline__ bool same_run(const int32_t* coords, int64_t a) {
 
 // Per voxel: bits 0-1 = separators after it (0..2), bit 2 = a separator
 // before it (voxel 0 only).  Block sums of the slot counts 1 + both.
-// With `ready` set (the map build's dense query wrote the flags from the
-// entries it had in registers), the flags are only read.
+// With `ready` set, the map build's dense query has written three bits per
+// voxel to `raw` (bit 0: a run ends at the voxel, bit 1: one of its nine
+// (dz, dy, +1) cells is active, bit 2: one of its nine (dz, dy, -1) cells
+// is active), and the map is not read: a run end's right cells and the next
+// voxel's left cells have equal map entries in all nine groups exactly when
+// they are the same cells (the next voxel two cells further on the same
+// line) or none of them is active.
 __global__ void __launch_bounds__(kXrunBlock) xrun_count_kernel(const int32_t* __restrict__ coords,
                                                                 const int32_t* __restrict__ nmap, int64_t n,
                                                                 uint8_t* __restrict__ flags,
                                                                 int64_t* __restrict__ block_sums,
-                                                                const int* __restrict__ ready) {
+                                                                const int* __restrict__ ready,
+                                                                const uint8_t* __restrict__ raw) {
   __shared__ int64_t warp_sums[kXrunBlock / 32];
   const int64_t i = static_cast<int64_t>(blockIdx.x) * kXrunBlock + threadIdx.x;
   const bool pre = ready != nullptr && *ready != 0;
   uint32_t f = 0;
   if (i < n && pre) {
-    f = flags[i];
+    const uint32_t a = raw[i];
+    if (a & 1u) {
+      if (i + 1 >= n) {
+        f = (a & 2u) ? 1u : 0u;
+      } else {
+        const int32_t* c = coords + 3 * i;
+        const bool shared_cells = __ldg(c + 3) == __ldg(c) && __ldg(c + 4) == __ldg(c + 1) &&
+                                  __ldg(c + 5) == __ldg(c + 2) + 2;
+        const bool same = shared_cells || ((a & 2u) == 0u && (raw[i + 1] & 4u) == 0u);
+        f = same ? 1u : 2u;
+      }
+    }
+    if (i == 0 && (a & 4u)) f |= 4u;
+    flags[i] = static_cast<uint8_t>(f);
   } else if (i < n) {
     const bool run_end = i + 1 >= n || !same_run(coords, i);
     if (run_end) {
@@ -164,14 +183,16 @@ __global__ void __launch_bounds__(kXrunBlock) xrun_fill_kernel(const uint8_t* __
 
 size_t xrun_workspace_bytes(int64_t n) {
   const int64_t nb = (n + kXrunBlock - 1) / kXrunBlock;
-  return static_cast<size_t>(((n + 255) / 256) * 256) + static_cast<size_t>(nb) * 8u + 256u;
+  return 2 * static_cast<size_t>(((n + 255) / 256) * 256) + static_cast<size_t>(nb) * 8u + 256u;
 }
 
 int64_t xrun_slot_capacity(int64_t n) { return 3 * n + 1; }
 
-uint8_t* xrun_flags(void* workspace) { return static_cast<uint8_t*>(workspace); }
+// The per-voxel bits the map build's dense query writes (after the flags).
+uint8_t* xrun_raw_bits(void* workspace, int64_t n) { return static_cast<uint8_t*>(workspace) + ((n + 255) / 256) * 256; }
 
-// Workspace: per-voxel flags (N bytes, rounded up to 256), the block sums,
+// Workspace: per-voxel flags (N bytes, rounded up to 256), the map build's
+// per-voxel bits (the same), the block sums,
 // and an overflow word (set if the slots would pass `cap`; never with
 // cap >= xrun_slot_capacity(n)).
 spconv_status launch_xrun_layout(const int32_t* coords, const int32_t* nmap, int64_t n, int32_t* slots,
@@ -179,12 +200,13 @@ spconv_status launch_xrun_layout(const int32_t* coords, const int32_t* nmap, int
                                  const int* flags_ready) {
   const int64_t nb = (n + kXrunBlock - 1) / kXrunBlock;
   uint8_t* flags = static_cast<uint8_t*>(workspace);
-  int64_t* block_sums = reinterpret_cast<int64_t*>(static_cast<uint8_t*>(workspace) + ((n + 255) / 256) * 256);
+  uint8_t* raw = xrun_raw_bits(workspace, n);
+  int64_t* block_sums = reinterpret_cast<int64_t*>(static_cast<uint8_t*>(workspace) + 2 * ((n + 255) / 256) * 256);
   int32_t* overflow = reinterpret_cast<int32_t*>(block_sums + nb);
   spconv_status st = SPCONV_OK;
   if (!cuda_ok(cudaMemsetAsync(overflow, 0, sizeof(int32_t), stream), "cudaMemsetAsync", &st)) return st;
   xrun_count_kernel<<<static_cast<unsigned>(nb), kXrunBlock, 0, stream>>>(coords, nmap, n, flags, block_sums,
-                                                                         flags_ready);
+                                                                         flags_ready, raw);
   if (!cuda_ok(cudaGetLastError(), "xrun_count_kernel", &st)) return st;
   xrun_scan_kernel<<<1, kXrunBlock, 0, stream>>>(block_sums, nb, slot_count);
   if (!cuda_ok(cudaGetLastError(), "xrun_scan_kernel", &st)) return st;
