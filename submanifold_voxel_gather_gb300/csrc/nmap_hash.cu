@@ -477,7 +477,6 @@ __global__ void __launch_bounds__(kThreads)
   if (!dense_rows(flags, table, table_bytes, &d)) return;
   const int64_t i64 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i64 >= n) return;
-  constexpr bool live = true;
   const int32_t i = static_cast<int32_t>(i64);
   const int32_t missing = static_cast<int32_t>(n);
   const int z = __ldg(coords + 3 * static_cast<int64_t>(i)), y = __ldg(coords + 3 * static_cast<int64_t>(i) + 1);
@@ -493,37 +492,30 @@ __global__ void __launch_bounds__(kThreads)
     }
   };
   if constexpr (kStd27) {
-    int32_t left[9], right[9];  // (dz, dy, -1) and (dz, dy, +1) entries, group g = 3 (dz + 1) + dy + 1
+    bool any_left = false, any_right = false, run_end = false;  // kXFlags: folded as the rows go
 #pragma unroll
     for (int dz = -1; dz <= 1; ++dz) {
 #pragma unroll
       for (int dy = -1; dy <= 1; ++dy) {
-        const int g = 3 * (dz + 1) + (dy + 1);
-        const int k0 = 3 * g;  // offset (dz, dy, -1); +1, +2 follow
+        const int k0 = 9 * (dz + 1) + 3 * (dy + 1);  // offset (dz, dy, -1); +1, +2 follow
         int32_t rs;
         uint32_t wbase;
         row_of(z + dz, y + dy, &rs, &wbase);
-        left[g] = dense_lookup(d, rs, wbase, x - 1, missing);
-        right[g] = dense_lookup(d, rs, wbase, x + 1, missing);
-        if (live) {
-          nmap[static_cast<int64_t>(k0) * n + i] = left[g];
-          nmap[static_cast<int64_t>(k0 + 1) * n + i] =
-              (dz == 0 && dy == 0) ? i : dense_lookup(d, rs, wbase, x, missing);
-          nmap[static_cast<int64_t>(k0 + 2) * n + i] = right[g];
+        const int32_t left = dense_lookup(d, rs, wbase, x - 1, missing);
+        const int32_t right = dense_lookup(d, rs, wbase, x + 1, missing);
+        nmap[static_cast<int64_t>(k0) * n + i] = left;
+        nmap[static_cast<int64_t>(k0 + 1) * n + i] =
+            (dz == 0 && dy == 0) ? i : dense_lookup(d, rs, wbase, x, missing);
+        nmap[static_cast<int64_t>(k0 + 2) * n + i] = right;
+        if constexpr (kXFlags) {
+          any_left |= left != missing;
+          any_right |= right != missing;
+          if (dz == 0 && dy == 0) run_end = right == missing;
         }
       }
     }
     if constexpr (kXFlags) {
-      if (live) {
-        bool any_right = false, any_left = false;
-#pragma unroll
-        for (int g = 0; g < 9; ++g) {
-          any_right |= right[g] != missing;
-          any_left |= left[g] != missing;
-        }
-        xflags[i] = static_cast<uint8_t>((right[4] == missing ? 1u : 0u) | (any_right ? 2u : 0u) |
-                                         (any_left ? 4u : 0u));
-      }
+      xflags[i] = static_cast<uint8_t>((run_end ? 1u : 0u) | (any_right ? 2u : 0u) | (any_left ? 4u : 0u));
       if (blockIdx.x == 0 && threadIdx.x == 0) flags[kFlagXrunReady] = 1;
     }
   } else {
