@@ -69,6 +69,8 @@ def parse_args():
     ap.add_argument("--e2e-slots", type=int, default=3,
                     help="end-to-end steps in flight (one stream and buffer set each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-epilogue", action="store_true",
+                    help="skip timing the fused residual + SiLU epilogue against the plain conv")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="approximate CPU work of the oracle baseline sample")
     ap.add_argument("--materialized", action="store_true",
@@ -562,6 +564,20 @@ def copy_bandwidths(torch, dev, d_in, h_in, d_out, h_out, streams, reps=3):
             "both_gbs": (h2d + d2h) / t_both / 1e6}
 
 
+def time_calls(torch, fn, stream, reps=5, warmup=2):
+    """Mean device time of fn() over reps calls (CUDA events on `stream`)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 def xrun_supported(layer, wl):
     """Shapes the row-shifted conv takes: bf16, Ci = 128, Co <= 128, the 27
     lexicographic 3x3x3 offsets."""
@@ -687,6 +703,28 @@ def run_ours(args):
                   "allocated_during_build": during_build, "allocated_during_conv": during_conv,
                   "gather_materialised_bytes": 0,
                   "note": "nmap (4*K*N bytes) is the build's output and the conv's input, not counted"}
+
+    # ---- the fused epilogue out = SiLU(conv + bias + residual) against the
+    # plain conv, on the same map and the same conv kernel
+    epilogue = None
+    if not args.no_epilogue:
+        res = out.clone()
+        out2 = torch.empty_like(out)
+
+        def fused_conv():
+            if xrun is not None:
+                sv.submconv3d_xrun(feats, nmap, xrun["slots"], xrun["count"], w, bias, out=out2, residual=res,
+                                   activation="silu")
+            else:
+                sv.submconv3d(feats, nmap, w, bias, out=out2, residual=res, activation="silu", dtype=tf)
+
+        plain_ms = time_calls(torch, lambda: conv(feats, nmap, w, bias, out2, xrun), stream)
+        fused_ms = time_calls(torch, fused_conv, stream)
+        sv.device_status()
+        epilogue = {"plain_ms": plain_ms, "fused_ms": fused_ms, "ratio": fused_ms / plain_ms,
+                    "act": "silu", "residual": True}
+        del res, out2
+        torch.cuda.empty_cache()
 
     # ---- end to end through the public API with pinned host buffers
     e2e = None
@@ -847,6 +885,7 @@ def run_ours(args):
         "peak_extra": peak_extra,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        **({"epilogue": epilogue} if epilogue is not None else {}),
         # per step: the map build's eight kernels (flag reset, range/order/box
         # check, clear, insert, dense-row prefix, dense-row query, row-hash
         # query, voxel-hash query: the paths not taken return at once) and

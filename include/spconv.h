@@ -430,6 +430,31 @@ spconv_status spconv_submconv3d_xrun(const void* feats_dev, const int32_t* nmap_
                                      int32_t Co, spconv_dtype dtype, void* stream);
 
 /*
+ * spconv_submconv3d_xrun with the fused epilogue of spconv_submconv3d_ex:
+ *
+ *     out[n, co] = act(conv[n, co] + bias[co] + residual[n, co])
+ *
+ * in fp32 on the accumulator, then one rounding to bf16.  An extension for
+ * chaining decoder layers (the page runs the convolution layer after layer,
+ * "sparse_conv_metal.py" module docstring, and defines no epilogue beyond
+ * the bias).
+ *
+ *  residual_dev  (N, Co) bf16, 16-byte aligned, or NULL for none.  It may
+ *                be the same buffer as out_dev (an in-place residual
+ *                update); it must not overlap feats_dev.
+ *  act           SPCONV_ACT_NONE, SPCONV_ACT_RELU or SPCONV_ACT_SILU; any
+ *                other value gives SPCONV_ERR_INVALID_ARG.
+ *
+ * Other arguments, shapes and errors as spconv_submconv3d_xrun; with
+ * residual_dev == NULL and SPCONV_ACT_NONE the two calls are the same.
+ */
+spconv_status spconv_submconv3d_xrun_ex(const void* feats_dev, const int32_t* nmap_dev, const int32_t* slots_dev,
+                                        int64_t slots_capacity, const int64_t* slot_count_dev, const void* w_dev,
+                                        const void* bias_dev, const void* residual_dev, void* out_dev, int64_t N,
+                                        int32_t K, int32_t Ci, int32_t Co, spconv_dtype dtype,
+                                        spconv_activation act, void* stream);
+
+/*
  * spconv_submconv3d_dgrad over an x-run slot layout: dfeats (N, Ci) from
  * dout (N, Co), dfeats[n] = sum_k dout[nmap[k, n]] . w[K-1-k]^T (the map of
  * the 3x3x3 offsets is symmetric), with the row-shifted operands of

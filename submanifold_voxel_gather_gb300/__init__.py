@@ -108,6 +108,9 @@ def load_library() -> ctypes.CDLL:
         lib.spconv_submconv3d_xrun.argtypes = [vp, vp, vp, i64, vp, vp, vp, vp, i64, i32, i32, i32,
                                                ctypes.c_int, vp]
         lib.spconv_submconv3d_xrun.restype = ctypes.c_int
+        lib.spconv_submconv3d_xrun_ex.argtypes = [vp, vp, vp, i64, vp, vp, vp, vp, vp, i64, i32, i32, i32,
+                                                  ctypes.c_int, ctypes.c_int, vp]
+        lib.spconv_submconv3d_xrun_ex.restype = ctypes.c_int
         lib.spconv_submconv3d_dgrad_xrun.argtypes = [vp, vp, vp, i64, vp, vp, vp, i64, i32, i32, i32,
                                                      ctypes.c_int, vp]
         lib.spconv_submconv3d_dgrad_xrun.restype = ctypes.c_int
@@ -425,10 +428,15 @@ def build_nmap_xrun(coords, out=None, slots=None, slot_count=None, workspace=Non
     return out, slots, slot_count
 
 
-def submconv3d_xrun(feats, nmap, slots, slot_count, w, bias=None, out=None, stream=None):
+def submconv3d_xrun(feats, nmap, slots, slot_count, w, bias=None, out=None, stream=None, residual=None,
+                    activation=None):
     """``submconv3d`` over an x-run slot layout from ``xrun_layout``
     (spconv_submconv3d_xrun): bf16, K = 27, Ci = 128, Co <= 128.  Returns out
-    (N, Co)."""
+    (N, Co).
+
+    ``residual`` (N, Co) and ``activation`` ("relu" or "silu") select the
+    fused epilogue out = act(conv + bias + residual)
+    (spconv_submconv3d_xrun_ex); ``out`` may be the residual tensor itself."""
     torch = _torch()
     _require_cuda(feats, "feats", torch.bfloat16)
     _require_cuda(nmap, "nmap", torch.int32)
@@ -449,9 +457,22 @@ def submconv3d_xrun(feats, nmap, slots, slot_count, w, bias=None, out=None, stre
         _require_cuda(out, "out", feats.dtype)
         if tuple(out.shape) != (n, co):
             raise ValueError("out must have shape (N, Co)")
-    _check(load_library().spconv_submconv3d_xrun(_ptr(feats), _ptr(nmap), _ptr(slots), slots.numel(),
-                                                 _ptr(slot_count), _ptr(w), _ptr(bias), _ptr(out), n, k, ci, co,
-                                                 BF16, _stream_handle(stream)))
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(a for a in ACTIVATIONS if a)}")
+    if residual is not None:
+        _require_cuda(residual, "residual", torch.bfloat16)
+        if tuple(residual.shape) != (n, co):
+            raise ValueError("residual must have shape (N, Co)")
+    act = ACTIVATIONS[activation]
+    lib = load_library()
+    if residual is None and act == 0:
+        _check(lib.spconv_submconv3d_xrun(_ptr(feats), _ptr(nmap), _ptr(slots), slots.numel(), _ptr(slot_count),
+                                          _ptr(w), _ptr(bias), _ptr(out), n, k, ci, co, BF16,
+                                          _stream_handle(stream)))
+    else:
+        _check(lib.spconv_submconv3d_xrun_ex(_ptr(feats), _ptr(nmap), _ptr(slots), slots.numel(),
+                                             _ptr(slot_count), _ptr(w), _ptr(bias), _ptr(residual), _ptr(out), n,
+                                             k, ci, co, BF16, act, _stream_handle(stream)))
     return out
 
 

@@ -29,8 +29,9 @@
 //   warp 1     MMA issuer: per kept group, 3 offsets x 2 chunks x 4 MMAs of
 //              M = 128 channels, N = 256 slots, K = 16, fp32 in tensor memory
 //              (two accumulator buffers);
-//   warps 4-7  epilogue: + bias, one rounding to bf16, rows of voxel slots
-//              stored, separator rows dropped.
+//   warps 4-7  epilogue: + bias (and, fused, + residual and ReLU/SiLU), one
+//              rounding to bf16, rows of voxel slots stored, separator rows
+//              dropped.
 // Every mbarrier wait is bounded; on timeout the kernel records an error bit,
 // drains its own loads and MMAs, frees its tensor memory and returns.
 #include <cuda_bf16.h>
@@ -38,6 +39,7 @@
 
 #include <mutex>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -64,6 +66,10 @@ constexpr int kRingRow = kGRowsAlloc;         // int32 entries per ring row
 constexpr int kProducerWarp0 = 8;
 constexpr int kProducerThreads = 128;
 constexpr int kEpilogueWarp0 = 4;
+// Fused epilogue: a 32-slot chunk is staged in fp32 (16 KB); its 16-byte
+// output pieces (32 rows x Co / 8) are at most 4 per epilogue thread.
+constexpr int kFusedPieces = 32 * 16 / 128;
+constexpr uint32_t kStageBytes = 32u * 128u * 4u;
 constexpr uint64_t kAStepUnits = (16 * 128) >> 4;   // one K step of channel-major weights
 constexpr uint64_t kBStepUnits = (16 * 2) >> 4;     // one K step of K-major rows
 // An operand shifted by dxi rows in its 1024-byte-aligned chunk is the
@@ -81,8 +87,10 @@ struct XrParams {
   const int64_t* slot_count;
   int64_t slots_capacity;  // entries of slots: S is clamped to it
   const __nv_bfloat16* bias;
+  const __nv_bfloat16* residual;  // (N, co) or null; may be `out` itself
   __nv_bfloat16* out;
   int64_t n;
+  int32_t act;       // spconv_activation of the fused epilogue
   int32_t co;        // row stride of out and weights' Co
   int32_t co_count;  // channels computed (== co, <= 128)
   uint32_t idesc;
@@ -165,6 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   int32_t* ring = reinterpret_cast<int32_t*>(smem + p.off_ring);
   __nv_bfloat16* stage_out = reinterpret_cast<__nv_bfloat16*>(smem + p.off_stage_out);
+  float* stage_f32 = reinterpret_cast<float*>(smem + p.off_stage_out);  // the same memory, fused epilogue
+  const bool fused = p.residual != nullptr || p.act != SPCONV_ACT_NONE;
   int32_t* codes_s = reinterpret_cast<int32_t*>(smem + p.off_codes);
   float* bias_s = reinterpret_cast<float*>(smem + p.off_bias);
   uint32_t* wmeta = reinterpret_cast<uint32_t*>(smem + p.off_meta);
@@ -527,21 +537,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = static_cast<int>(threadIdx.x) - kEpilogueWarp0 * 32;  // 0..127
     const int chunks_per_row = p.co_count / 8;
     const int co_l = static_cast<int>(sub) * 32 + static_cast<int>(lane);
+    // Fused epilogue: the residual pieces (16 bytes each) this thread stores
+    // for chunk vc of the tile; each thread reads, then writes, the same
+    // (row, piece) pairs, so the residual may be `out` itself.
+    auto load_residual = [&](uint4 (&res)[kFusedPieces], int vc) {
+#pragma unroll
+      for (int j = 0; j < kFusedPieces; ++j) {
+        const int q = et + 128 * j;
+        const int r = q / chunks_per_row;
+        const int c8 = q - r * chunks_per_row;
+        const int32_t code = q < 32 * chunks_per_row ? codes_s[vc * 32 + r] : -1;
+        res[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (p.residual != nullptr && code >= 0 && code < n_rows)
+          res[j] = *reinterpret_cast<const uint4*>(p.residual + static_cast<int64_t>(code) * p.co + c8 * 8);
+      }
+    };
     uint32_t tile_i = 0;
     for (int64_t t = blockIdx.x; t < t_end; t += gridDim.x, ++tile_i) {
       const uint32_t buf = tile_i & 1u;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(smem_addr(&tmem_full[buf]), (tile_i >> 1) & 1u));
-      if (!epi_all(got)) break;
-      tc_fence_after();
       const int64_t s0 = t * kTileN;
-      const uint32_t tcol = tmem_base + ((sub * 32u) << 16) + buf * static_cast<uint32_t>(kTileN);
       // The tile's slot codes (the output row of each slot), read once and
-      // coalesced: a row's store then never waits on a load of its code.
+      // coalesced while the accumulator is still being computed: a row's
+      // store then never waits on a load of its code.
       epi_bar();  // the previous tile's codes are no longer read
       codes_s[et] = slot_code(p.slots, s0 + et, S);
       codes_s[et + 128] = slot_code(p.slots, s0 + et + 128, S);
+      // The residual of chunk 0 is loaded before the wait and each later
+      // chunk's while the one before it is stored, so no chunk waits on
+      // its residual's load.
+      uint4 res_cur[kFusedPieces], res_nxt[kFusedPieces];
+      if (fused) {
+        epi_bar();  // the codes are in
+        load_residual(res_cur, 0);
+      }
+      const bool got = __all_sync(0xffffffffu, mbar_wait(smem_addr(&tmem_full[buf]), (tile_i >> 1) & 1u));
+      if (!epi_all(got)) break;
+      tc_fence_after();
+      const uint32_t tcol = tmem_base + ((sub * 32u) << 16) + buf * static_cast<uint32_t>(kTileN);
       for (int vc = 0; vc < kTileN / 32; ++vc) {
         epi_bar();  // the previous chunk's staged rows have been stored (and the codes are in)
+        if (fused) {
+          if (vc + 1 < kTileN / 32) load_residual(res_nxt, vc + 1);
+          const uint4 (&res)[kFusedPieces] = res_cur;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tcol + vc * 32, v);
+          tmem_ld_wait();
+          if (co_l < p.co_count) {
+            const float b = bias_s[co_l];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) stage_f32[i * 128 + co_l] = __uint_as_float(v[i]) + b;
+          }
+          epi_bar();
+#pragma unroll
+          for (int j = 0; j < kFusedPieces; ++j) {
+            const int q = et + 128 * j;
+            if (q >= 32 * chunks_per_row) break;
+            const int r = q / chunks_per_row;
+            const int c8 = q - r * chunks_per_row;
+            const int32_t code = codes_s[vc * 32 + r];
+            if (code < 0 || code >= n_rows) continue;
+            const float4 a0 = *reinterpret_cast<const float4*>(stage_f32 + r * 128 + c8 * 8);
+            const float4 a1 = *reinterpret_cast<const float4*>(stage_f32 + r * 128 + c8 * 8 + 4);
+            const __nv_bfloat162* rh = reinterpret_cast<const __nv_bfloat162*>(&res[j]);
+            const float2 r0 = __bfloat1622float2(rh[0]), r1 = __bfloat1622float2(rh[1]);
+            const float2 r2 = __bfloat1622float2(rh[2]), r3 = __bfloat1622float2(rh[3]);
+            uint4 o;
+            __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+            oh[0] = __floats2bfloat162_rn(apply_activation_bf16(a0.x + r0.x, p.act),
+                                          apply_activation_bf16(a0.y + r0.y, p.act));
+            oh[1] = __floats2bfloat162_rn(apply_activation_bf16(a0.z + r1.x, p.act),
+                                          apply_activation_bf16(a0.w + r1.y, p.act));
+            oh[2] = __floats2bfloat162_rn(apply_activation_bf16(a1.x + r2.x, p.act),
+                                          apply_activation_bf16(a1.y + r2.y, p.act));
+            oh[3] = __floats2bfloat162_rn(apply_activation_bf16(a1.z + r3.x, p.act),
+                                          apply_activation_bf16(a1.w + r3.y, p.act));
+            *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(code) * p.co + c8 * 8) = o;
+          }
+#pragma unroll
+          for (int j = 0; j < kFusedPieces; ++j) res_cur[j] = res_nxt[j];
+          continue;
+        }
         uint32_t v[32];
         tmem_ld_32x32b_x32(tcol + vc * 32, v);
         tmem_ld_wait();
@@ -624,8 +699,8 @@ spconv_status read_and_clear_xrun_device_error(cudaStream_t stream, unsigned int
 
 spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int32_t* slots,
                                int64_t slots_capacity, const int64_t* slot_count, const void* w,
-                               const void* bias, void* out, int64_t n, int32_t co, bool dgrad,
-                               cudaStream_t stream) {
+                               const void* bias, const void* residual, void* out, int64_t n, int32_t co,
+                               int act, bool dgrad, cudaStream_t stream) {
   spconv_status st = SPCONV_OK;
   EncodeTiledFn encode = xrun_encode_fn(&st);
   if (encode == nullptr) return st;
@@ -654,8 +729,10 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
   p.slot_count = slot_count;
   p.slots_capacity = slots_capacity;
   p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.residual = static_cast<const __nv_bfloat16*>(residual);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.n = n;
+  p.act = act;
   p.co = co;
   p.co_count = co;
   // D f32, A and B bf16, A (weights) channel-major (forward) or K-major
@@ -671,7 +748,7 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
   p.off_ring = off;
   off += kXRing * kRingRow * 4u;
   p.off_stage_out = off;
-  off += 32u * 128u * 2u;
+  off += kStageBytes;  // bf16 rows, or fp32 ones for the fused epilogue
   p.off_codes = off;
   off += kTileN * 4u;
   p.off_bias = off;

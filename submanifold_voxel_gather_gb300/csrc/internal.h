@@ -93,17 +93,18 @@ size_t xrun_workspace_bytes(int64_t n);
 int64_t xrun_slot_capacity(int64_t n);
 // flags_ready (optional): a word that, when set on the device, says the map
 // build's dense query wrote its per-voxel bits at xrun_raw_bits(workspace,
-// n); the layout then decides the separators from them and the coordinates
-// instead of reading the map.
+// n); the layout then decides the separators from those bits alone instead
+// of reading the map and the coordinates.
 spconv_status launch_xrun_layout(const int32_t* coords, const int32_t* nmap, int64_t n, int32_t* slots,
                                  int64_t cap, int64_t* slot_count, void* workspace, cudaStream_t stream,
                                  const int* flags_ready = nullptr);
 uint8_t* xrun_raw_bits(void* workspace, int64_t n);
 // bf16, lexicographic 3x3x3 offsets; 128 reduced channels (forward Ci, or
-// forward Co for the input gradient) and co <= 128 output channels
+// forward Co for the input gradient) and co <= 128 output channels.
+// residual (or null) and act: the fused epilogue act(conv + bias + residual).
 spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int32_t* slots,
                                int64_t slots_capacity, const int64_t* slot_count, const void* w,
-                               const void* bias, void* out, int64_t n, int32_t co, bool dgrad,
-                               cudaStream_t stream);
+                               const void* bias, const void* residual, void* out, int64_t n, int32_t co,
+                               int act, bool dgrad, cudaStream_t stream);
 
 }  // namespace spconv

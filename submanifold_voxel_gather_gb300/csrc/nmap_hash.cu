@@ -460,12 +460,44 @@ __device__ __forceinline__ int32_t dense_lookup(const DenseRows& d, int32_t rs, 
   return rs + static_cast<int32_t>(e.y + __popc(e.x & ((1u << b) - 1u)));
 }
 
+// Dense rows: the voxels at x - 1, x and x + 1 of one row (cx = x - xmin,
+// inside the box), from the occupancy word that holds cx; the word before or
+// after it is read only when cx is its first or last bit.
+__device__ __forceinline__ void dense_lookup3(const DenseRows& d, int32_t rs, uint32_t wbase, uint32_t cx,
+                                              int32_t missing, int32_t* left, int32_t* mid, int32_t* right) {
+  *left = missing;
+  *mid = missing;
+  *right = missing;
+  if (rs < 0) return;
+  const uint32_t wi = cx >> 5, b = cx & 31u;
+  const uint2 e = __ldg(d.words + wbase + wi);
+  const int32_t base = rs + static_cast<int32_t>(e.y);
+  const uint32_t own = (e.x >> b) & 1u;
+  const int32_t rank = base + __popc(e.x & ((1u << b) - 1u));  // voxels of the row before cx
+  if (own) *mid = rank;
+  if (b > 0u) {
+    if ((e.x >> (b - 1u)) & 1u) *left = rank - 1;
+  } else if (wi > 0u) {
+    const uint2 f = __ldg(d.words + wbase + wi - 1u);
+    if (f.x >> 31) *left = rs + static_cast<int32_t>(f.y) + __popc(f.x) - 1;
+  }
+  if (b < 31u) {
+    if ((e.x >> (b + 1u)) & 1u) *right = rank + static_cast<int32_t>(own);
+  } else if (cx + 1u < static_cast<uint32_t>(d.nx)) {
+    const uint2 f = __ldg(d.words + wbase + wi + 1u);
+    if (f.x & 1u) *right = rs + static_cast<int32_t>(f.y);
+  }
+}
+
 // Sorted input, dense rows: nmap[k, n] for every offset, by one row-start
-// load per (dz, dy) row and one occupancy-word load per offset.
+// load per (dz, dy) row and, for the lexicographic 3x3x3 list, one
+// occupancy-word load per row (two at a word edge); else one per offset.
 // kXFlags (lexicographic 3x3x3 list only): also what the x-run layout
 // (xrun.cu) needs of each voxel, from the entries in registers: bit 0 the
 // voxel ends a run (no voxel at x + 1), bit 1 one of its nine (dz, dy, +1)
-// cells is active, bit 2 one of its nine (dz, dy, -1) cells is active.
+// cells is active, bit 2 one of its nine (dz, dy, -1) cells is active, bit 3
+// the voxel ends a run and the cell (z, y, x + 2) is active (then, the input
+// being sorted, that cell is the next voxel's).
 template <bool kStd27, bool kXFlags>
 __global__ void __launch_bounds__(kThreads)
     nmap_query_dense_kernel(const int32_t* __restrict__ coords, int64_t n, void* table,
@@ -492,7 +524,7 @@ __global__ void __launch_bounds__(kThreads)
     }
   };
   if constexpr (kStd27) {
-    bool any_left = false, any_right = false, run_end = false;  // kXFlags: folded as the rows go
+    bool any_left = false, any_right = false, run_end = false, next_at_2 = false;  // kXFlags
 #pragma unroll
     for (int dz = -1; dz <= 1; ++dz) {
 #pragma unroll
@@ -501,21 +533,25 @@ __global__ void __launch_bounds__(kThreads)
         int32_t rs;
         uint32_t wbase;
         row_of(z + dz, y + dy, &rs, &wbase);
-        const int32_t left = dense_lookup(d, rs, wbase, x - 1, missing);
-        const int32_t right = dense_lookup(d, rs, wbase, x + 1, missing);
+        int32_t left, mid, right;
+        dense_lookup3(d, rs, wbase, static_cast<uint32_t>(x - d.xmin), missing, &left, &mid, &right);
         nmap[static_cast<int64_t>(k0) * n + i] = left;
-        nmap[static_cast<int64_t>(k0 + 1) * n + i] =
-            (dz == 0 && dy == 0) ? i : dense_lookup(d, rs, wbase, x, missing);
+        nmap[static_cast<int64_t>(k0 + 1) * n + i] = (dz == 0 && dy == 0) ? i : mid;
         nmap[static_cast<int64_t>(k0 + 2) * n + i] = right;
         if constexpr (kXFlags) {
           any_left |= left != missing;
           any_right |= right != missing;
-          if (dz == 0 && dy == 0) run_end = right == missing;
+          if (dz == 0 && dy == 0) {
+            run_end = right == missing;
+            // sorted input: after a run end, the next voxel is (z, y, x + 2) when that cell is active
+            next_at_2 = run_end && dense_lookup(d, rs, wbase, x + 2, missing) != missing;
+          }
         }
       }
     }
     if constexpr (kXFlags) {
-      xflags[i] = static_cast<uint8_t>((run_end ? 1u : 0u) | (any_right ? 2u : 0u) | (any_left ? 4u : 0u));
+      xflags[i] = static_cast<uint8_t>((run_end ? 1u : 0u) | (any_right ? 2u : 0u) | (any_left ? 4u : 0u) |
+                                       (next_at_2 ? 8u : 0u));
       if (blockIdx.x == 0 && threadIdx.x == 0) flags[kFlagXrunReady] = 1;
     }
   } else {

@@ -346,6 +346,17 @@ spconv_status spconv_submconv3d_xrun(const void* feats_dev, const int32_t* nmap_
                                      int64_t slots_capacity, const int64_t* slot_count_dev, const void* w_dev,
                                      const void* bias_dev, void* out_dev, int64_t N, int32_t K, int32_t Ci,
                                      int32_t Co, spconv_dtype dtype, void* stream) {
+  return spconv_submconv3d_xrun_ex(feats_dev, nmap_dev, slots_dev, slots_capacity, slot_count_dev, w_dev, bias_dev,
+                                   nullptr, out_dev, N, K, Ci, Co, dtype, SPCONV_ACT_NONE, stream);
+}
+
+spconv_status spconv_submconv3d_xrun_ex(const void* feats_dev, const int32_t* nmap_dev, const int32_t* slots_dev,
+                                        int64_t slots_capacity, const int64_t* slot_count_dev, const void* w_dev,
+                                        const void* bias_dev, const void* residual_dev, void* out_dev, int64_t N,
+                                        int32_t K, int32_t Ci, int32_t Co, spconv_dtype dtype,
+                                        spconv_activation act, void* stream) {
+  if (act != SPCONV_ACT_NONE && act != SPCONV_ACT_RELU && act != SPCONV_ACT_SILU)
+    return fail(SPCONV_ERR_INVALID_ARG, "unknown activation");
   if (N < 1 || N >= (int64_t{1} << 30)) return fail(SPCONV_ERR_INVALID_ARG, "N must be in [1, 2^30)");
   if (dtype != SPCONV_BF16 || K != 27 || Ci != 128 || Co < 16 || Co > 128 || Co % 16 != 0)
     return fail(SPCONV_ERR_UNSUPPORTED, "the x-run conv takes bf16, K = 27, Ci = 128 and Co in [16, 128], a multiple of 16");
@@ -354,13 +365,15 @@ spconv_status spconv_submconv3d_xrun(const void* feats_dev, const int32_t* nmap_
     return fail(SPCONV_ERR_INVALID_ARG, "feats, nmap, slots, slot_count, w and out must be non-NULL");
   if (!spconv::aligned(feats_dev, 16) || !spconv::aligned(w_dev, 16) || !spconv::aligned(out_dev, 16) ||
       !spconv::aligned(nmap_dev, 4) || !spconv::aligned(slots_dev, 4) || !spconv::aligned(slot_count_dev, 8) ||
-      (bias_dev != nullptr && !spconv::aligned(bias_dev, 2)))
+      (bias_dev != nullptr && !spconv::aligned(bias_dev, 2)) ||
+      (residual_dev != nullptr && !spconv::aligned(residual_dev, 16)))
     return fail(SPCONV_ERR_INVALID_ARG, "misaligned pointer");
   if (slots_capacity < 1) return fail(SPCONV_ERR_INVALID_ARG, "slots_capacity must be >= 1");
   spconv_status st = spconv::check_device();
   if (st != SPCONV_OK) return st;
   st = spconv::launch_conv_xrun(feats_dev, nmap_dev, slots_dev, slots_capacity, slot_count_dev, w_dev, bias_dev,
-                                out_dev, N, Co, false, static_cast<cudaStream_t>(stream));
+                                residual_dev, out_dev, N, Co, static_cast<int>(act), false,
+                                static_cast<cudaStream_t>(stream));
   return st == SPCONV_OK ? spconv::ok() : st;
 }
 
@@ -382,7 +395,8 @@ spconv_status spconv_submconv3d_dgrad_xrun(const void* dout_dev, const int32_t* 
   spconv_status st = spconv::check_device();
   if (st != SPCONV_OK) return st;
   st = spconv::launch_conv_xrun(dout_dev, nmap_dev, slots_dev, slots_capacity, slot_count_dev, w_dev, nullptr,
-                                dfeats_dev, N, Ci, true, static_cast<cudaStream_t>(stream));
+                                nullptr, dfeats_dev, N, Ci, static_cast<int>(SPCONV_ACT_NONE), true,
+                                static_cast<cudaStream_t>(stream));
   return st == SPCONV_OK ? spconv::ok() : st;
 }
 

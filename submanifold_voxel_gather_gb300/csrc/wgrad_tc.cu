@@ -569,9 +569,25 @@ spconv_status launch_wgrad_tc(const void* feats, const void* dout, const int32_t
     p.num_groups = (p.num_atoms + kAtoms - 1) / kAtoms;
     p.total_chunks = (n + kChunkVox - 1) / kChunkVox;
     // About four items per SM: long voxel ranges keep the reductions into dw
-    // few (one 128 x 256 tile per item).
+    // few (one 128 x 256 tile per item).  Among up to twice that many ranges
+    // the count is taken whose items fill the last round over the CTAs best
+    // (with 14 atom groups and 152 SMs: 76 ranges, 7 items per CTA, instead
+    // of 44 ranges, where 8 CTAs ran a fifth item while the others waited).
     int64_t ranges = (4 * static_cast<int64_t>(sms) + p.num_groups - 1) / p.num_groups;
     if (ranges < 1) ranges = 1;
+    {
+      const int64_t r0 = ranges;
+      double best = 1e30;
+      for (int64_t r = r0; r <= 2 * r0 && r <= p.total_chunks; ++r) {
+        const int64_t items = r * p.num_groups;
+        const int64_t rounds = (items + sms - 1) / sms;
+        const double waste = static_cast<double>(rounds * sms) / static_cast<double>(items);
+        if (waste < best - 1e-9) {
+          best = waste;
+          ranges = r;
+        }
+      }
+    }
     p.chunks_per_item = (p.total_chunks + ranges - 1) / ranges;
     p.num_ranges = (p.total_chunks + p.chunks_per_item - 1) / p.chunks_per_item;
     p.num_items = static_cast<int64_t>(p.num_groups) * p.num_ranges;

@@ -34,6 +34,8 @@ namespace spconv {
 namespace {
 
 constexpr int kXrunBlock = 1024;
+constexpr int kXrunPer = 4;  // voxels per thread in the count and the fill
+constexpr int64_t kXrunSpan = static_cast<int64_t>(kXrunBlock) * kXrunPer;
 
 // Normalised map entry: the row, or n for every kind of missing entry.
 __device__ __forceinline__ int32_t map_row(const int32_t* nmap, int64_t n, int k, int64_t v) {
@@ -47,92 +49,133 @@ __device__ __forceinline__ bool same_run(const int32_t* coords, int64_t a) {
   return __ldg(p + 3) == __ldg(p) && __ldg(p + 4) == __ldg(p + 1) && __ldg(p + 5) == __ldg(p + 2) + 1;
 }
 
-// Per voxel: bits 0-1 = separators after it (0..2), bit 2 = a separator
-// before it (voxel 0 only).  Block sums of the slot counts 1 + both.
-// With `ready` set, the map build's dense query has written three bits per
-// voxel to `raw` (bit 0: a run ends at the voxel, bit 1: one of its nine
-// (dz, dy, +1) cells is active, bit 2: one of its nine (dz, dy, -1) cells
-// is active), and the map is not read: a run end's right cells and the next
-// voxel's left cells have equal map entries in all nine groups exactly when
-// they are the same cells (the next voxel two cells further on the same
-// line) or none of them is active.
+// Flags of voxel i: bits 0-1 = separators after it (0..2), bit 2 = a
+// separator before it (voxel 0 only).  From the map and the coordinates.
+__device__ __noinline__ uint32_t voxel_flags_from_map(const int32_t* coords, const int32_t* nmap, int64_t n,
+                                                         int64_t i) {
+  uint32_t f = 0;
+  const bool run_end = i + 1 >= n || !same_run(coords, i);
+  if (run_end) {
+    if (i + 1 >= n) {
+      bool any = false;
+      for (int g = 0; g < 9; ++g) any |= map_row(nmap, n, 3 * g + 2, i) != n;
+      f = any ? 1u : 0u;
+    } else {
+      bool same = true;
+      for (int g = 0; g < 9; ++g) same &= map_row(nmap, n, 3 * g + 2, i) == map_row(nmap, n, 3 * g, i + 1);
+      f = same ? 1u : 2u;
+    }
+  }
+  if (i == 0) {
+    bool any = false;
+    for (int g = 0; g < 9; ++g) any |= map_row(nmap, n, 3 * g, 0) != n;
+    if (any) f |= 4u;
+  }
+  return f;
+}
+
+// The same flags from the bits the map build's dense query writes per voxel
+// (sorted input only): bit 0 a run ends at the voxel, bit 1 one of its nine
+// (dz, dy, +1) cells is active, bit 2 one of its nine (dz, dy, -1) cells is
+// active, bit 3 it ends a run and the next voxel is two cells further on its
+// line.  A run end's right cells and the next voxel's left cells have equal
+// map entries in all nine groups exactly when they are the same cells or none
+// of them is active.  `a` is the voxel's bits, `a_next` the next voxel's.
+__device__ __forceinline__ uint32_t voxel_flags_from_bits(int64_t i, int64_t n, uint32_t a, uint32_t a_next) {
+  uint32_t f = 0;
+  if (a & 1u) {
+    if (i + 1 >= n) f = (a & 2u) ? 1u : 0u;
+    else f = ((a & 8u) != 0u || ((a & 2u) == 0u && (a_next & 4u) == 0u)) ? 1u : 2u;
+  }
+  if (i == 0 && (a & 4u)) f |= 4u;
+  return f;
+}
+
+__device__ __forceinline__ uint32_t slot_count_of(uint32_t f) { return 1u + (f & 3u) + ((f >> 2) & 1u); }
+
+// The flags of voxels i0 .. i0 + kXrunPer - 1, one byte each (0 past n).
+// With the dense query's bits (`pre`), computed from them; else read from
+// `flags`, which the count wrote.  Both buffers are padded to 256 bytes.
+__device__ __forceinline__ uint32_t flags4(const uint8_t* flags, const uint8_t* raw, bool pre, int64_t n,
+                                           int64_t i0) {
+  if (!pre) return *reinterpret_cast<const uint32_t*>(flags + i0);
+  const uint32_t a4 = *reinterpret_cast<const uint32_t*>(raw + i0);
+  const uint32_t a_after = i0 + kXrunPer < n ? raw[i0 + kXrunPer] : 0u;
+  uint32_t packed = 0;
+#pragma unroll
+  for (int j = 0; j < kXrunPer; ++j) {
+    const uint32_t a = (a4 >> (8 * j)) & 0xffu;
+    const uint32_t a_next = j + 1 < kXrunPer ? (a4 >> (8 * (j + 1))) & 0xffu : a_after;
+    if (i0 + j < n) packed |= voxel_flags_from_bits(i0 + j, n, a, a_next) << (8 * j);
+  }
+  return packed;
+}
+
+__device__ __forceinline__ uint32_t slot_count4(uint32_t f4, int64_t n, int64_t i0) {
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int j = 0; j < kXrunPer; ++j)
+    if (i0 + j < n) cnt += slot_count_of((f4 >> (8 * j)) & 0xffu);
+  return cnt;
+}
+
+// Each thread takes kXrunPer consecutive voxels: block sums of the slot
+// counts; without the dense query's bits also the flags (one 32-bit store).
+// `ready` is the word the dense query sets when it wrote the bits.
 __global__ void __launch_bounds__(kXrunBlock) xrun_count_kernel(const int32_t* __restrict__ coords,
                                                                 const int32_t* __restrict__ nmap, int64_t n,
                                                                 uint8_t* __restrict__ flags,
                                                                 int64_t* __restrict__ block_sums,
                                                                 const int* __restrict__ ready,
                                                                 const uint8_t* __restrict__ raw) {
-  __shared__ int64_t warp_sums[kXrunBlock / 32];
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * kXrunBlock + threadIdx.x;
+  __shared__ uint32_t warp_sums[kXrunBlock / 32];
+  const int64_t i0 = (static_cast<int64_t>(blockIdx.x) * kXrunBlock + threadIdx.x) * kXrunPer;
   const bool pre = ready != nullptr && *ready != 0;
-  uint32_t f = 0;
-  if (i < n && pre) {
-    const uint32_t a = raw[i];
-    if (a & 1u) {
-      if (i + 1 >= n) {
-        f = (a & 2u) ? 1u : 0u;
-      } else {
-        const int32_t* c = coords + 3 * i;
-        const bool shared_cells = __ldg(c + 3) == __ldg(c) && __ldg(c + 4) == __ldg(c + 1) &&
-                                  __ldg(c + 5) == __ldg(c + 2) + 2;
-        const bool same = shared_cells || ((a & 2u) == 0u && (raw[i + 1] & 4u) == 0u);
-        f = same ? 1u : 2u;
-      }
+  uint32_t cnt = 0;
+  if (i0 < n) {
+    uint32_t packed = 0;
+    if (pre) {
+      packed = flags4(flags, raw, true, n, i0);
+    } else {
+#pragma unroll 1
+      for (int j = 0; j < kXrunPer; ++j)
+        if (i0 + j < n) packed |= voxel_flags_from_map(coords, nmap, n, i0 + j) << (8 * j);
+      *reinterpret_cast<uint32_t*>(flags + i0) = packed;
     }
-    if (i == 0 && (a & 4u)) f |= 4u;
-    flags[i] = static_cast<uint8_t>(f);
-  } else if (i < n) {
-    const bool run_end = i + 1 >= n || !same_run(coords, i);
-    if (run_end) {
-      if (i + 1 >= n) {
-        bool any = false;
-        for (int g = 0; g < 9; ++g) any |= map_row(nmap, n, 3 * g + 2, i) != n;
-        f = any ? 1u : 0u;
-      } else {
-        bool same = true;
-        for (int g = 0; g < 9; ++g) same &= map_row(nmap, n, 3 * g + 2, i) == map_row(nmap, n, 3 * g, i + 1);
-        f = same ? 1u : 2u;
-      }
-    }
-    if (i == 0) {
-      bool any = false;
-      for (int g = 0; g < 9; ++g) any |= map_row(nmap, n, 3 * g, 0) != n;
-      if (any) f |= 4u;
-    }
-    flags[i] = static_cast<uint8_t>(f);
+    cnt = slot_count4(packed, n, i0);
   }
-  int64_t cnt = i < n ? 1 + (f & 3u) + ((f >> 2) & 1u) : 0;
   for (int o = 16; o > 0; o >>= 1) cnt += __shfl_down_sync(0xffffffffu, cnt, o);
   if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = cnt;
   __syncthreads();
   if (threadIdx.x < 32) {
-    int64_t s = warp_sums[threadIdx.x];
+    uint32_t s = warp_sums[threadIdx.x];
     for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
     if (threadIdx.x == 0) block_sums[blockIdx.x] = s;
   }
 }
 
 // Exclusive scan of one value per thread of the block; returns the block total.
-__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* warp_sums, int64_t* out) {
+template <typename T>
+__device__ __forceinline__ T block_exclusive_scan(T v, T* warp_sums, T* out) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int64_t x = v;
+  T x = v;
   for (int o = 1; o < 32; o <<= 1) {
-    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    const T y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int64_t w = warp_sums[lane];
+    T w = warp_sums[lane];
     for (int o = 1; o < 32; o <<= 1) {
-      const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+      const T y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
     warp_sums[lane] = w;  // inclusive over warps
   }
   __syncthreads();
-  const int64_t before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
-  const int64_t total = warp_sums[31];
+  const T before = (warp > 0 ? warp_sums[warp - 1] : T(0)) + x - v;
+  const T total = warp_sums[31];
   __syncthreads();  // warp_sums is reused by the next call
   *out = before;
   return total;
@@ -147,42 +190,52 @@ __global__ void __launch_bounds__(kXrunBlock) xrun_scan_kernel(int64_t* __restri
     const int64_t j = base + threadIdx.x;
     const int64_t v = j < nb ? block_sums[j] : 0;
     int64_t ex;
-    const int64_t total = block_exclusive_scan(v, warp_sums, &ex);
+    const int64_t total = block_exclusive_scan<int64_t>(v, warp_sums, &ex);
     if (j < nb) block_sums[j] = carry + ex;
     carry += total;
   }
   if (threadIdx.x == 0) *slot_count = carry;
 }
 
-// Each voxel writes its slot and the separators around it.
+// Each voxel writes its slot and the separators around it (kXrunPer
+// consecutive voxels per thread, as in the count).  A block's slots number
+// at most 4 * kXrunBlock * kXrunPer, so the in-block scan is 32-bit.
 __global__ void __launch_bounds__(kXrunBlock) xrun_fill_kernel(const uint8_t* __restrict__ flags, int64_t n,
                                                                const int64_t* __restrict__ block_offsets,
                                                                int32_t* __restrict__ slots, int64_t cap,
-                                                               int32_t* __restrict__ overflow) {
-  __shared__ int64_t warp_sums[32];
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * kXrunBlock + threadIdx.x;
-  const uint32_t f = i < n ? flags[i] : 0u;
-  const int64_t cnt = i < n ? 1 + (f & 3u) + ((f >> 2) & 1u) : 0;
-  int64_t ex;
-  block_exclusive_scan(cnt, warp_sums, &ex);
-  if (i >= n) return;
+                                                               int32_t* __restrict__ overflow,
+                                                               const int* __restrict__ ready,
+                                                               const uint8_t* __restrict__ raw) {
+  __shared__ uint32_t warp_sums[32];
+  const int64_t i0 = (static_cast<int64_t>(blockIdx.x) * kXrunBlock + threadIdx.x) * kXrunPer;
+  const bool pre = ready != nullptr && *ready != 0;
+  const uint32_t f4 = i0 < n ? flags4(flags, raw, pre, n, i0) : 0u;
+  const uint32_t cnt = i0 < n ? slot_count4(f4, n, i0) : 0u;
+  uint32_t ex;
+  block_exclusive_scan<uint32_t>(cnt, warp_sums, &ex);
+  if (i0 >= n) return;
   int64_t s = block_offsets[blockIdx.x] + ex;
   if (s + cnt > cap) {
     atomicExch(overflow, 1);
     return;
   }
-  const int32_t v = static_cast<int32_t>(i);
-  if (f & 4u) slots[s++] = -3 - 2 * v;  // left of voxel 0
-  slots[s++] = v;
-  const uint32_t after = f & 3u;
-  if (after >= 1u) slots[s++] = -2 - 2 * v;        // right of this run end (shared when one)
-  if (after == 2u) slots[s] = -3 - 2 * (v + 1);    // left of the next run's start
+#pragma unroll
+  for (int j = 0; j < kXrunPer; ++j) {
+    if (i0 + j >= n) break;
+    const uint32_t f = (f4 >> (8 * j)) & 0xffu;
+    const int32_t v = static_cast<int32_t>(i0 + j);
+    if (f & 4u) slots[s++] = -3 - 2 * v;  // left of voxel 0
+    slots[s++] = v;
+    const uint32_t after = f & 3u;
+    if (after >= 1u) slots[s++] = -2 - 2 * v;        // right of this run end (shared when one)
+    if (after == 2u) slots[s++] = -3 - 2 * (v + 1);  // left of the next run's start
+  }
 }
 
 }  // namespace
 
 size_t xrun_workspace_bytes(int64_t n) {
-  const int64_t nb = (n + kXrunBlock - 1) / kXrunBlock;
+  const int64_t nb = (n + kXrunSpan - 1) / kXrunSpan;
   return 2 * static_cast<size_t>(((n + 255) / 256) * 256) + static_cast<size_t>(nb) * 8u + 256u;
 }
 
@@ -198,7 +251,7 @@ uint8_t* xrun_raw_bits(void* workspace, int64_t n) { return static_cast<uint8_t*
 spconv_status launch_xrun_layout(const int32_t* coords, const int32_t* nmap, int64_t n, int32_t* slots,
                                  int64_t cap, int64_t* slot_count, void* workspace, cudaStream_t stream,
                                  const int* flags_ready) {
-  const int64_t nb = (n + kXrunBlock - 1) / kXrunBlock;
+  const int64_t nb = (n + kXrunSpan - 1) / kXrunSpan;
   uint8_t* flags = static_cast<uint8_t*>(workspace);
   uint8_t* raw = xrun_raw_bits(workspace, n);
   int64_t* block_sums = reinterpret_cast<int64_t*>(static_cast<uint8_t*>(workspace) + 2 * ((n + 255) / 256) * 256);
@@ -211,7 +264,7 @@ spconv_status launch_xrun_layout(const int32_t* coords, const int32_t* nmap, int
   xrun_scan_kernel<<<1, kXrunBlock, 0, stream>>>(block_sums, nb, slot_count);
   if (!cuda_ok(cudaGetLastError(), "xrun_scan_kernel", &st)) return st;
   xrun_fill_kernel<<<static_cast<unsigned>(nb), kXrunBlock, 0, stream>>>(flags, n, block_sums, slots, cap,
-                                                                           overflow);
+                                                                           overflow, flags_ready, raw);
   if (!cuda_ok(cudaGetLastError(), "xrun_fill_kernel", &st)) return st;
   return SPCONV_OK;
 }

@@ -157,6 +157,12 @@ def test_xrun_entry_points_validate_without_gpu(lib):
                       None))[0] == -1
     assert _status(xc(fake, fake, fake, 31, fake, fake, None, fake, 0, 27, 128, 128, 2, None))[0] == -1
     assert _status(xc(fake, fake, fake, 0, fake, fake, None, fake, n, 27, 128, 128, 2, None))[0] == -1
+    xe = lib.spconv_submconv3d_xrun_ex
+    assert _status(xe(fake, fake, fake, 31, fake, fake, None, fake, fake, n, 27, 128, 128, 2, 3, None))[0] == -1
+    assert _status(xe(fake, fake, fake, 31, fake, fake, None, ctypes.c_void_p(0x100008), fake, n, 27, 128, 128,
+                      2, 1, None))[0] == -1
+    assert _status(xe(fake, fake, fake, 31, fake, fake, None, fake, fake, n, 27, 64, 128, 2, 2, None))[0] == -2
+    assert _status(xe(fake, None, fake, 31, fake, fake, None, fake, fake, n, 27, 128, 128, 2, 0, None))[0] == -1
     xd = lib.spconv_submconv3d_dgrad_xrun
     assert _status(xd(fake, fake, fake, 31, fake, fake, fake, n, 27, 128, 64, 2, None))[0] == -2
     assert _status(xd(fake, fake, fake, 31, fake, fake, fake, n, 27, 256, 128, 2, None))[0] == -2

@@ -149,6 +149,55 @@ def test_xrun_conv_workload_sample(sv, oracle_mod, workload):
     assert_within(got, ref, sabs, "bf16")
 
 
+@pytest.mark.parametrize("act", ["relu", "silu", None])
+@pytest.mark.parametrize("name,co", [("random", 128), ("line", 48), ("shuffled", 128), ("single", 16)])
+def test_xrun_fused_epilogue_matches_oracle(sv, oracle_mod, name, co, act):
+    """out = act(conv + bias + residual) over the layout: against the
+    oracle (tolerance scaled by the activation's slope bound, as for the
+    voxel-tile epilogue) and near the voxel-tile kernel's fused epilogue."""
+    coords = shapes()[name]
+    n = len(coords)
+    nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    feats = W.values(co + n, 31, (n, 128), "bf16")
+    w = W.values(co + n, 32, (27, 128, co), "bf16", 1.0 / np.sqrt(27 * 128))
+    b = W.values(co + n, 33, (co,), "bf16", 0.1)
+    res = W.values(co + n, 34, (n, co), "bf16")
+    ref, scale = oracle_mod.conv_fused(feats, nmap, w, b, "bf16", residual=res, act=act or "none",
+                                       threads=oracle_mod.host_threads())
+    _, nm, slots, count = gpu_layout(sv, coords, nmap)
+    f, ww, bb, r = (torch_storage(x, "bf16") for x in (feats, w, b, res))
+    out = sv.submconv3d_xrun(f, nm, slots, count, ww, bb, residual=r, activation=act)
+    tiles = sv.submconv3d(f, nm, ww, bb, residual=r, activation=act)
+    sv.device_status()
+    assert_within(to_f64(out), ref, scale, "bf16")
+    assert_near_plain(out, tiles, scale)
+
+
+@pytest.mark.parametrize("act", ["relu", None])
+def test_xrun_fused_epilogue_in_place_and_without_residual(sv, oracle_mod, act):
+    """out is the residual buffer itself; and an activation alone."""
+    coords = shapes()["dense"]
+    n = len(coords)
+    nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    feats = W.values(5, 41, (n, 128), "bf16")
+    w = W.values(5, 42, (27, 128, 128), "bf16", 1.0 / np.sqrt(27 * 128))
+    b = W.values(5, 43, (128,), "bf16", 0.1)
+    res = W.values(5, 44, (n, 128), "bf16")
+    _, nm, slots, count = gpu_layout(sv, coords, nmap)
+    f, ww, bb, r = (torch_storage(x, "bf16") for x in (feats, w, b, res))
+    got = sv.submconv3d_xrun(f, nm, slots, count, ww, bb, out=r, residual=r, activation=act)
+    assert got.data_ptr() == r.data_ptr()
+    ref, scale = oracle_mod.conv_fused(feats, nmap, w, b, "bf16", residual=res, act=act or "none",
+                                       threads=oracle_mod.host_threads())
+    assert_within(to_f64(got), ref, scale, "bf16")
+    if act is not None:
+        got2 = sv.submconv3d_xrun(f, nm, slots, count, ww, bb, activation=act)
+        ref2, scale2 = oracle_mod.conv_fused(feats, nmap, w, b, "bf16", residual=None, act=act,
+                                             threads=oracle_mod.host_threads())
+        assert_within(to_f64(got2), ref2, scale2, "bf16")
+    sv.device_status()
+
+
 @pytest.mark.parametrize("ci", [16, 64, 128])
 @pytest.mark.parametrize("name", ["random", "dense", "line", "isolated", "shuffled"])
 def test_xrun_dgrad_matches_oracle_and_plain(sv, oracle_mod, name, ci):
