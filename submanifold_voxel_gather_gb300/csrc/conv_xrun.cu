@@ -66,10 +66,18 @@ constexpr int kRingRow = kGRowsAlloc;         // int32 entries per ring row
 constexpr int kProducerWarp0 = 8;
 constexpr int kProducerThreads = 128;
 constexpr int kEpilogueWarp0 = 4;
-// Fused epilogue: a 32-slot chunk is staged in fp32 (16 KB); its 16-byte
-// output pieces (32 rows x Co / 8) are at most 4 per epilogue thread.
-constexpr int kFusedPieces = 32 * 16 / 128;
-constexpr uint32_t kStageBytes = 32u * 128u * 4u;
+// Epilogue staging, 16 KB.  The plain epilogue stages 32-slot chunks of
+// bf16 output rows (8 KB).  With a residual the chunks are 16 slots: their
+// acc + bias rows in fp32 (8 KB), and two 4 KB windows of 16 residual rows
+// each, loaded by TMA, chunk c into window c & 1 while chunk c - 1 is
+// stored from the other.
+constexpr uint32_t kStageBytes = 16384u;
+constexpr uint32_t kResChunk = 16;                             // slots per fused chunk
+constexpr uint32_t kWindowBytes = kResChunk * 128u * 2u;        // 4 KB
+constexpr uint32_t kWindowOff = kResChunk * 128u * 4u;          // after the fp32 rows
+static_assert(kWindowOff + 2u * kWindowBytes <= kStageBytes, "the fused staging must fit the 16 KB");
+constexpr uint32_t kRowOffNone = 0xffu;  // slot without a voxel
+constexpr uint32_t kRowOffFar = 0xfeu;   // voxel outside its chunk's window (only with an invalid layout)
 constexpr uint64_t kAStepUnits = (16 * 128) >> 4;   // one K step of channel-major weights
 constexpr uint64_t kBStepUnits = (16 * 2) >> 4;     // one K step of K-major rows
 // An operand shifted by dxi rows in its 1024-byte-aligned chunk is the
@@ -99,6 +107,7 @@ struct XrParams {
   uint32_t off_ring;
   uint32_t off_stage_out;
   uint32_t off_codes;  // the epilogue's copy of the current tile's 256 slot codes
+  uint32_t off_rowoff; // per slot of the tile: its voxel's row in its chunk's window; per chunk its first voxel
   uint32_t off_bias;
   uint32_t off_meta;
   uint32_t off_bars;
@@ -164,7 +173,8 @@ __device__ __forceinline__ bool issue_group(uint32_t flag, int g, bool issued) {
 // MMAs are done with it.  Each SM then streams half the weight bytes.
 template <bool kDgrad, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
-    submconv_xrun_kernel(const __grid_constant__ CUtensorMap tm_w, const XrParams p) {
+    submconv_xrun_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_res,
+                         const XrParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -173,9 +183,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   int32_t* ring = reinterpret_cast<int32_t*>(smem + p.off_ring);
   __nv_bfloat16* stage_out = reinterpret_cast<__nv_bfloat16*>(smem + p.off_stage_out);
-  float* stage_f32 = reinterpret_cast<float*>(smem + p.off_stage_out);  // the same memory, fused epilogue
-  const bool fused = p.residual != nullptr || p.act != SPCONV_ACT_NONE;
+  // Fused residual: the voxel rows of a 32-slot chunk are consecutive (the
+  // layout lists voxels in index order), so the chunk's residual rows come
+  // as one 32-row window by TMA, which keeps the epilogue's loads off the
+  // load/store pipe that the gathers use (residual rows loaded by the
+  // threads slowed the whole kernel by 40%).
+  const bool fused = p.residual != nullptr;
   int32_t* codes_s = reinterpret_cast<int32_t*>(smem + p.off_codes);
+  uint8_t* rowoff_s = smem + p.off_rowoff;                                          // [256]
+  int32_t* chunk_first = reinterpret_cast<int32_t*>(smem + p.off_rowoff + kTileN);  // [16]
   float* bias_s = reinterpret_cast<float*>(smem + p.off_bias);
   uint32_t* wmeta = reinterpret_cast<uint32_t*>(smem + p.off_meta);
   uint32_t* ring_flag = wmeta + kWSlots;
@@ -189,7 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tmem_full = ring_empty + kXRing;
   uint64_t* tmem_empty = tmem_full + 2;
   uint64_t* drain = tmem_empty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* res_full = drain + 1;  // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(res_full + 2);
   uint32_t* consumed_holder = tmem_holder + 1;
   uint32_t* fills_holder = tmem_holder + 2;
 
@@ -211,10 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&tmem_empty[i]), 4);
     }
     mbar_init(smem_addr(drain), 1);
+    mbar_init(smem_addr(&res_full[0]), 1);
+    mbar_init(smem_addr(&res_full[1]), 1);
     *consumed_holder = 0;
     *fills_holder = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_w);
+    if (p.residual != nullptr) tma_prefetch_desc(&tm_res);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_holder), 512);
@@ -537,108 +557,167 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = static_cast<int>(threadIdx.x) - kEpilogueWarp0 * 32;  // 0..127
     const int chunks_per_row = p.co_count / 8;
     const int co_l = static_cast<int>(sub) * 32 + static_cast<int>(lane);
-    // Fused epilogue: the residual pieces (16 bytes each) this thread stores
-    // for chunk vc of the tile; each thread reads, then writes, the same
-    // (row, piece) pairs, so the residual may be `out` itself.
-    auto load_residual = [&](uint4 (&res)[kFusedPieces], int vc) {
-#pragma unroll
-      for (int j = 0; j < kFusedPieces; ++j) {
-        const int q = et + 128 * j;
-        const int r = q / chunks_per_row;
-        const int c8 = q - r * chunks_per_row;
-        const int32_t code = q < 32 * chunks_per_row ? codes_s[vc * 32 + r] : -1;
-        res[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (p.residual != nullptr && code >= 0 && code < n_rows)
-          res[j] = *reinterpret_cast<const uint4*>(p.residual + static_cast<int64_t>(code) * p.co + c8 * 8);
+    // The residual window of fused chunk c (16 slots), into window c & 1:
+    // 16 rows from the chunk's first voxel (rows past N read as zero); a
+    // chunk without voxels only completes the barrier's phase.
+    const uint32_t res_bytes = kResChunk * static_cast<uint32_t>(p.co) * 2u;
+    const uint32_t stage_base = smem_addr(smem + p.off_stage_out);
+    float* stage_f32 = reinterpret_cast<float*>(smem + p.off_stage_out);
+    auto window = [&](int c) {
+      return reinterpret_cast<const __nv_bfloat16*>(smem + p.off_stage_out + kWindowOff +
+                                                     static_cast<uint32_t>(c & 1) * kWindowBytes);
+    };
+    auto issue_residual = [&](int c) {
+      const int32_t first = chunk_first[c];
+      const uint32_t bar = smem_addr(&res_full[c & 1]);
+      fence_proxy_async_smem();  // the window's previous contents were read through the generic proxy
+      if (first < 0) {
+        mbar_arrive(bar);
+      } else {
+        mbar_arrive_expect_tx(bar, res_bytes);
+        tma_load_2d(stage_base + kWindowOff + static_cast<uint32_t>(c & 1) * kWindowBytes, &tm_res, 0, first, bar);
       }
     };
+    // The voxel a slot names or sits next to, for the L2 prefetch of the
+    // next tile's residual rows.
+    auto slot_voxel_near = [&](int64_t s) -> int64_t {
+      const int32_t c = slot_code(p.slots, s, S);
+      if (c >= 0) return c;
+      if (c <= -2) return static_cast<int64_t>((-2 - c) >> 1);
+      return -1;
+    };
+    uint32_t res_phase = 0;  // bit b: the phase window b's barrier waits for next
+    bool ok_res = true;
+    uint32_t res_pending = 0;  // window loads issued and not yet waited for (bits)
     uint32_t tile_i = 0;
     for (int64_t t = blockIdx.x; t < t_end; t += gridDim.x, ++tile_i) {
       const uint32_t buf = tile_i & 1u;
       const int64_t s0 = t * kTileN;
       // The tile's slot codes (the output row of each slot), read once and
       // coalesced while the accumulator is still being computed: a row's
-      // store then never waits on a load of its code.
+      // store then never waits on a load of its code.  Warp `sub` holds
+      // slots 32 sub + lane and 128 + 32 sub + lane: 16-slot chunks 2 sub,
+      // 2 sub + 1, 8 + 2 sub and 9 + 2 sub, one per half-warp.
       epi_bar();  // the previous tile's codes are no longer read
-      codes_s[et] = slot_code(p.slots, s0 + et, S);
-      codes_s[et + 128] = slot_code(p.slots, s0 + et + 128, S);
-      // The residual of chunk 0 is loaded before the wait and each later
-      // chunk's while the one before it is stored, so no chunk waits on
-      // its residual's load.
-      uint4 res_cur[kFusedPieces], res_nxt[kFusedPieces];
+      const int32_t code0 = slot_code(p.slots, s0 + et, S);
+      const int32_t code1 = slot_code(p.slots, s0 + et + 128, S);
+      codes_s[et] = code0;
+      codes_s[et + 128] = code1;
       if (fused) {
-        epi_bar();  // the codes are in
-        load_residual(res_cur, 0);
+        const uint32_t half = lane < 16 ? 0x0000ffffu : 0xffff0000u;
+        const bool v0 = code0 >= 0 && code0 < n_rows, v1 = code1 >= 0 && code1 < n_rows;
+        const uint32_t f0 = __reduce_min_sync(half, v0 ? static_cast<uint32_t>(code0) : 0xffffffffu);
+        const uint32_t f1 = __reduce_min_sync(half, v1 ? static_cast<uint32_t>(code1) : 0xffffffffu);
+        const uint32_t d0 = static_cast<uint32_t>(code0) - f0, d1 = static_cast<uint32_t>(code1) - f1;
+        rowoff_s[et] = static_cast<uint8_t>(!v0 ? kRowOffNone : (d0 < kResChunk ? d0 : kRowOffFar));
+        rowoff_s[et + 128] = static_cast<uint8_t>(!v1 ? kRowOffNone : (d1 < kResChunk ? d1 : kRowOffFar));
+        if ((lane & 15) == 0) {
+          chunk_first[et / kResChunk] = f0 == 0xffffffffu ? -1 : static_cast<int32_t>(f0);
+          chunk_first[(et + 128) / kResChunk] = f1 == 0xffffffffu ? -1 : static_cast<int32_t>(f1);
+        }
+      }
+      epi_bar();  // the codes (and the chunks' windows) are in
+      if (fused) {
+        // Both windows are free here (the previous tile's stores are done):
+        // chunks 0 and 1 now, and the next tile's residual rows into L2.
+        if (et == 0) {
+          issue_residual(0);
+          issue_residual(1);
+          const int64_t vn = slot_voxel_near(s0 + static_cast<int64_t>(gridDim.x) * kTileN);
+          if (vn >= 0 && vn < n_rows) {
+            const int64_t rows = n_rows - vn < kTileN ? n_rows - vn : static_cast<int64_t>(kTileN);
+            bulk_prefetch_l2(p.residual + vn * p.co, static_cast<uint32_t>(rows * p.co * 2));
+          }
+        }
+        res_pending = 3u;
       }
       const bool got = __all_sync(0xffffffffu, mbar_wait(smem_addr(&tmem_full[buf]), (tile_i >> 1) & 1u));
       if (!epi_all(got)) break;
       tc_fence_after();
       const uint32_t tcol = tmem_base + ((sub * 32u) << 16) + buf * static_cast<uint32_t>(kTileN);
-      for (int vc = 0; vc < kTileN / 32; ++vc) {
-        epi_bar();  // the previous chunk's staged rows have been stored (and the codes are in)
-        if (fused) {
-          if (vc + 1 < kTileN / 32) load_residual(res_nxt, vc + 1);
-          const uint4 (&res)[kFusedPieces] = res_cur;
+      if (fused) {
+        const int cpr = chunks_per_row;  // 16-byte pieces per row
+        for (int c = 0; c < static_cast<int>(kTileN / kResChunk); ++c) {
+          epi_bar();  // the previous chunk's rows have been stored
+          if (c >= 1 && c + 1 < static_cast<int>(kTileN / kResChunk)) {
+            // window (c + 1) & 1 held chunk c - 1, whose stores are done
+            if (et == 0) issue_residual(c + 1);
+            res_pending |= 1u << ((c + 1) & 1);
+          }
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tcol + c * kResChunk, v);
+          tmem_ld_wait();
+          if (co_l < p.co_count) {
+            const float b = bias_s[co_l];
+#pragma unroll
+            for (int i = 0; i < static_cast<int>(kResChunk); ++i) stage_f32[i * 128 + co_l] = __uint_as_float(v[i]) + b;
+          }
+          const uint32_t wb = static_cast<uint32_t>(c & 1);
+          ok_res = __all_sync(0xffffffffu, mbar_wait(smem_addr(&res_full[wb]), (res_phase >> wb) & 1u)) && ok_res;
+          res_phase ^= 1u << wb;
+          res_pending &= ~(1u << wb);
+          epi_bar();  // staged, and every thread saw the window land
+          const __nv_bfloat16* win = window(c);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int q = et + 128 * j;
+            if (q >= static_cast<int>(kResChunk) * cpr) break;
+            const int r = q / cpr;
+            const int c8 = q - r * cpr;
+            const int32_t code = codes_s[c * kResChunk + r];
+            if (code < 0 || code >= n_rows) continue;
+            const uint32_t o = rowoff_s[c * kResChunk + r];
+            const uint4 rr = o < kResChunk
+                                 ? *reinterpret_cast<const uint4*>(win + o * static_cast<uint32_t>(p.co) + c8 * 8)
+                                 : *reinterpret_cast<const uint4*>(p.residual + static_cast<int64_t>(code) * p.co + c8 * 8);
+            const float4 a0 = *reinterpret_cast<const float4*>(stage_f32 + r * 128 + c8 * 8);
+            const float4 a1 = *reinterpret_cast<const float4*>(stage_f32 + r * 128 + c8 * 8 + 4);
+            const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
+            uint32_t ow[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float lo = apply_activation_bf16(x[2 * h] + __uint_as_float(rw[h] << 16), p.act);
+              const float hi = apply_activation_bf16(x[2 * h + 1] + __uint_as_float(rw[h] & 0xffff0000u), p.act);
+              const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+              ow[h] = *reinterpret_cast<const uint32_t*>(&pr);
+            }
+            *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(code) * p.co + c8 * 8) =
+                make_uint4(ow[0], ow[1], ow[2], ow[3]);
+          }
+        }
+      } else {
+        for (int vc = 0; vc < kTileN / 32; ++vc) {
+          epi_bar();  // the previous chunk's staged rows have been stored
           uint32_t v[32];
           tmem_ld_32x32b_x32(tcol + vc * 32, v);
           tmem_ld_wait();
           if (co_l < p.co_count) {
             const float b = bias_s[co_l];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) stage_f32[i * 128 + co_l] = __uint_as_float(v[i]) + b;
+            for (int i = 0; i < 32; ++i)
+              stage_out[i * 128 + co_l] = __float2bfloat16_rn(apply_activation_bf16(__uint_as_float(v[i]) + b, p.act));
           }
-          epi_bar();
-#pragma unroll
-          for (int j = 0; j < kFusedPieces; ++j) {
-            const int q = et + 128 * j;
-            if (q >= 32 * chunks_per_row) break;
+          epi_bar();  // staged
+          for (int q = et; q < 32 * chunks_per_row; q += 128) {
             const int r = q / chunks_per_row;
             const int c8 = q - r * chunks_per_row;
             const int32_t code = codes_s[vc * 32 + r];
-            if (code < 0 || code >= n_rows) continue;
-            const float4 a0 = *reinterpret_cast<const float4*>(stage_f32 + r * 128 + c8 * 8);
-            const float4 a1 = *reinterpret_cast<const float4*>(stage_f32 + r * 128 + c8 * 8 + 4);
-            const __nv_bfloat162* rh = reinterpret_cast<const __nv_bfloat162*>(&res[j]);
-            const float2 r0 = __bfloat1622float2(rh[0]), r1 = __bfloat1622float2(rh[1]);
-            const float2 r2 = __bfloat1622float2(rh[2]), r3 = __bfloat1622float2(rh[3]);
-            uint4 o;
-            __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
-            oh[0] = __floats2bfloat162_rn(apply_activation_bf16(a0.x + r0.x, p.act),
-                                          apply_activation_bf16(a0.y + r0.y, p.act));
-            oh[1] = __floats2bfloat162_rn(apply_activation_bf16(a0.z + r1.x, p.act),
-                                          apply_activation_bf16(a0.w + r1.y, p.act));
-            oh[2] = __floats2bfloat162_rn(apply_activation_bf16(a1.x + r2.x, p.act),
-                                          apply_activation_bf16(a1.y + r2.y, p.act));
-            oh[3] = __floats2bfloat162_rn(apply_activation_bf16(a1.z + r3.x, p.act),
-                                          apply_activation_bf16(a1.w + r3.y, p.act));
-            *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(code) * p.co + c8 * 8) = o;
+            if (code >= 0 && code < n_rows)
+              *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(code) * p.co + c8 * 8) =
+                  *reinterpret_cast<const uint4*>(stage_out + r * 128 + c8 * 8);
           }
-#pragma unroll
-          for (int j = 0; j < kFusedPieces; ++j) res_cur[j] = res_nxt[j];
-          continue;
-        }
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tcol + vc * 32, v);
-        tmem_ld_wait();
-        if (co_l < p.co_count) {
-          const float b = bias_s[co_l];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) stage_out[i * 128 + co_l] = __float2bfloat16_rn(__uint_as_float(v[i]) + b);
-        }
-        epi_bar();
-        for (int q = et; q < 32 * chunks_per_row; q += 128) {
-          const int r = q / chunks_per_row;
-          const int c8 = q - r * chunks_per_row;
-          const int32_t code = codes_s[vc * 32 + r];
-          if (code >= 0 && code < n_rows)
-            *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(code) * p.co + c8 * 8) =
-                *reinterpret_cast<const uint4*>(stage_out + r * 128 + c8 * 8);
         }
       }
+      if (!epi_all(ok_res)) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&tmem_empty[buf]));
     }
+    // Only after a timed-out wait can a window load still be in flight:
+    // wait for it (bounded) before the CTA's memory goes away.
+    for (int b2 = 0; b2 < 2; ++b2)
+      if (res_pending & (1u << b2)) mbar_wait(smem_addr(&res_full[b2]), (res_phase >> b2) & 1u);
   }
 
   // ---------------------------------------------------------- teardown
@@ -721,6 +800,21 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SPCONV_ERR_CUDA, "cuTensorMapEncodeTiled(w) failed: " + std::to_string(r));
+  // The residual (N, co) as 2-D rows; box = kResChunk rows of co channels,
+  // no swizzle (rows past N read as zero).  Unused without a residual.
+  CUtensorMap tm_res = tm_w;
+  if (residual != nullptr) {
+    cuuint64_t rdims[2] = {static_cast<cuuint64_t>(co), static_cast<cuuint64_t>(n)};
+    cuuint64_t rstrides[1] = {static_cast<cuuint64_t>(co) * 2u};
+    // one fused chunk's window: kResChunk rows (kWindowBytes at co = 128)
+    cuuint32_t rbox[2] = {static_cast<cuuint32_t>(co), kResChunk};
+    cuuint32_t restr[2] = {1u, 1u};
+    r = encode(&tm_res, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(residual), rdims, rstrides, rbox,
+               restr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(SPCONV_ERR_CUDA, "cuTensorMapEncodeTiled(residual) failed: " + std::to_string(r));
+  }
 
   XrParams p{};
   p.feats = static_cast<const __nv_bfloat16*>(feats);
@@ -748,16 +842,18 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
   p.off_ring = off;
   off += kXRing * kRingRow * 4u;
   p.off_stage_out = off;
-  off += kStageBytes;  // bf16 rows, or fp32 ones for the fused epilogue
+  off += kStageBytes;  // 128-byte aligned, as are the windows in it (TMA destinations)
   p.off_codes = off;
   off += kTileN * 4u;
+  p.off_rowoff = off;
+  off += kTileN + (kTileN / kResChunk) * 4u;
   p.off_bias = off;
   off += 128u * 4u;
   p.off_meta = off;
   off += (kWSlots + kXRing) * 4u;
   off = (off + 7u) & ~7u;
   p.off_bars = off;
-  off += (2u * kGBufs + 2u * kWSlots + 2u * kXRing + 5u) * 8u + 16u;
+  off += (2u * kGBufs + 2u * kWSlots + 2u * kXRing + 7u) * 8u + 16u;
   const uint32_t smem_bytes = off + 1024u;  // slack for the 1024-byte alignment
   if (smem_bytes > 232448u) return fail(SPCONV_ERR_UNSUPPORTED, "x-run conv: shared memory layout too large");
 
@@ -793,7 +889,7 @@ spconv_status launch_conv_xrun(const void* feats, const int32_t* nmap, const int
   }
   if (clusters < 1) return fail(SPCONV_ERR_UNSUPPORTED, "x-run conv: no CTA pair fits on this device");
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (clusters < sms / 2 ? clusters : sms / 2)), 1, 1);
-  if (!cuda_ok(cudaLaunchKernelEx(&cfg, kern, tm_w, p), "submconv_xrun_kernel", &st)) return st;
+  if (!cuda_ok(cudaLaunchKernelEx(&cfg, kern, tm_w, tm_res, p), "submconv_xrun_kernel", &st)) return st;
   return SPCONV_OK;
 }
 

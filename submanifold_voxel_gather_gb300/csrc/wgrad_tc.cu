@@ -18,8 +18,9 @@
 // overlaps the next item's MMAs) and then adds its 128 x 256 partial tile to
 // dw with fp32 reductions.  dw is zeroed before the launch.
 //
-// Warp roles mirror the forward kernel: warp 2 loads the map entries of each
-// (item, chunk) into a ring and flags atoms with any valid entry; warps 8-11
+// Warp roles mirror the forward kernel: warps 2 and 3 load the map entries
+// of each (item, chunk) into a ring (alternate chunks) and flag atoms with
+// any valid entry; warps 8-11
 // gather the atoms' feature rows (zero rows for missing neighbours, and no
 // stage at all for a chunk in which no atom has one); warp 0 loads the dout
 // tile and writes the stage metadata; warp 1 issues the MMAs; warps 4-7 read
@@ -39,7 +40,8 @@ constexpr int kThreads = 384;
 constexpr int kProducerWarp0 = 8;
 constexpr int kProducerThreads = 128;
 constexpr int kEpilogueWarp0 = 4;
-constexpr int kRing = 16;
+constexpr int kRing = 16;  // even: the two map loaders keep to alternate rows
+static_assert(kRing % 2 == 0, "two loaders take alternate ring rows");
 constexpr int kChunkVox = 64;              // voxels per stage (K of four MMAs)
 constexpr int kAtoms = 4;                  // 64-channel atoms per item (N <= 256)
 constexpr uint32_t kABytes = 128 * 128;    // dout tile: 128 channels x 64 voxels
@@ -50,16 +52,6 @@ constexpr int kMaxSmem = 232448;
 constexpr uint64_t kKStepUnits = (16 * 128) >> 4;  // 16 voxel rows of 128 B, 16-byte units
 
 enum : uint32_t { kMetaFirst = 1u, kMetaEnd = 2u };
-
-// Tiled 2-D TMA load into shared memory, completion credited to `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
 
 struct WgParams {
   const __nv_bfloat16* feats;
@@ -168,50 +160,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_holder;
   const int64_t n_rows = p.n;
 
-  if (warp == 2) {
-    // ------------------------------------------------------ map loader
+  if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------ map loaders
     // One ring row per (item, chunk): the 64 entries of each atom's offset,
     // normalised to a valid index or -1, and a mask of atoms with any valid
-    // entry.  Two voxels per lane; batches of four chunks, the next batch's
-    // loads in flight while this one is published (the map is read from DRAM
-    // once: latency, not bandwidth, sets this warp's pace).
+    // entry.  The CTA's (item, chunk) sequence is split between two warps:
+    // warp 2 fills the rows of even positions, warp 3 of odd ones (the ring
+    // length is even, so each keeps to its own rows).  Two voxels per lane;
+    // batches of four of the warp's chunks, the next batch's loads in flight
+    // while this one is published.  The map is read from device memory
+    // once, so a loader's pace is set by the load latency: two loaders
+    // keep twice the chunks in flight.
     constexpr int kBatch = 4;
-    auto load_batch = [&](int32_t (&vv)[kBatch][kAtoms][2], int64_t it, int32_t g, int64_t chunk0,
-                          int64_t left) {
+    const int64_t parity = warp - 2;
+    struct Pos {
+      int64_t item, c, c0, cnt;
+      int32_t group;
+    };
+    auto advance = [&](Pos& q, int64_t steps) {
+      q.c += steps;
+      while (q.item < p.num_items && q.c >= q.cnt) {
+        q.c -= q.cnt;
+        q.item += gridDim.x;
+        if (q.item < p.num_items) item_coords(p, q.item, &q.group, &q.c0, &q.cnt);
+      }
+    };
+    auto load_batch = [&](int32_t (&vv)[kBatch][kAtoms][2], Pos q) {
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b)
+      for (int b = 0; b < kBatch; ++b) {
 #pragma unroll
         for (int j = 0; j < kAtoms; ++j) {
-          const int32_t atom = g * kAtoms + j;
+          const int32_t atom = q.group * kAtoms + j;
           const int32_t kk = atom / p.atoms_per_k;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int64_t vox = (chunk0 + b) * kChunkVox + lane + 32 * h;
+            const int64_t vox = (q.c0 + q.c) * kChunkVox + lane + 32 * h;
             vv[b][j][h] = -1;
-            if (it < p.num_items && b < left && atom < p.num_atoms && vox < n_rows)
+            if (q.item < p.num_items && atom < p.num_atoms && vox < n_rows)
               vv[b][j][h] = __ldg(p.nmap + static_cast<int64_t>(kk) * n_rows + vox);
           }
         }
-    };
-    uint32_t e = 0, ephase = 0;
-    bool ok = true;
-    int64_t item = blockIdx.x, c = 0, c0 = 0, c_count = 0;
-    int32_t group = 0;
-    if (item < p.num_items) item_coords(p, item, &group, &c0, &c_count);
-    int32_t cur[kBatch][kAtoms][2], nxt[kBatch][kAtoms][2];
-    load_batch(cur, item, group, c0 + c, c_count - c);
-    while (item < p.num_items && ok) {
-      int64_t item2 = item, c2 = c + kBatch, c02 = c0, cnt2 = c_count;
-      int32_t g2 = group;
-      if (c2 >= c_count) {
-        item2 = item + gridDim.x;
-        c2 = 0;
-        if (item2 < p.num_items) item_coords(p, item2, &g2, &c02, &cnt2);
+        advance(q, 2);
       }
-      load_batch(nxt, item2, g2, c02 + c2, cnt2 - c2);
+    };
+    Pos pos{static_cast<int64_t>(blockIdx.x), 0, 0, 0, 0};
+    if (pos.item < p.num_items) item_coords(p, pos.item, &pos.group, &pos.c0, &pos.cnt);
+    advance(pos, parity);
+    int64_t t = parity;  // position in the CTA's sequence: ring row t % kRing
+    bool ok = true;
+    int32_t cur[kBatch][kAtoms][2], nxt[kBatch][kAtoms][2];
+    load_batch(cur, pos);
+    while (pos.item < p.num_items && ok) {
+      Pos npos = pos;
+      advance(npos, 2 * kBatch);
+      load_batch(nxt, npos);
+      Pos q = pos;
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
-        if (c + b >= c_count) break;
+        if (q.item >= p.num_items) break;
+        const uint32_t e = static_cast<uint32_t>(t % kRing);
+        const uint32_t ephase = static_cast<uint32_t>((t / kRing) & 1);
         if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ring_empty[e]), ephase ^ 1))) {
           ok = false;
           break;
@@ -230,10 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) ring_mask[e] = mask;
         mbar_arrive(smem_addr(&ring_full[e]));
-        if (++e == kRing) {
-          e = 0;
-          ephase ^= 1;
-        }
+        t += 2;
+        advance(q, 2);
       }
 #pragma unroll
       for (int b = 0; b < kBatch; ++b)
@@ -241,11 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < kAtoms; ++j)
 #pragma unroll
           for (int h = 0; h < 2; ++h) cur[b][j][h] = nxt[b][j][h];
-      item = item2;
-      c = c2;
-      group = g2;
-      c0 = c02;
-      c_count = cnt2;
+      pos = npos;
     }
   } else if (warp >= kProducerWarp0) {
     // ------------------------------------------------------ gather producers
