@@ -80,6 +80,12 @@ constexpr uint64_t kAStepUnits = (kKPerMma * 128) >> 4;
 constexpr uint64_t kBStepUnits = (kKPerMma * 2) >> 4;
 constexpr int kMaxStages = 8;
 constexpr int kMaxSmem = 232448;       // 227 KB opt-in limit per block
+// bf16 epilogue with a residual: 16-row chunks, one 128-channel block at a
+// time, staged in fp32 (8 KB) next to two 4 KB windows of residual rows.
+constexpr uint32_t kResRows = 16;
+constexpr uint32_t kResWindowOff = kResRows * 128u * 4u;
+constexpr uint32_t kResWindowBytes = kResRows * 128u * 2u;
+static_assert(kResWindowOff + 2u * kResWindowBytes <= 32u * 128u * 4u, "fits the 16 KB output staging");
 
 enum : uint32_t { kMetaFirst = 1u, kMetaEnd = 2u };
 
@@ -100,6 +106,7 @@ struct TcParams {
   int32_t act;       // spconv_activation
   int32_t dgrad;     // input gradient: selects the kDgrad instantiation
   int32_t tma_out;   // plain bf16 epilogue in voxel order: each 32-row block of out is written by one TMA store
+  int32_t tma_res;   // bf16 epilogue with a residual: 16-row windows of the residual come by TMA (tm_out holds its map)
   int32_t num_chunks;
   int32_t cps;       // 64-channel chunks per stage: 2 when Ci % 128 == 0 and Co <= 128, else 1
   uint32_t stages;
@@ -257,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = tmem_empty + 2;
   uint64_t* raw_full = drain + 1;    // tf32 forward: raw weight slots (two)
   uint64_t* raw_empty = raw_full + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(raw_empty + 2);
+  uint64_t* res_full = raw_empty + 2;  // bf16 residual epilogue: the two windows
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(res_full + 2);
   uint32_t* consumed_holder = tmem_holder + 1;
   uint32_t* fills_holder = tmem_holder + 2;
   uint32_t* raw_consumed_holder = tmem_holder + 3;
@@ -280,13 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&raw_full[i]), 1);
       mbar_init(smem_addr(&raw_empty[i]), 1);
+      mbar_init(smem_addr(&res_full[i]), 1);
     }
     *consumed_holder = 0;
     *fills_holder = 0;
     *raw_consumed_holder = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_w);
-    if (p.tma_out) tma_prefetch_desc(&tm_out);
+    if (p.tma_out || p.tma_res) tma_prefetch_desc(&tm_out);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_holder), p.tmem_cols);
@@ -712,33 +721,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = static_cast<int>(threadIdx.x) - kEpilogueWarp0 * 32;  // 0..127
     const int chunks_per_row = p.co_count / 8;                           // 16-byte chunks
     const bool fused = p.residual != nullptr || p.act != SPCONV_ACT_NONE;
-    // Fused epilogue (residual and/or activation): one 128-channel block at a
-    // time is staged in fp32 (32 rows x 128, 16 KB), and the store phase adds
-    // the residual, read as 16-byte pieces of its rows (coalesced, few load
-    // instructions: the load/store pipe is shared with the gather), applies
-    // the activation and rounds once.  Each thread reads and writes the same
-    // (row, piece) pairs, residual first, so the residual may be the output.
-    // The next chunk's pieces are loaded as soon as the current ones are used.
+    // bf16 with a residual (the tiles' rows are consecutive voxels, no
+    // order): 16-row chunks, one 128-channel block at a time.  The channel
+    // phase stages acc + bias in fp32; TMA brings the block's 16 residual
+    // rows into one of two windows (window u & 1 for step u = chunk * MBLK +
+    // block, step u + 1's loading while step u is stored); the store phase
+    // adds them per 16-byte piece, applies the activation and rounds once.
+    // Without a residual the activation is applied before the bf16 staging
+    // of the plain paths.  Each (row, piece) is read and then written by the
+    // same thread, so the residual may be the output.
     float* stage_f = reinterpret_cast<float*>(stage_out);
-    const __nv_bfloat16* residual_bf = static_cast<const __nv_bfloat16*>(p.residual);
     __nv_bfloat16* out_bf = static_cast<__nv_bfloat16*>(p.out);
-    uint4 res[MBLK][4];
-    auto load_residual = [&](int mb, int64_t nb) {
-      const int ppr = min(128, p.co_count - mb * 128) / 8;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int q = et + 128 * j;
-        res[mb][j] = make_uint4(0u, 0u, 0u, 0u);
-        if (p.residual != nullptr && q < 32 * ppr) {
-          const int r = q / ppr;
-          const int c8 = q - r * ppr;
-          const int64_t row = slot_voxel(p.order, nb + r, n_rows);
-          if (row >= 0)
-            res[mb][j] = __ldg(reinterpret_cast<const uint4*>(residual_bf + row * p.co + p.co_base +
-                                                              mb * 128 + c8 * 8));
-        }
+    const uint32_t stage_base = smem_addr(stage_out);
+    auto issue_window = [&](int64_t n0, int u) {
+      const int c = u / MBLK, mb = u - (u / MBLK) * MBLK;
+      const uint32_t bar = smem_addr(&res_full[u & 1]);
+      fence_proxy_async_smem();  // the window's previous contents were read through the generic proxy
+      const int64_t row = n0 + static_cast<int64_t>(c) * kResRows;
+      if (row >= n_rows) {
+        mbar_arrive(bar);
+      } else {
+        mbar_arrive_expect_tx(bar, kResWindowBytes);
+        tma_load_2d(stage_base + kResWindowOff + static_cast<uint32_t>(u & 1) * kResWindowBytes, &tm_out,
+                    p.co_base + mb * 128, static_cast<int32_t>(row), bar);
       }
     };
+    uint32_t res_phase = 0;    // bit w: the phase window w's barrier waits for next
+    uint32_t res_pending = 0;  // window loads issued and not yet waited for (bits)
+    bool ok_res = true;
     uint32_t tile_i = 0;
     for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++tile_i) {
       const uint32_t buf = tile_i % kAccBufs;
@@ -792,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-      } else if (!fused && p.tma_out) {
+      } else if (p.tma_out) {
         // The staged block (32 rows x MBLK * 128 channels, the rows of out
         // in voxel order) goes out as one TMA store: the thread stores would
         // queue on the load/store pipe behind the gathers (measured: with
@@ -810,9 +820,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             if (co_l < p.co_count) {
               const float b = bias_s[co_l];
+              if (p.act == SPCONV_ACT_NONE) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                stage_out[i * kOutStride + co_l] = __float2bfloat16_rn(__uint_as_float(v[i]) + b);
+                for (int i = 0; i < 32; ++i)
+                  stage_out[i * kOutStride + co_l] = __float2bfloat16_rn(__uint_as_float(v[i]) + b);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  stage_out[i * kOutStride + co_l] =
+                      __float2bfloat16_rn(apply_activation_bf16(__uint_as_float(v[i]) + b, p.act));
+              }
             }
           }
           fence_proxy_async_smem();  // the store reads the block through the async proxy
@@ -822,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit_group();
           }
         }
-      } else if (!fused) {
+      } else if (p.residual == nullptr) {
         for (int vc = 0; vc < TILE_N / 32; ++vc) {
           epilogue_bar();  // the previous chunk's staged rows have been stored
 #pragma unroll
@@ -833,9 +850,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             if (co_l < p.co_count) {
               const float b = bias_s[co_l];
+              if (p.act == SPCONV_ACT_NONE) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                stage_out[i * kOutStride + co_l] = __float2bfloat16_rn(__uint_as_float(v[i]) + b);
+                for (int i = 0; i < 32; ++i)
+                  stage_out[i * kOutStride + co_l] = __float2bfloat16_rn(__uint_as_float(v[i]) + b);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  stage_out[i * kOutStride + co_l] =
+                      __float2bfloat16_rn(apply_activation_bf16(__uint_as_float(v[i]) + b, p.act));
+              }
             }
           }
           epilogue_bar();
@@ -849,54 +873,68 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+        // residual epilogue (bf16); window 0 is free (step nu - 2 of the
+        // previous tile was stored before its step nu - 1 began)
+        constexpr int nu = static_cast<int>(TILE_N / kResRows) * MBLK;
+        if (et == 0) issue_window(n0, 0);
+        res_pending |= 1u;
+        for (int u = 0; u < nu; ++u) {
+          const int c = u / MBLK, mb = u - (u / MBLK) * MBLK;
+          epilogue_bar();  // step u - 1 is stored: its window and the staging are free
+          if (u + 1 < nu) {
+            if (et == 0) issue_window(n0, u + 1);
+            res_pending |= 1u << ((u + 1) & 1);
+          }
+          const int co_s = static_cast<int>(sub) * 32 + static_cast<int>(lane);
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tcol + mb * TILE_N + c * kResRows, v);
+          tmem_ld_wait();
+          const float b = bias_s[mb * 128 + co_s];  // zero beyond co_count
 #pragma unroll
-        for (int mb = 0; mb < MBLK; ++mb) load_residual(mb, n0);
-        for (int vc = 0; vc < TILE_N / 32; ++vc) {
-          const int64_t nb = n0 + vc * 32;
+          for (int i = 0; i < static_cast<int>(kResRows); ++i) stage_f[i * 128 + co_s] = __uint_as_float(v[i]) + b;
+          const uint32_t w = static_cast<uint32_t>(u & 1);
+          ok_res = __all_sync(0xffffffffu, mbar_wait(smem_addr(&res_full[w]), (res_phase >> w) & 1u)) && ok_res;
+          res_phase ^= 1u << w;
+          res_pending &= ~(1u << w);
+          epilogue_bar();  // staged, and every thread saw the window land
+          const __nv_bfloat16* win =
+              reinterpret_cast<const __nv_bfloat16*>(smem + p.off_stage_out + kResWindowOff + w * kResWindowBytes);
+          const int ppr = min(128, p.co_count - mb * 128) / 8;
 #pragma unroll
-          for (int mb = 0; mb < MBLK; ++mb) {
-            const int ppr = min(128, p.co_count - mb * 128) / 8;
-            const int co_s = static_cast<int>(sub) * 32 + static_cast<int>(lane);
-            epilogue_bar();  // the staging buffer is free
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tcol + mb * TILE_N + vc * 32, v);
-            tmem_ld_wait();
-            const float b = bias_s[mb * 128 + co_s];  // zero beyond co_count
+          for (int j = 0; j < 2; ++j) {
+            const int q = et + 128 * j;
+            if (q >= static_cast<int>(kResRows) * ppr) break;
+            const int r = q / ppr;
+            const int c8 = q - r * ppr;
+            const int64_t row = n0 + c * static_cast<int>(kResRows) + r;
+            if (row >= n_rows) continue;
+            const uint4 rr = *reinterpret_cast<const uint4*>(win + r * 128 + c8 * 8);
+            const float4 a0 = *reinterpret_cast<const float4*>(stage_f + r * 128 + c8 * 8);
+            const float4 a1 = *reinterpret_cast<const float4*>(stage_f + r * 128 + c8 * 8 + 4);
+            const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
+            uint32_t o[4];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) stage_f[i * 128 + co_s] = __uint_as_float(v[i]) + b;
-            epilogue_bar();
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int q = et + 128 * j;
-              if (q >= 32 * ppr) continue;
-              const int r = q / ppr;
-              const int c8 = q - r * ppr;
-              const int64_t row = slot_voxel(p.order, nb + r, n_rows);
-              if (row < 0) continue;
-              const float4 a0 = *reinterpret_cast<const float4*>(stage_f + r * 128 + c8 * 8);
-              const float4 a1 = *reinterpret_cast<const float4*>(stage_f + r * 128 + c8 * 8 + 4);
-              const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-              const uint32_t rw[4] = {res[mb][j].x, res[mb][j].y, res[mb][j].z, res[mb][j].w};
-              uint32_t o[4];
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                const float lo = apply_activation_bf16(x[2 * h] + __uint_as_float(rw[h] << 16), p.act);
-                const float hi =
-                    apply_activation_bf16(x[2 * h + 1] + __uint_as_float(rw[h] & 0xFFFF0000u), p.act);
-                const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
-                o[h] = *reinterpret_cast<const uint32_t*>(&pr);
-              }
-              *reinterpret_cast<uint4*>(out_bf + row * p.co + p.co_base + mb * 128 + c8 * 8) =
-                  make_uint4(o[0], o[1], o[2], o[3]);
+            for (int h = 0; h < 4; ++h) {
+              const float lo = apply_activation_bf16(x[2 * h] + __uint_as_float(rw[h] << 16), p.act);
+              const float hi = apply_activation_bf16(x[2 * h + 1] + __uint_as_float(rw[h] & 0xFFFF0000u), p.act);
+              const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+              o[h] = *reinterpret_cast<const uint32_t*>(&pr);
             }
-            if (vc + 1 < TILE_N / 32) load_residual(mb, nb + 32);
+            *reinterpret_cast<uint4*>(out_bf + row * p.co + p.co_base + mb * 128 + c8 * 8) =
+                make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
+        if (!epilogue_all(ok_res)) break;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&tmem_empty[buf]));
     }
+    // Only after a timed-out wait can a window load still be in flight:
+    // wait for it (bounded) before the CTA's memory goes away.
+    for (int w2 = 0; w2 < 2; ++w2)
+      if (res_pending & (1u << w2)) mbar_wait(smem_addr(&res_full[w2]), (res_phase >> w2) & 1u);
     if (p.tma_out && et == 0) bulk_wait_all();  // the last stores are complete
   }
 
@@ -968,7 +1006,7 @@ spconv_status launch_shape(const CUtensorMap& tm_w, const CUtensorMap& tm_out, T
   const uint32_t stage_out_bytes = (32u * MBLK * 128u * 2u > 32u * 128u * 4u) ? 32u * MBLK * 128u * 2u
                                                                               : 32u * 128u * 4u;
   const uint32_t fixed = 2u * p.raw_bytes + ring_bytes + stage_out_bytes + 256u * 4u +
-                         (kMaxStages + kRing) * 4u + (2u * kMaxStages + 2u * kRing + 9u) * 8u + 32u + 1024u;
+                         (kMaxStages + kRing) * 4u + (2u * kMaxStages + 2u * kRing + 11u) * 8u + 32u + 1024u;
   uint32_t stages = (kMaxSmem - fixed) / p.stage_bytes;
   constexpr uint32_t parts = kSplit ? 2u : 1u;
   if (stages * parts > kMaxStages) stages = kMaxStages / parts;
@@ -987,7 +1025,7 @@ spconv_status launch_shape(const CUtensorMap& tm_w, const CUtensorMap& tm_out, T
   off += (stages + kRing) * 4u;
   off = (off + 7u) & ~7u;
   p.off_bars = off;
-  off += (2u * stages * parts + 2u * kRing + 9u) * 8u + 32u;
+  off += (2u * stages * parts + 2u * kRing + 11u) * 8u + 32u;
   const uint32_t smem_bytes = off + 1024u;  // slack for the 1024-byte alignment
 
   auto kern = submconv_tc_kernel<TILE_N, MBLK, kHoist, kDgrad, kSplit, kTf32>;
@@ -1087,7 +1125,8 @@ spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_
     CUtensorMap tm_out;
     std::memset(&tm_out, 0, sizeof tm_out);
     p.tma_out = 0;
-    if (!tf32 && order == nullptr && residual == nullptr && act == SPCONV_ACT_NONE) {
+    p.tma_res = 0;
+    if (!tf32 && order == nullptr && residual == nullptr) {
       const cuuint32_t box_co = p.co_count <= 128 ? 128u : 256u;
       cuuint64_t odims[2] = {static_cast<cuuint64_t>(co), static_cast<cuuint64_t>(n)};
       cuuint64_t ostrides[1] = {static_cast<cuuint64_t>(co) * 2u};
@@ -1099,6 +1138,19 @@ spconv_status launch_conv_tc(spconv_dtype dtype, const void* feats, const int32_
       if (ro != CUDA_SUCCESS)
         return fail(SPCONV_ERR_CUDA, "cuTensorMapEncodeTiled(out) failed: " + std::to_string(ro));
       p.tma_out = 1;
+    } else if (!tf32 && order == nullptr && residual != nullptr) {
+      // The residual (N, Co) by 16-row windows of 128 channels (channels
+      // past Co and rows past N read as zero).
+      cuuint64_t rdims[2] = {static_cast<cuuint64_t>(co), static_cast<cuuint64_t>(n)};
+      cuuint64_t rstrides[1] = {static_cast<cuuint64_t>(co) * 2u};
+      cuuint32_t rbox[2] = {128u, kResRows};
+      cuuint32_t restr[2] = {1, 1};
+      CUresult rr = encode(&tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(residual), rdims,
+                           rstrides, rbox, restr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (rr != CUDA_SUCCESS)
+        return fail(SPCONV_ERR_CUDA, "cuTensorMapEncodeTiled(residual) failed: " + std::to_string(rr));
+      p.tma_res = 1;
     }
     if (tf32) {
       // one 32-channel chunk per stage (48 KB, or 64 KB with two M blocks)
