@@ -720,9 +720,15 @@ def run_ours(args):
 
         plain_ms = time_calls(torch, lambda: conv(feats, nmap, w, bias, out2, xrun), stream)
         fused_ms = time_calls(torch, fused_conv, stream)
-        sv.device_status()
         epilogue = {"plain_ms": plain_ms, "fused_ms": fused_ms, "ratio": fused_ms / plain_ms,
-                    "act": "silu", "residual": True}
+                    "act": "silu", "residual": True, "kernel": XRUN_KERNEL if xrun is not None else DOMINANT_KERNEL}
+        if xrun is not None:
+            # the voxel-tile kernel's fused epilogue on the same inputs
+            tp = time_calls(torch, lambda: sv.submconv3d(feats, nmap, w, bias, out=out2, dtype=tf), stream)
+            tf_ms = time_calls(torch, lambda: sv.submconv3d(feats, nmap, w, bias, out=out2, residual=res,
+                                                              activation="silu", dtype=tf), stream)
+            epilogue["tiles"] = {"plain_ms": tp, "fused_ms": tf_ms, "ratio": tf_ms / tp, "kernel": DOMINANT_KERNEL}
+        sv.device_status()
         del res, out2
         torch.cuda.empty_cache()
 

@@ -262,3 +262,73 @@ def test_fused_build_and_layout_at_full_size(sv, oracle_mod):
     assert int(count.item()) == int(count2.item())
     s = int(count.item())
     assert torch.equal(slots[:s], slots2[:s])
+
+
+def bracketed_runs_layout(coords, seed):
+    """Another valid layout of the same voxels: every run between its own
+    left and right separator (none shared), the runs in a seeded random
+    order.  Voxels of one 16- or 32-slot chunk then do not have consecutive
+    indices, which the fused epilogue's residual windows must handle."""
+    n = len(coords)
+    c = coords.astype(np.int64)
+    cont = np.zeros(n, bool)
+    cont[:-1] = (c[1:, 0] == c[:-1, 0]) & (c[1:, 1] == c[:-1, 1]) & (c[1:, 2] == c[:-1, 2] + 1)
+    starts = np.concatenate([[0], np.nonzero(~cont[:-1])[0] + 1])
+    ends = np.concatenate([starts[1:], [n]])
+    runs = [np.concatenate([[-3 - 2 * a], np.arange(a, b), [-2 - 2 * (b - 1)]]) for a, b in zip(starts, ends)]
+    order = np.random.default_rng(seed).permutation(len(runs))
+    return np.concatenate([runs[i] for i in order]).astype(np.int32)
+
+
+@pytest.mark.parametrize("name", ["random", "dense", "line"])
+def test_xrun_conv_on_a_shuffled_bracketed_layout(sv, oracle_mod, name):
+    """The conv, its fused epilogue and the input gradient on a layout whose
+    runs come in random order: the same sums as on the regular layout."""
+    import torch
+    coords = shapes()[name]
+    n = len(coords)
+    nmap = oracle_mod.build_nmap(coords, W.offsets_3x3x3())
+    slots_np = bracketed_runs_layout(coords, seed=n)
+    nm = torch.from_numpy(np.ascontiguousarray(nmap, dtype=np.int32)).cuda()
+    slots = torch.from_numpy(slots_np).cuda()
+    count = torch.tensor([len(slots_np)], dtype=torch.int64, device="cuda")
+    feats = W.values(n, 51, (n, 128), "bf16")
+    w = W.values(n, 52, (27, 128, 128), "bf16", 1.0 / np.sqrt(27 * 128))
+    b = W.values(n, 53, (128,), "bf16", 0.1)
+    res = W.values(n, 54, (n, 128), "bf16")
+    f, ww, bb, r = (torch_storage(x, "bf16") for x in (feats, w, b, res))
+    out = sv.submconv3d_xrun(f, nm, slots, count, ww, bb)
+    fused = sv.submconv3d_xrun(f, nm, slots, count, ww, bb, residual=r, activation="silu")
+    dg = sv.submconv3d_dgrad_xrun(f, nm, slots, count, ww)
+    sv.device_status()
+    ref, sabs = oracle_mod.conv(feats, nmap, w, b, "bf16", threads=oracle_mod.host_threads())
+    assert_within(to_f64(out), ref, sabs, "bf16")
+    assert_near_plain(out, sv.submconv3d(f, nm, ww, bb), sabs)
+    fref, fscale = oracle_mod.conv_fused(feats, nmap, w, b, "bf16", residual=res, act="silu",
+                                         threads=oracle_mod.host_threads())
+    assert_within(to_f64(fused), fref, fscale, "bf16")
+    dref, dabs = oracle_mod.dgrad(feats, nmap, w, "bf16", threads=oracle_mod.host_threads())
+    assert_within(to_f64(dg), dref, dabs, "bf16")
+
+
+def test_xrun_fused_epilogue_full_size_sample(sv, oracle_mod):
+    """Medium workload at full size (1.0 M voxels, 1.12 M slots), residual
+    + SiLU in place: sampled rows against the oracle, every row near the
+    voxel-tile kernel's fused epilogue."""
+    import torch
+    wl = W.make("medium")
+    layer = wl.layers[0]
+    c = torch.from_numpy(wl.coords).cuda()
+    nm, slots, count = sv.build_nmap_xrun(c)
+    res = W.values(77, 61, (wl.N, layer.Co), "bf16")
+    f, ww, bb = (torch_storage(x, "bf16") for x in (layer.feats, layer.w, layer.bias))
+    r = torch_storage(res, "bf16")
+    tiles = sv.submconv3d(f, nm, ww, bb, residual=r, activation="silu")
+    out = r.clone()
+    sv.submconv3d_xrun(f, nm, slots, count, ww, bb, out=out, residual=out, activation="silu")
+    sv.device_status()
+    assert_near_plain(out, tiles)
+    rows = sample_rows(wl.N, 1500, seed=8)
+    ref, scale = oracle_mod.conv_fused(layer.feats, nm.cpu().numpy(), layer.w, layer.bias, "bf16", residual=res,
+                                       act="silu", rows=rows, threads=oracle_mod.host_threads())
+    assert_within(to_f64(out[torch.from_numpy(rows).cuda()]), ref, scale, "bf16")
