@@ -892,12 +892,12 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         **({"epilogue": epilogue} if epilogue is not None else {}),
-        # per step: the map build's eight kernels (flag reset, range/order/box
-        # check, clear, insert, dense-row prefix, dense-row query, row-hash
-        # query, voxel-hash query: the paths not taken return at once) and
-        # one conv launch (Co <= 256) (with --xrun: three layout kernels and
-        # one conv launch)
-        "gpu_launches": ((8 + 3 + 1) if args.xrun else (8 + (co + 255) // 256)) * args.steps,
+        # per step: the map build's seven kernels (flag reset, range/order/box
+        # check, clear, insert, dense-row query, row-hash query, voxel-hash
+        # query: the paths not taken return at once) and one conv launch
+        # (Co <= 256) (on the x-run path: three layout kernels and one conv
+        # launch)
+        "gpu_launches": ((7 + 3 + 1) if args.xrun else (7 + (co + 255) // 256)) * args.steps,
         "clocks": clocks,
         "generation_s": gen_s,
         **({"per_config": per_config} if per_config is not None else {}),

@@ -10,20 +10,18 @@
 // path returns at once):
 //
 // Sorted input whose bounding box is small enough (the usual case: a
-// voxeliser emits sorted coordinates in a bounded grid).  Each (z, y) row of
-// cells is a contiguous run of voxels, and the box's rows are laid out
-// densely in the workspace: per row the index of its first voxel, and per
-// 32 cells of a row an occupancy word with the count of the row's voxels
-// before it.  A neighbour at x is then one word load: present if its bit is
-// set, at index row start + count before the word + popcount of the lower
-// bits.  No search and no probe:
+// voxeliser emits sorted coordinates in a bounded grid).  The voxels of 32
+// consecutive cells of a (z, y) row have consecutive indices, so the box's
+// rows are laid out densely in the workspace as words of 32 cells: an
+// occupancy bit per cell and the index of the word's first voxel.  A
+// neighbour at x is then one word load: present if its bit is set, at index
+// first + popcount of the lower bits.  No search and no probe:
 //
-//   clear   row starts := -1, words := 0
-//   insert  the first voxel of each row writes the row start; every voxel
-//           sets its bit (one atomic OR per word and warp)
-//   prefix  one warp per row: exclusive prefix of the words' popcounts
-//   query   one thread per voxel: per (dz, dy) row one row-start load, then
-//           one word load per dx
+//   clear   words := 0
+//   insert  every voxel sets its bit (one atomic OR per word and warp); the
+//           first voxel of each word writes its index
+//   query   one thread per voxel: per (dz, dy) row one word load for x - 1,
+//           x and x + 1 (two at a word edge)
 //
 // Sorted input with a larger box.  A hash of rows (row -> index of its first
 // voxel, table sized from the row count) is enough:
@@ -203,8 +201,7 @@ struct DenseRows {
   int32_t nz, ny, nx;  // box extents
   int32_t wpr;         // occupancy words per row
   uint32_t rows;       // nz * ny
-  uint2* words;        // rows * wpr entries {occupancy bits, voxels of the row before the word}
-  int32_t* row_start;  // rows entries, -1 for an empty row
+  uint2* words;        // rows * wpr entries {occupancy bits, index of the word's first voxel}
 };
 
 // Whether the build takes the dense path (sorted, in range, and the box's
@@ -221,7 +218,7 @@ __device__ __forceinline__ bool dense_rows(const int* flags, void* table, unsign
   const unsigned long long wpr = (nx + 31ull) >> 5;
   const unsigned long long rows = nz * ny;
   if (rows >= (1ull << 31) || rows * wpr >= (1ull << 31)) return false;
-  if (rows * wpr * 8ull + rows * 4ull > table_bytes) return false;
+  if (rows * wpr * 8ull > table_bytes) return false;
   d->zmin = zmin;
   d->ymin = ymin;
   d->xmin = xmin;
@@ -231,7 +228,6 @@ __device__ __forceinline__ bool dense_rows(const int* flags, void* table, unsign
   d->wpr = static_cast<int32_t>(wpr);
   d->rows = static_cast<uint32_t>(rows);
   d->words = static_cast<uint2*>(table);
-  d->row_start = reinterpret_cast<int32_t*>(d->words + rows * wpr);
   return true;
 }
 
@@ -312,7 +308,6 @@ __global__ void hash_clear_kernel(Slot* table, unsigned long long cap, int* flag
   if (dense_rows(flags, table, cap * sizeof(Slot), &d)) {  // sorted, small box: the dense rows
     const unsigned long long nw = static_cast<unsigned long long>(d.rows) * d.wpr;
     for (unsigned long long i = tid; i < nw; i += stride) d.words[i] = make_uint2(0u, 0u);
-    for (unsigned long long i = tid; i < d.rows; i += stride) d.row_start[i] = -1;
     return;
   }
   if (!(f & kFlagUnsorted)) {  // sorted input: only the row table
@@ -339,9 +334,10 @@ __global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n
   if (f & kFlagRange) return;
   DenseRows d;
   if (dense_rows(flags, table, (mask + 1ull) * sizeof(Slot), &d)) {
-    // dense rows: the first voxel of each row writes the row start, every
-    // voxel sets its occupancy bit (the voxels of one word and warp combine
-    // their bits first: one atomic OR each)
+    // dense rows: every voxel sets its occupancy bit (the voxels of one word
+    // and warp combine their bits first: one atomic OR each); the first
+    // voxel of each word (the input being sorted, the word's voxels have
+    // consecutive indices) writes its index beside the bits
     const bool live = i < n;
     uint32_t word = 0xFFFFFFFFu, bit = 0u;
     if (live) {
@@ -351,9 +347,19 @@ __global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n
       const uint32_t cx = static_cast<uint32_t>(x - d.xmin);
       word = row * static_cast<uint32_t>(d.wpr) + (cx >> 5);
       bit = 1u << (cx & 31u);
-      if (i == 0 || coords[3 * (i - 1)] != z || coords[3 * (i - 1) + 1] != y)
-        d.row_start[row] = static_cast<int32_t>(i);
     }
+    // the previous voxel's word: from the lane before, or loaded by lane 0
+    uint32_t prev_word = __shfl_up_sync(0xffffffffu, word, 1);
+    if ((threadIdx.x & 31u) == 0u && live) {
+      prev_word = 0xFFFFFFFEu;
+      if (i > 0) {
+        const int pz = coords[3 * (i - 1)], py = coords[3 * (i - 1) + 1], px = coords[3 * (i - 1) + 2];
+        prev_word = (static_cast<uint32_t>(pz - d.zmin) * static_cast<uint32_t>(d.ny) +
+                     static_cast<uint32_t>(py - d.ymin)) * static_cast<uint32_t>(d.wpr) +
+                    (static_cast<uint32_t>(px - d.xmin) >> 5);
+      }
+    }
+    if (live && prev_word != word) d.words[word].y = static_cast<uint32_t>(i);
     const uint32_t peers = __match_any_sync(0xffffffffu, word);
     const uint32_t bits = __reduce_or_sync(peers, bit);
     if (live && (threadIdx.x & 31u) == static_cast<uint32_t>(__ffs(peers) - 1)) atomicOr(&d.words[word].x, bits);
@@ -422,56 +428,30 @@ __global__ void hash_insert_kernel(const int32_t* __restrict__ coords, int64_t n
   atomicOr(flags, kFlagFull);
 }
 
-// Dense rows: per row (one warp each), the count of the row's voxels before
-// each occupancy word (exclusive prefix of the words' popcounts).
-__global__ void __launch_bounds__(kThreads) dense_prefix_kernel(int* flags, void* table,
-                                                                unsigned long long table_bytes) {
-  DenseRows d;
-  if (!dense_rows(flags, table, table_bytes, &d)) return;
-  const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t warps = gridDim.x * (blockDim.x >> 5);
-  for (uint32_t row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < d.rows; row += warps) {
-    if (d.row_start[row] < 0) continue;  // empty row: never read
-    uint2* w = d.words + static_cast<size_t>(row) * d.wpr;
-    uint32_t carry = 0;
-    for (int32_t base = 0; base < d.wpr; base += 32) {
-      const int32_t j = base + static_cast<int32_t>(lane);
-      const uint32_t c = j < d.wpr ? __popc(w[j].x) : 0u;
-      uint32_t incl = c;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= static_cast<uint32_t>(off)) incl += v;
-      }
-      if (j < d.wpr) w[j].y = carry + incl - c;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
-}
-
-// Dense rows: the voxel at (zq, yq, xq), or `missing`.
-__device__ __forceinline__ int32_t dense_lookup(const DenseRows& d, int32_t rs, uint32_t wbase, int xq,
+// Dense rows: the voxel at (zq, yq, xq) of a row inside the box (`inbox`,
+// its words from wbase), or `missing`.
+__device__ __forceinline__ int32_t dense_lookup(const DenseRows& d, bool inbox, uint32_t wbase, int xq,
                                                int32_t missing) {
   const uint32_t cx = static_cast<uint32_t>(xq - d.xmin);
-  if (rs < 0 || cx >= static_cast<uint32_t>(d.nx)) return missing;
+  if (!inbox || cx >= static_cast<uint32_t>(d.nx)) return missing;
   const uint2 e = __ldg(d.words + wbase + (cx >> 5));
   const uint32_t b = cx & 31u;
   if (((e.x >> b) & 1u) == 0u) return missing;
-  return rs + static_cast<int32_t>(e.y + __popc(e.x & ((1u << b) - 1u)));
+  return static_cast<int32_t>(e.y + __popc(e.x & ((1u << b) - 1u)));
 }
 
 // Dense rows: the voxels at x - 1, x and x + 1 of one row (cx = x - xmin,
 // inside the box), from the occupancy word that holds cx; the word before or
 // after it is read only when cx is its first or last bit.
-__device__ __forceinline__ void dense_lookup3(const DenseRows& d, int32_t rs, uint32_t wbase, uint32_t cx,
+__device__ __forceinline__ void dense_lookup3(const DenseRows& d, bool inbox, uint32_t wbase, uint32_t cx,
                                               int32_t missing, int32_t* left, int32_t* mid, int32_t* right) {
   *left = missing;
   *mid = missing;
   *right = missing;
-  if (rs < 0) return;
+  if (!inbox) return;
   const uint32_t wi = cx >> 5, b = cx & 31u;
   const uint2 e = __ldg(d.words + wbase + wi);
-  const int32_t base = rs + static_cast<int32_t>(e.y);
+  const int32_t base = static_cast<int32_t>(e.y);
   const uint32_t own = (e.x >> b) & 1u;
   const int32_t rank = base + __popc(e.x & ((1u << b) - 1u));  // voxels of the row before cx
   if (own) *mid = rank;
@@ -479,27 +459,29 @@ __device__ __forceinline__ void dense_lookup3(const DenseRows& d, int32_t rs, ui
     if ((e.x >> (b - 1u)) & 1u) *left = rank - 1;
   } else if (wi > 0u) {
     const uint2 f = __ldg(d.words + wbase + wi - 1u);
-    if (f.x >> 31) *left = rs + static_cast<int32_t>(f.y) + __popc(f.x) - 1;
+    if (f.x >> 31) *left = static_cast<int32_t>(f.y) + __popc(f.x) - 1;
   }
   if (b < 31u) {
     if ((e.x >> (b + 1u)) & 1u) *right = rank + static_cast<int32_t>(own);
   } else if (cx + 1u < static_cast<uint32_t>(d.nx)) {
     const uint2 f = __ldg(d.words + wbase + wi + 1u);
-    if (f.x & 1u) *right = rs + static_cast<int32_t>(f.y);
+    if (f.x & 1u) *right = static_cast<int32_t>(f.y);
   }
 }
 
-// Sorted input, dense rows: nmap[k, n] for every offset, by one row-start
-// load per (dz, dy) row and, for the lexicographic 3x3x3 list, one
-// occupancy-word load per row (two at a word edge); else one per offset.
+// Sorted input, dense rows: nmap[k, n] for every offset; for the
+// lexicographic 3x3x3 list one occupancy-word load per (dz, dy) row (two at a
+// word edge), else one per offset.
 // kXFlags (lexicographic 3x3x3 list only): also what the x-run layout
 // (xrun.cu) needs of each voxel, from the entries in registers: bit 0 the
 // voxel ends a run (no voxel at x + 1), bit 1 one of its nine (dz, dy, +1)
 // cells is active, bit 2 one of its nine (dz, dy, -1) cells is active, bit 3
 // the voxel ends a run and the cell (z, y, x + 2) is active (then, the input
 // being sorted, that cell is the next voxel's).
+// Eight blocks per SM (32 registers): the query waits on its loads, so the
+// extra warps pay (measured at decoder scale: build 0.606 -> 0.590 ms).
 template <bool kStd27, bool kXFlags>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 8)
     nmap_query_dense_kernel(const int32_t* __restrict__ coords, int64_t n, void* table,
                             unsigned long long table_bytes, int* flags,
                             const __grid_constant__ QueryPlan plan, int32_t* __restrict__ nmap,
@@ -513,15 +495,10 @@ __global__ void __launch_bounds__(kThreads)
   const int32_t missing = static_cast<int32_t>(n);
   const int z = __ldg(coords + 3 * static_cast<int64_t>(i)), y = __ldg(coords + 3 * static_cast<int64_t>(i) + 1);
   const int x = __ldg(coords + 3 * static_cast<int64_t>(i) + 2);
-  auto row_of = [&](int zq, int yq, int32_t* rs, uint32_t* wbase) {
+  auto row_of = [&](int zq, int yq, bool* inbox, uint32_t* wbase) {
     const uint32_t rz = static_cast<uint32_t>(zq - d.zmin), ry = static_cast<uint32_t>(yq - d.ymin);
-    *rs = -1;
-    *wbase = 0;
-    if (rz < static_cast<uint32_t>(d.nz) && ry < static_cast<uint32_t>(d.ny)) {
-      const uint32_t row = rz * static_cast<uint32_t>(d.ny) + ry;
-      *rs = __ldg(d.row_start + row);
-      *wbase = row * static_cast<uint32_t>(d.wpr);
-    }
+    *inbox = rz < static_cast<uint32_t>(d.nz) && ry < static_cast<uint32_t>(d.ny);
+    *wbase = *inbox ? (rz * static_cast<uint32_t>(d.ny) + ry) * static_cast<uint32_t>(d.wpr) : 0u;
   };
   if constexpr (kStd27) {
     bool any_left = false, any_right = false, run_end = false, next_at_2 = false;  // kXFlags
@@ -530,11 +507,11 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int dy = -1; dy <= 1; ++dy) {
         const int k0 = 9 * (dz + 1) + 3 * (dy + 1);  // offset (dz, dy, -1); +1, +2 follow
-        int32_t rs;
+        bool in_box;
         uint32_t wbase;
-        row_of(z + dz, y + dy, &rs, &wbase);
+        row_of(z + dz, y + dy, &in_box, &wbase);
         int32_t left, mid, right;
-        dense_lookup3(d, rs, wbase, static_cast<uint32_t>(x - d.xmin), missing, &left, &mid, &right);
+        dense_lookup3(d, in_box, wbase, static_cast<uint32_t>(x - d.xmin), missing, &left, &mid, &right);
         nmap[static_cast<int64_t>(k0) * n + i] = left;
         nmap[static_cast<int64_t>(k0 + 1) * n + i] = (dz == 0 && dy == 0) ? i : mid;
         nmap[static_cast<int64_t>(k0 + 2) * n + i] = right;
@@ -544,7 +521,7 @@ __global__ void __launch_bounds__(kThreads)
           if (dz == 0 && dy == 0) {
             run_end = right == missing;
             // sorted input: after a run end, the next voxel is (z, y, x + 2) when that cell is active
-            next_at_2 = run_end && dense_lookup(d, rs, wbase, x + 2, missing) != missing;
+            next_at_2 = run_end && dense_lookup(d, in_box, wbase, x + 2, missing) != missing;
           }
         }
       }
@@ -556,12 +533,12 @@ __global__ void __launch_bounds__(kThreads)
     }
   } else {
     for (int32_t g = 0; g < plan.groups; ++g) {
-      int32_t rs;
+      bool in_box;
       uint32_t wbase;
-      row_of(z + plan.grp_dz[g], y + plan.grp_dy[g], &rs, &wbase);
+      row_of(z + plan.grp_dz[g], y + plan.grp_dy[g], &in_box, &wbase);
       const int m0 = plan.grp_first[g], m1 = m0 + plan.grp_count[g];
       for (int m = m0; m < m1; ++m)
-        nmap[static_cast<int64_t>(plan.mem_k[m]) * n + i] = dense_lookup(d, rs, wbase, x + plan.mem_dx[m], missing);
+        nmap[static_cast<int64_t>(plan.mem_k[m]) * n + i] = dense_lookup(d, in_box, wbase, x + plan.mem_dx[m], missing);
     }
   }
 }
@@ -874,11 +851,9 @@ spconv_status launch_build_nmap(const int32_t* coords, int64_t n, const BuildOff
   hash_insert_kernel<<<grid, kThreads, 0, stream>>>(coords, n, table, cap - 1, flags);
   if (!cuda_ok(cudaGetLastError(), "hash_insert_kernel launch", &st)) return st;
 
-  // Dense-row path (sorted input, small box): per-row word prefixes, then
-  // the query; both return at once on the other paths.
+  // Dense-row path (sorted input, small box): the query; it returns at
+  // once on the other paths.
   const unsigned long long table_bytes = static_cast<unsigned long long>(cap) * sizeof(Slot);
-  dense_prefix_kernel<<<16u * static_cast<unsigned>(sms), kThreads, 0, stream>>>(flags, table, table_bytes);
-  if (!cuda_ok(cudaGetLastError(), "dense_prefix_kernel launch", &st)) return st;
   bool std27 = k == 27;
   for (int32_t a = 0; a < k && std27; ++a)
     std27 = offs.d[3 * a] == a / 9 - 1 && offs.d[3 * a + 1] == (a / 3) % 3 - 1 && offs.d[3 * a + 2] == a % 3 - 1;
