@@ -199,37 +199,44 @@ __global__ void __launch_bounds__(kXrunBlock) xrun_scan_kernel(int64_t* __restri
 
 // Each voxel writes its slot and the separators around it (kXrunPer
 // consecutive voxels per thread, as in the count).  A block's slots number
-// at most 4 * kXrunBlock * kXrunPer, so the in-block scan is 32-bit.
+// at most 4 * kXrunBlock * kXrunPer, so the in-block scan is 32-bit.  They
+// are assembled in shared memory (dynamic, kFillSmem bytes) and written out
+// in one coalesced pass: written straight from the threads, each store
+// instruction of a warp touched 32 short runs a few slots apart.
+constexpr uint32_t kFillSmem = 4u * kXrunBlock * kXrunPer * 4u;
 __global__ void __launch_bounds__(kXrunBlock) xrun_fill_kernel(const uint8_t* __restrict__ flags, int64_t n,
                                                                const int64_t* __restrict__ block_offsets,
                                                                int32_t* __restrict__ slots, int64_t cap,
                                                                int32_t* __restrict__ overflow,
                                                                const int* __restrict__ ready,
                                                                const uint8_t* __restrict__ raw) {
+  extern __shared__ int32_t block_slots[];
   __shared__ uint32_t warp_sums[32];
   const int64_t i0 = (static_cast<int64_t>(blockIdx.x) * kXrunBlock + threadIdx.x) * kXrunPer;
   const bool pre = ready != nullptr && *ready != 0;
   const uint32_t f4 = i0 < n ? flags4(flags, raw, pre, n, i0) : 0u;
   const uint32_t cnt = i0 < n ? slot_count4(f4, n, i0) : 0u;
   uint32_t ex;
-  block_exclusive_scan<uint32_t>(cnt, warp_sums, &ex);
-  if (i0 >= n) return;
-  int64_t s = block_offsets[blockIdx.x] + ex;
-  if (s + cnt > cap) {
-    atomicExch(overflow, 1);
+  const uint32_t total = block_exclusive_scan<uint32_t>(cnt, warp_sums, &ex);
+  const int64_t s0 = block_offsets[blockIdx.x];
+  if (s0 + total > cap) {  // the same for every thread of the block
+    if (threadIdx.x == 0) atomicExch(overflow, 1);
     return;
   }
+  uint32_t s = ex;
 #pragma unroll
   for (int j = 0; j < kXrunPer; ++j) {
     if (i0 + j >= n) break;
     const uint32_t f = (f4 >> (8 * j)) & 0xffu;
     const int32_t v = static_cast<int32_t>(i0 + j);
-    if (f & 4u) slots[s++] = -3 - 2 * v;  // left of voxel 0
-    slots[s++] = v;
+    if (f & 4u) block_slots[s++] = -3 - 2 * v;  // left of voxel 0
+    block_slots[s++] = v;
     const uint32_t after = f & 3u;
-    if (after >= 1u) slots[s++] = -2 - 2 * v;        // right of this run end (shared when one)
-    if (after == 2u) slots[s++] = -3 - 2 * (v + 1);  // left of the next run's start
+    if (after >= 1u) block_slots[s++] = -2 - 2 * v;        // right of this run end (shared when one)
+    if (after == 2u) block_slots[s++] = -3 - 2 * (v + 1);  // left of the next run's start
   }
+  __syncthreads();
+  for (uint32_t k = threadIdx.x; k < total; k += kXrunBlock) slots[s0 + k] = block_slots[k];
 }
 
 }  // namespace
@@ -263,8 +270,12 @@ spconv_status launch_xrun_layout(const int32_t* coords, const int32_t* nmap, int
   if (!cuda_ok(cudaGetLastError(), "xrun_count_kernel", &st)) return st;
   xrun_scan_kernel<<<1, kXrunBlock, 0, stream>>>(block_sums, nb, slot_count);
   if (!cuda_ok(cudaGetLastError(), "xrun_scan_kernel", &st)) return st;
-  xrun_fill_kernel<<<static_cast<unsigned>(nb), kXrunBlock, 0, stream>>>(flags, n, block_sums, slots, cap,
-                                                                           overflow, flags_ready, raw);
+  if (!cuda_ok(cudaFuncSetAttribute(xrun_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(kFillSmem)),
+               "cudaFuncSetAttribute", &st))
+    return st;
+  xrun_fill_kernel<<<static_cast<unsigned>(nb), kXrunBlock, kFillSmem, stream>>>(flags, n, block_sums, slots, cap,
+                                                                                   overflow, flags_ready, raw);
   if (!cuda_ok(cudaGetLastError(), "xrun_fill_kernel", &st)) return st;
   return SPCONV_OK;
 }
