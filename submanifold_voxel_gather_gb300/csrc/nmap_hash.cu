@@ -248,33 +248,12 @@ __global__ void __launch_bounds__(kThreads) order_check_kernel(const int32_t* __
   int my_bits = 0;
   unsigned int my_rows = 0;
   int lo[3] = {INT_MAX, INT_MAX, INT_MAX}, hi[3] = {INT_MIN, INT_MIN, INT_MIN};
-  // Each warp takes 32 consecutive voxels per step; the neighbouring
-  // voxels' coordinates come from the lanes beside (loaded at the warp's
-  // edges), so each voxel is read once.
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const uint32_t lane = threadIdx.x & 31u;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31u); base < n;
-       base += stride) {
-    const int64_t i = base + lane;
-    const bool live = i < n;
-    int z = 0, y = 0, x = 0;
-    if (live) {
-      z = __ldg(coords + 3 * i);
-      y = __ldg(coords + 3 * i + 1);
-      x = __ldg(coords + 3 * i + 2);
-    }
-    const unsigned long long key = pack_coord(z, y, x);
-    unsigned long long next_key = __shfl_down_sync(0xffffffffu, key, 1);
-    int pz = __shfl_up_sync(0xffffffffu, z, 1), py = __shfl_up_sync(0xffffffffu, y, 1);
-    if (!live) continue;
-    if (lane == 31u && i + 1 < n) next_key = voxel_key(coords, i + 1);
-    if (lane == 0u && i > 0) {
-      pz = __ldg(coords + 3 * (i - 1));
-      py = __ldg(coords + 3 * (i - 1) + 1);
-    }
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int z = __ldg(coords + 3 * i), y = __ldg(coords + 3 * i + 1), x = __ldg(coords + 3 * i + 2);
     if (!in_grid(z) || !in_grid(y) || !in_grid(x)) my_bits |= kFlagRange;
-    if (i + 1 < n && !(key < next_key)) my_bits |= kFlagUnsorted;
-    if (i == 0 || pz != z || py != y) ++my_rows;
+    if (i + 1 < n && !(pack_coord(z, y, x) < voxel_key(coords, i + 1))) my_bits |= kFlagUnsorted;
+    if (i == 0 || __ldg(coords + 3 * (i - 1)) != z || __ldg(coords + 3 * (i - 1) + 1) != y) ++my_rows;
     lo[0] = min(lo[0], z);
     hi[0] = max(hi[0], z);
     lo[1] = min(lo[1], y);
