@@ -578,6 +578,16 @@ def time_calls(torch, fn, stream, reps=5, warmup=2):
     return e0.elapsed_time(e1) / reps
 
 
+def time_pair(torch, fa, fb, stream, rounds=4, reps=2):
+    """Median device times of fa() and fb(), measured in alternation (a
+    clock that drifts during the run then biases neither)."""
+    ta, tb = [], []
+    for _ in range(rounds):
+        ta.append(time_calls(torch, fa, stream, reps=reps, warmup=1))
+        tb.append(time_calls(torch, fb, stream, reps=reps, warmup=1))
+    return float(np.median(ta)), float(np.median(tb))
+
+
 def xrun_supported(layer, wl):
     """Shapes the row-shifted conv takes: bf16, Ci = 128, Co <= 128, the 27
     lexicographic 3x3x3 offsets."""
@@ -718,15 +728,14 @@ def run_ours(args):
             else:
                 sv.submconv3d(feats, nmap, w, bias, out=out2, residual=res, activation="silu", dtype=tf)
 
-        plain_ms = time_calls(torch, lambda: conv(feats, nmap, w, bias, out2, xrun), stream)
-        fused_ms = time_calls(torch, fused_conv, stream)
+        plain_ms, fused_ms = time_pair(torch, lambda: conv(feats, nmap, w, bias, out2, xrun), fused_conv, stream)
         epilogue = {"plain_ms": plain_ms, "fused_ms": fused_ms, "ratio": fused_ms / plain_ms,
                     "act": "silu", "residual": True, "kernel": XRUN_KERNEL if xrun is not None else DOMINANT_KERNEL}
         if xrun is not None:
             # the voxel-tile kernel's fused epilogue on the same inputs
-            tp = time_calls(torch, lambda: sv.submconv3d(feats, nmap, w, bias, out=out2, dtype=tf), stream)
-            tf_ms = time_calls(torch, lambda: sv.submconv3d(feats, nmap, w, bias, out=out2, residual=res,
-                                                              activation="silu", dtype=tf), stream)
+            tp, tf_ms = time_pair(torch, lambda: sv.submconv3d(feats, nmap, w, bias, out=out2, dtype=tf),
+                                  lambda: sv.submconv3d(feats, nmap, w, bias, out=out2, residual=res,
+                                                        activation="silu", dtype=tf), stream)
             epilogue["tiles"] = {"plain_ms": tp, "fused_ms": tf_ms, "ratio": tf_ms / tp, "kernel": DOMINANT_KERNEL}
         sv.device_status()
         del res, out2

@@ -746,6 +746,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.co_base + mb * 128, static_cast<int32_t>(row), bar);
       }
     };
+    // This thread's 16-byte output pieces of a 16-row block of M block mb:
+    // (row, 8-channel column), the same in every step, computed once.
+    int prow[MBLK][2], pcol[MBLK][2], npieces[MBLK];
+#pragma unroll
+    for (int mb = 0; mb < MBLK; ++mb) {
+      const int ppr = max(0, min(128, p.co_count - mb * 128) / 8);
+      npieces[mb] = static_cast<int>(kResRows) * ppr;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int q = et + 128 * j;
+        prow[mb][j] = ppr > 0 ? q / ppr : 0;
+        pcol[mb][j] = (q - prow[mb][j] * ppr) * 8;
+      }
+    }
     uint32_t res_phase = 0;    // bit w: the phase window w's barrier waits for next
     uint32_t res_pending = 0;  // window loads issued and not yet waited for (bits)
     bool ok_res = true;
@@ -825,10 +839,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 32; ++i)
                   stage_out[i * kOutStride + co_l] = __float2bfloat16_rn(__uint_as_float(v[i]) + b);
               } else {
+                with_activation(p.act, [&](auto tag) {
+                  constexpr int kA = decltype(tag)::value;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  stage_out[i * kOutStride + co_l] =
-                      __float2bfloat16_rn(apply_activation_bf16(__uint_as_float(v[i]) + b, p.act));
+                  for (int i = 0; i < 32; ++i)
+                    stage_out[i * kOutStride + co_l] =
+                        __float2bfloat16_rn(activation_bf16<kA>(__uint_as_float(v[i]) + b));
+                });
               }
             }
           }
@@ -855,10 +872,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 32; ++i)
                   stage_out[i * kOutStride + co_l] = __float2bfloat16_rn(__uint_as_float(v[i]) + b);
               } else {
+                with_activation(p.act, [&](auto tag) {
+                  constexpr int kA = decltype(tag)::value;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  stage_out[i * kOutStride + co_l] =
-                      __float2bfloat16_rn(apply_activation_bf16(__uint_as_float(v[i]) + b, p.act));
+                  for (int i = 0; i < 32; ++i)
+                    stage_out[i * kOutStride + co_l] =
+                        __float2bfloat16_rn(activation_bf16<kA>(__uint_as_float(v[i]) + b));
+                });
               }
             }
           }
@@ -899,31 +919,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           epilogue_bar();  // staged, and every thread saw the window land
           const __nv_bfloat16* win =
               reinterpret_cast<const __nv_bfloat16*>(smem + p.off_stage_out + kResWindowOff + w * kResWindowBytes);
-          const int ppr = min(128, p.co_count - mb * 128) / 8;
+          with_activation(p.act, [&](auto tag) {
+            constexpr int kA = decltype(tag)::value;
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int q = et + 128 * j;
-            if (q >= static_cast<int>(kResRows) * ppr) break;
-            const int r = q / ppr;
-            const int c8 = q - r * ppr;
-            const int64_t row = n0 + c * static_cast<int>(kResRows) + r;
-            if (row >= n_rows) continue;
-            const uint4 rr = *reinterpret_cast<const uint4*>(win + r * 128 + c8 * 8);
-            const float4 a0 = *reinterpret_cast<const float4*>(stage_f + r * 128 + c8 * 8);
-            const float4 a1 = *reinterpret_cast<const float4*>(stage_f + r * 128 + c8 * 8 + 4);
-            const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
-            uint32_t o[4];
+            for (int j = 0; j < 2; ++j) {
+              // (selects, not an index by the run-time block: registers)
+              if (et + 128 * j >= (mb == 0 ? npieces[0] : npieces[MBLK - 1])) break;
+              const int r = mb == 0 ? prow[0][j] : prow[MBLK - 1][j];
+              const int col = mb == 0 ? pcol[0][j] : pcol[MBLK - 1][j];
+              const int64_t row = n0 + c * static_cast<int>(kResRows) + r;
+              if (row >= n_rows) continue;
+              const uint4 rr = *reinterpret_cast<const uint4*>(win + r * 128 + col);
+              const float4 a0 = *reinterpret_cast<const float4*>(stage_f + r * 128 + col);
+              const float4 a1 = *reinterpret_cast<const float4*>(stage_f + r * 128 + col + 4);
+              const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+              const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
+              uint32_t o[4];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const float lo = apply_activation_bf16(x[2 * h] + __uint_as_float(rw[h] << 16), p.act);
-              const float hi = apply_activation_bf16(x[2 * h + 1] + __uint_as_float(rw[h] & 0xFFFF0000u), p.act);
-              const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
-              o[h] = *reinterpret_cast<const uint32_t*>(&pr);
+              for (int h = 0; h < 4; ++h) {
+                const float lo = activation_bf16<kA>(x[2 * h] + __uint_as_float(rw[h] << 16));
+                const float hi = activation_bf16<kA>(x[2 * h + 1] + __uint_as_float(rw[h] & 0xFFFF0000u));
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+                o[h] = *reinterpret_cast<const uint32_t*>(&pr);
+              }
+              *reinterpret_cast<uint4*>(out_bf + row * p.co + p.co_base + mb * 128 + col) =
+                  make_uint4(o[0], o[1], o[2], o[3]);
             }
-            *reinterpret_cast<uint4*>(out_bf + row * p.co + p.co_base + mb * 128 + c8 * 8) =
-                make_uint4(o[0], o[1], o[2], o[3]);
-          }
+          });
         }
         if (!epilogue_all(ok_res)) break;
       }

@@ -586,6 +586,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (c <= -2) return static_cast<int64_t>((-2 - c) >> 1);
       return -1;
     };
+    // This thread's 16-byte output pieces: (row, 8-channel column) of a
+    // 32-slot chunk (plain, up to four) or a 16-slot chunk (residual, up to
+    // two); the same in every chunk, so computed once.
+    int prow[4], pcol[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int q = et + 128 * j;
+      prow[j] = q / chunks_per_row;
+      pcol[j] = (q - prow[j] * chunks_per_row) * 8;
+    }
+    const int plain_pieces = 32 * chunks_per_row, res_pieces = static_cast<int>(kResChunk) * chunks_per_row;
     uint32_t res_phase = 0;  // bit b: the phase window b's barrier waits for next
     bool ok_res = true;
     uint32_t res_pending = 0;  // window loads issued and not yet waited for (bits)
@@ -636,7 +647,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tcol = tmem_base + ((sub * 32u) << 16) + buf * static_cast<uint32_t>(kTileN);
       if (fused) {
-        const int cpr = chunks_per_row;  // 16-byte pieces per row
         for (int c = 0; c < static_cast<int>(kTileN / kResChunk); ++c) {
           epi_bar();  // the previous chunk's rows have been stored
           if (c >= 1 && c + 1 < static_cast<int>(kTileN / kResChunk)) {
@@ -658,33 +668,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           res_pending &= ~(1u << wb);
           epi_bar();  // staged, and every thread saw the window land
           const __nv_bfloat16* win = window(c);
+          with_activation(p.act, [&](auto tag) {
+            constexpr int kA = decltype(tag)::value;
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int q = et + 128 * j;
-            if (q >= static_cast<int>(kResChunk) * cpr) break;
-            const int r = q / cpr;
-            const int c8 = q - r * cpr;
-            const int32_t code = codes_s[c * kResChunk + r];
-            if (code < 0 || code >= n_rows) continue;
-            const uint32_t o = rowoff_s[c * kResChunk + r];
-            const uint4 rr = o < kResChunk
-                                 ? *reinterpret_cast<const uint4*>(win + o * static_cast<uint32_t>(p.co) + c8 * 8)
-                                 : *reinterpret_cast<const uint4*>(p.residual + static_cast<int64_t>(code) * p.co + c8 * 8);
-            const float4 a0 = *reinterpret_cast<const float4*>(stage_f32 + r * 128 + c8 * 8);
-            const float4 a1 = *reinterpret_cast<const float4*>(stage_f32 + r * 128 + c8 * 8 + 4);
-            const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
-            uint32_t ow[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const float lo = apply_activation_bf16(x[2 * h] + __uint_as_float(rw[h] << 16), p.act);
-              const float hi = apply_activation_bf16(x[2 * h + 1] + __uint_as_float(rw[h] & 0xffff0000u), p.act);
-              const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
-              ow[h] = *reinterpret_cast<const uint32_t*>(&pr);
+            for (int j = 0; j < 2; ++j) {
+              if (et + 128 * j >= res_pieces) break;
+              const int r = prow[j], col = pcol[j];
+              const int32_t code = codes_s[c * kResChunk + r];
+              if (code < 0 || code >= n_rows) continue;
+              const uint32_t o = rowoff_s[c * kResChunk + r];
+              const uint4 rr = o < kResChunk
+                                   ? *reinterpret_cast<const uint4*>(win + o * static_cast<uint32_t>(p.co) + col)
+                                   : *reinterpret_cast<const uint4*>(p.residual + static_cast<int64_t>(code) * p.co + col);
+              const float4 a0 = *reinterpret_cast<const float4*>(stage_f32 + r * 128 + col);
+              const float4 a1 = *reinterpret_cast<const float4*>(stage_f32 + r * 128 + col + 4);
+              const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+              const uint32_t rw[4] = {rr.x, rr.y, rr.z, rr.w};
+              uint32_t ow[4];
+  #pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const float lo = activation_bf16<kA>(x[2 * h] + __uint_as_float(rw[h] << 16));
+                const float hi = activation_bf16<kA>(x[2 * h + 1] + __uint_as_float(rw[h] & 0xffff0000u));
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+                ow[h] = *reinterpret_cast<const uint32_t*>(&pr);
+              }
+              *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(code) * p.co + col) =
+                  make_uint4(ow[0], ow[1], ow[2], ow[3]);
             }
-            *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(code) * p.co + c8 * 8) =
-                make_uint4(ow[0], ow[1], ow[2], ow[3]);
-          }
+          });
         }
       } else {
         for (int vc = 0; vc < kTileN / 32; ++vc) {
@@ -694,18 +705,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           if (co_l < p.co_count) {
             const float b = bias_s[co_l];
+            with_activation(p.act, [&](auto tag) {
+              constexpr int kA = decltype(tag)::value;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              stage_out[i * 128 + co_l] = __float2bfloat16_rn(apply_activation_bf16(__uint_as_float(v[i]) + b, p.act));
+              for (int i = 0; i < 32; ++i)
+                stage_out[i * 128 + co_l] = __float2bfloat16_rn(activation_bf16<kA>(__uint_as_float(v[i]) + b));
+            });
           }
           epi_bar();  // staged
-          for (int q = et; q < 32 * chunks_per_row; q += 128) {
-            const int r = q / chunks_per_row;
-            const int c8 = q - r * chunks_per_row;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (et + 128 * j >= plain_pieces) break;
+            const int r = prow[j], col = pcol[j];
             const int32_t code = codes_s[vc * 32 + r];
             if (code >= 0 && code < n_rows)
-              *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(code) * p.co + c8 * 8) =
-                  *reinterpret_cast<const uint4*>(stage_out + r * 128 + c8 * 8);
+              *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(code) * p.co + col) =
+                  *reinterpret_cast<const uint4*>(stage_out + r * 128 + col);
           }
         }
       }
