@@ -71,6 +71,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-epilogue", action="store_true",
                     help="skip timing the fused residual + SiLU epilogue against the plain conv")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip timing the input and weight gradients on the same map")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="approximate CPU work of the oracle baseline sample")
     ap.add_argument("--materialized", action="store_true",
@@ -741,6 +743,32 @@ def run_ours(args):
         del res, out2
         torch.cuda.empty_cache()
 
+    # ---- backward on the same map, outside the timed region: the input
+    # gradient (over the x-run layout when the step uses it) and the weight
+    # gradient, with this step's output standing in for dout
+    backward = None
+    if not args.no_backward and dtype == "bf16":
+        dout = out.clone()
+        din = torch.empty_like(feats)
+
+        xrun_dgrad = xrun is not None and co == 128  # the x-run input gradient reduces 128 channels
+
+        def dgrad():
+            if xrun_dgrad:
+                sv.submconv3d_dgrad_xrun(dout, nmap, xrun["slots"], xrun["count"], w, out=din)
+            else:
+                sv.submconv3d_dgrad(dout, nmap, w, out=din)
+
+        dg_ms = time_calls(torch, dgrad, stream, reps=3, warmup=1)
+        wg_ms = time_calls(torch, lambda: sv.submconv3d_wgrad(feats, dout, nmap), stream, reps=3, warmup=1)
+        sv.device_status()
+        backward = {"dgrad_ms": dg_ms, "dgrad_tflops": flops / (dg_ms * 1e-3) / 1e12,
+                    "dgrad_kernel": XRUN_KERNEL if xrun_dgrad else DOMINANT_KERNEL,
+                    "wgrad_ms": wg_ms, "wgrad_tflops": flops / (wg_ms * 1e-3) / 1e12,
+                    "wgrad_kernel": "wgrad_tc_kernel", "note": "2*valid_pairs*Ci*Co FLOPs each"}
+        del dout, din
+        torch.cuda.empty_cache()
+
     # ---- end to end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
@@ -901,6 +929,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         **({"epilogue": epilogue} if epilogue is not None else {}),
+        **({"backward": backward} if backward is not None else {}),
         # per step: the map build's seven kernels (flag reset, range/order/box
         # check, clear, insert, dense-row query, row-hash query, voxel-hash
         # query: the paths not taken return at once) and one conv launch
