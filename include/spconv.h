@@ -102,11 +102,14 @@ size_t spconv_build_nmap_workspace_size(int64_t N);
  * The call enqueues its kernels and then waits for the stream once to read
  * the error flags, so it cannot be captured into a CUDA graph.  A first
  * kernel checks the coordinate range and whether the coordinates are
- * strictly increasing in (z, y, x) order; the device then takes one of two
- * paths (the other path's kernels return at once).  Strictly increasing
- * input, as a voxeliser emits it, builds a hash of (z, y) rows and finds
- * neighbours by searching rows; any other order builds a hash of voxels.
- * Both give the same map.  Returns SPCONV_ERR_DUPLICATE_COORD if two
+ * strictly increasing in (z, y, x) order and finds their bounding box; the
+ * device then takes one of three paths (the other paths' kernels return at
+ * once).  Strictly increasing input, as a voxeliser emits it, whose box's
+ * rows fit the workspace lays the box out as words of 32 cells (an
+ * occupancy bit per cell and the index of the word's first voxel), so a
+ * neighbour is one word load; other strictly increasing input builds a
+ * hash of (z, y) rows and finds neighbours by searching rows; any other
+ * order builds a hash of voxels.  All give the same map.  Returns SPCONV_ERR_DUPLICATE_COORD if two
  * voxels share a coordinate and SPCONV_ERR_INVALID_ARG if a coordinate is
  * out of range; nmap is then undefined.
  */
