@@ -517,58 +517,58 @@ __global__ void __launch_bounds__(kThreads, 1)
             rslot ^= 1u;
             if (rslot == 0) rphase ^= 1u;
           }
-          continue;
-        }
-        for (int c = 0; c < p.num_chunks && ok; c += p.cps) {
-          for (int sub = 0; sub < p.cps; ++sub) {  // the stage's chunks, one weight block each
-            const uint32_t part = kSplit ? stage * 2u + static_cast<uint32_t>(sub) : stage;
-            const uint32_t fullb = smem_addr(&full[part]);
-            if (kSplit || sub == 0) {
-              if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&empty[part]), st_phase ^ 1))) {
-                ok = false;
-                break;
-              }
-              if (lane == 0) {
-                if (sub == 0) {
-                  // MMAs per part
-                  const int steps =
-                      (p.cps / static_cast<int>(parts)) * (min(kChunkE, p.ci - c * kChunkE) / kKPerMmaE);
-                  meta[stage] = (static_cast<uint32_t>(steps) << 8) | (issued ? 0u : kMetaFirst);
+        } else {
+          for (int c = 0; c < p.num_chunks && ok; c += p.cps) {
+            for (int sub = 0; sub < p.cps; ++sub) {  // the stage's chunks, one weight block each
+              const uint32_t part = kSplit ? stage * 2u + static_cast<uint32_t>(sub) : stage;
+              const uint32_t fullb = smem_addr(&full[part]);
+              if (kSplit || sub == 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&empty[part]), st_phase ^ 1))) {
+                  ok = false;
+                  break;
                 }
-                mbar_arrive_expect_tx(fullb, p.w_bytes / parts);
+                if (lane == 0) {
+                  if (sub == 0) {
+                    // MMAs per part
+                    const int steps =
+                        (p.cps / static_cast<int>(parts)) * (min(kChunkE, p.ci - c * kChunkE) / kKPerMmaE);
+                    meta[stage] = (static_cast<uint32_t>(steps) << 8) | (issued ? 0u : kMetaFirst);
+                  }
+                  mbar_arrive_expect_tx(fullb, p.w_bytes / parts);
+                }
+                ++fills;
               }
-              ++fills;
-            }
-            __syncwarp();
-            // With two parts MBLK is 1, so the part's block is `sub`; with one
-            // part, the M blocks are side by side.
-            if constexpr (kTf32) {
-              // tf32 input gradient: rows of w[K-1-k] (output channel =
-              // forward ci) with 32 of their forward-co entries each, K-major
-              if (static_cast<int>(lane) < MBLK) {
+              __syncwarp();
+              // With two parts MBLK is 1, so the part's block is `sub`; with one
+              // part, the M blocks are side by side.
+              if constexpr (kTf32) {
+                // tf32 input gradient: rows of w[K-1-k] (output channel =
+                // forward ci) with 32 of their forward-co entries each, K-major
+                if (static_cast<int>(lane) < MBLK) {
+                  const int mb = static_cast<int>(lane);
+                  tma_load_3d(smem_addr(smem + stage * p.stage_bytes) + mb * kWBlockBytes, &tm_w,
+                              c * kChunkE, p.co_base + mb * 128, k_count - 1 - kk, fullb);
+                }
+              } else if constexpr (!kDgrad) {
+                // forward: w[k] channel-major, two 64-channel boxes per M block
+                if (static_cast<int>(lane) < 2 * MBLK) {
+                  const int mb = static_cast<int>(lane) >> 1, half = static_cast<int>(lane) & 1;
+                  tma_load_3d(smem_addr(smem + stage * p.stage_bytes) + (sub + mb) * kWBlockBytes + half * 8192u,
+                              &tm_w, p.co_base + mb * 128 + half * 64, (c + sub) * kChunk, kk, fullb);
+                }
+              } else if (static_cast<int>(lane) < MBLK) {
+                // input gradient: rows of w[K-1-k] (output channel = forward ci)
+                // with 64 of their forward-co entries each, K-major
                 const int mb = static_cast<int>(lane);
-                tma_load_3d(smem_addr(smem + stage * p.stage_bytes) + mb * kWBlockBytes, &tm_w,
-                            c * kChunkE, p.co_base + mb * 128, k_count - 1 - kk, fullb);
+                tma_load_3d(smem_addr(smem + stage * p.stage_bytes) + (sub + mb) * kWBlockBytes, &tm_w,
+                            (c + sub) * kChunk, p.co_base + mb * 128, k_count - 1 - kk, fullb);
               }
-            } else if constexpr (!kDgrad) {
-              // forward: w[k] channel-major, two 64-channel boxes per M block
-              if (static_cast<int>(lane) < 2 * MBLK) {
-                const int mb = static_cast<int>(lane) >> 1, half = static_cast<int>(lane) & 1;
-                tma_load_3d(smem_addr(smem + stage * p.stage_bytes) + (sub + mb) * kWBlockBytes + half * 8192u,
-                            &tm_w, p.co_base + mb * 128 + half * 64, (c + sub) * kChunk, kk, fullb);
-              }
-            } else if (static_cast<int>(lane) < MBLK) {
-              // input gradient: rows of w[K-1-k] (output channel = forward ci)
-              // with 64 of their forward-co entries each, K-major
-              const int mb = static_cast<int>(lane);
-              tma_load_3d(smem_addr(smem + stage * p.stage_bytes) + (sub + mb) * kWBlockBytes, &tm_w,
-                          (c + sub) * kChunk, p.co_base + mb * 128, k_count - 1 - kk, fullb);
             }
-          }
-          issued = true;
-          if (++stage == S) {
-            stage = 0;
-            st_phase ^= 1;
+            issued = true;
+            if (++stage == S) {
+              stage = 0;
+              st_phase ^= 1;
+            }
           }
         }
       }
