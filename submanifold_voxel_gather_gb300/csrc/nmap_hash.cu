@@ -5,9 +5,9 @@
 // and N where there is none (wrapper docstring, kernel body); it takes the
 // map as given.  This file builds it.  A first pass checks the coordinate
 // range and whether the coordinates are strictly increasing in (z, y, x)
-// order, and counts the (z, y) rows.  The rest of the build takes one of two
-// paths, chosen on the device from that verdict (every kernel of the other
-// path returns at once):
+// order, counts the (z, y) rows and finds the bounding box.  The rest of the
+// build takes one of three paths, chosen on the device from that verdict
+// (every kernel of the other paths returns at once):
 //
 // Sorted input whose bounding box is small enough (the usual case: a
 // voxeliser emits sorted coordinates in a bounded grid).  The voxels of 32
