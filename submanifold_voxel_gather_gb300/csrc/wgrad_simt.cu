@@ -114,6 +114,49 @@ __global__ void __launch_bounds__(kThreads)
   atomicAdd(dbias + c, s);
 }
 
+// dbias[co] = sum_n dout[n, co], vectorised: a CTA sums a slab of kDbRows
+// rows; each thread takes one 16-byte piece (kVec channels) of every
+// (kThreads / pieces)-th row, so a warp reads whole rows, coalesced, with
+// many independent loads in flight; the CTA combines its threads' partial
+// sums in shared memory and adds one value per channel with an atomic.
+// (The per-column loop above reads 2 bytes a thread per row, one row after
+// another: at 1.0 M rows x 128 channels it took ~0.9 ms, longer than the
+// weight gradient itself.)
+constexpr int64_t kDbRows = 4096;
+
+template <typename T, int kVec>
+__global__ void __launch_bounds__(kThreads)
+    dbias_vec_kernel(const T* __restrict__ dout, float* __restrict__ dbias, int64_t n, int32_t co) {
+  __shared__ float part[kThreads * kVec];
+  const int pieces = co / kVec;  // <= kThreads (checked by the launcher)
+  const int rps = kThreads / pieces;
+  const int t = static_cast<int>(threadIdx.x);
+  const int g = t % pieces, r0 = t / pieces;
+  float acc[kVec];
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) acc[j] = 0.0f;
+  if (r0 < rps) {
+    const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kDbRows;
+    const int64_t v1 = v0 + kDbRows < n ? v0 + kDbRows : n;
+#pragma unroll 4
+    for (int64_t v = v0 + r0; v < v1; v += rps) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(dout + v * co) + g);
+      const T* e = reinterpret_cast<const T*>(&q);
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) acc[j] += widen(e[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) part[t * kVec + j] = acc[j];
+  __syncthreads();
+  for (int c = t; c < co; c += kThreads) {
+    const int gc = c / kVec, j = c - gc * kVec;
+    float s = 0.0f;
+    for (int r = 0; r < rps; ++r) s += part[(r * pieces + gc) * kVec + j];
+    atomicAdd(dbias + c, s);
+  }
+}
+
 template <typename T>
 spconv_status launch_typed(const T* feats, const T* dout, const int32_t* nmap, float* dw, float*,
                            int64_t n, int32_t k, int32_t ci, int32_t co, cudaStream_t stream) {
@@ -138,6 +181,20 @@ spconv_status launch_dbias(spconv_dtype dtype, const void* dout, float* dbias, i
   if (!cuda_ok(cudaMemsetAsync(dbias, 0, static_cast<size_t>(co) * sizeof(float), stream),
                "cudaMemsetAsync(dbias)", &st))
     return st;
+  const size_t esz = dtype == SPCONV_BF16 ? 2u : 4u;
+  const int vec = static_cast<int>(16u / esz);
+  if (co % vec == 0 && co / vec <= kThreads && reinterpret_cast<uintptr_t>(dout) % 16u == 0u) {
+    const int64_t blocks = (n + kDbRows - 1) / kDbRows;
+    if (blocks > 0x7fffffff) return fail(SPCONV_ERR_UNSUPPORTED, "problem too large for the dbias grid");
+    if (dtype == SPCONV_BF16)
+      dbias_vec_kernel<__nv_bfloat16, 8><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(dout), dbias, n, co);
+    else
+      dbias_vec_kernel<float, 4><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+          static_cast<const float*>(dout), dbias, n, co);
+    if (!cuda_ok(cudaGetLastError(), "dbias_vec_kernel launch", &st)) return st;
+    return SPCONV_OK;
+  }
   const int64_t slices = (n + kSlice - 1) / kSlice;
   if (slices > 65535) return fail(SPCONV_ERR_UNSUPPORTED, "problem too large for the dbias grid");
   const dim3 grid((co + kThreads - 1) / kThreads, static_cast<unsigned>(slices));
